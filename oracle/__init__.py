@@ -1,0 +1,16 @@
+"""CPU oracle for the whole-stack small-batch decode step.
+
+TEST INFRASTRUCTURE ONLY. It exists to check the CUDA megakernel, and only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may
+import it. The product package never imports it and it never imports the product package; the two
+share only the seeded inputs drawn by ``synthetic``.
+
+Everything is numpy in float64: activations, accumulations, the recurrent state. Weights are the
+bf16-rounded draws (exact in float64); NVFP4 weights are decoded exactly as e2m1 * e4m3 * fp32.
+The KV cache and the MLA latent cache hold bf16-rounded values, because bf16 is the cache's storage
+format in this design (the rounding is part of what the step computes, not an implementation detail).
+
+Parity status of each function is recorded in its docstring; the pins live in tests/test_oracle_*.py.
+"""
+from .model import Oracle  # noqa: F401
+from . import ops  # noqa: F401
