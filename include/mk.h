@@ -1,0 +1,199 @@
+/*
+ * mk.h — C ABI of the GB300 whole-model decode megakernel (libmk.so).
+ *
+ * One decode step of a whole decoder stack runs as ONE persistent CUDA kernel launch with one CTA per
+ * SM: embedding, every layer's RMSNorm, projections, attention (GQA or MLA) or delta-rule recurrence
+ * (gated delta net or KDA), SwiGLU feed-forward or MoE (router, shared and routed experts), residual,
+ * final norm, LM head and greedy argmax. Weight loads run ahead of compute across op and layer
+ * boundaries through a shared-memory ring. The design follows the pages' megakernel idea — one
+ * program for the whole layer stack, with a weight load issued as early as on-chip storage allows
+ * instead of at the start of the op that uses it (Kimi K3's TPU megakernel, "What a megakernel is,
+ * and what it fixes on a TPU"; tpu-megakernels README, intro) — re-designed for one GB300.
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device pointers on the handle's device; "host" pointers are
+ *     ordinary (pageable or pinned) host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Device work is
+ *     enqueued on it and the call returns without waiting, unless the call says otherwise.
+ *   - Host-side argument errors are returned at once and enqueue nothing. Errors found on the device
+ *     (a token id outside [0, vocab), a position outside the sequence's valid window, a watchdog
+ *     timeout of an inter-SM wait) are recorded in the handle's device status word, the kernel exits
+ *     early, and mk_get_status() reports them.
+ *   - A handle is not thread-safe: calls on one handle must come from one host thread at a time and
+ *     must use streams that are ordered with each other.
+ *   - No call falls back to the CPU and no call takes PyTorch types.
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_MAX_LAYERS 128
+
+typedef enum mk_status {
+  MK_OK = 0,
+  MK_ERR_INVALID_ARG = 1,  /* a host-side argument is out of range or inconsistent            */
+  MK_ERR_UNSUPPORTED = 2,  /* shape or feature this build does not implement                   */
+  MK_ERR_NOMEM = 3,        /* cudaMalloc failed                                                 */
+  MK_ERR_CUDA = 4,         /* a CUDA runtime call failed (see mk_last_error)                   */
+  MK_ERR_TIMEOUT = 5,      /* device watchdog: an inter-SM wait exceeded its time limit         */
+  MK_ERR_DEVICE = 6        /* device-side input check failed (token id, position window)        */
+} mk_status;
+
+typedef enum mk_mixer {
+  MK_MIXER_GQA = 0, /* grouped-query softmax attention over a bf16 KV cache, RoPE               */
+  MK_MIXER_GDN = 1, /* gated delta net: one sigmoid decay per head, fp32 state [dk x dv]/head    */
+  MK_MIXER_KDA = 2, /* Kimi delta attention: one sigmoid decay per key channel                   */
+  MK_MIXER_MLA = 3  /* multi-head latent attention, absorbed form, bf16 latent cache              */
+} mk_mixer;
+
+typedef enum mk_ffn { MK_FFN_DENSE = 0, MK_FFN_MOE = 1 } mk_ffn;
+typedef enum mk_expert_format { MK_FMT_BF16 = 0, MK_FMT_NVFP4 = 1 } mk_expert_format;
+
+/* Model shape. Every layer is  x += Mixer(RMSNorm(x)); x += FFN(RMSNorm(x))  (pre-norm, no biases),
+ * then a final RMSNorm and the LM head. RMSNorm gains multiply. */
+typedef struct mk_model_desc {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t vocab;
+  int32_t tied_embedding;          /* 1: the LM head is the embedding matrix                   */
+  float norm_eps;                  /* RMSNorm epsilon (also used for the MLA c_q / c_kv norms) */
+  float rope_theta;                /* rotate-half RoPE base                                    */
+  int32_t mixer[MK_MAX_LAYERS];    /* mk_mixer per layer                                      */
+  /* GQA */
+  int32_t n_q_heads, n_kv_heads, head_dim;
+  /* GDN / KDA */
+  int32_t lin_heads, lin_dk, lin_dv;
+  /* MLA */
+  int32_t mla_heads, q_lora, kv_lora, qk_nope, qk_rope, v_head;
+  /* FFN */
+  int32_t ffn_kind;                /* mk_ffn                                                    */
+  int32_t ffn_dim;                 /* dense SwiGLU hidden size                                 */
+  int32_t n_experts, top_k, n_shared, expert_dim, expert_format;
+  float route_scale;               /* routed weights = route_scale * s_sel / sum(s_sel)         */
+  /* capacity of the handle */
+  int32_t max_batch;               /* sequences per call                                       */
+  int32_t max_rows;                /* query rows per sequence per call (8 for speculative verify)*/
+  int32_t max_ctx;                 /* positions per sequence (KV / latent cache length)         */
+} mk_model_desc;
+
+/* Device pointers of one layer's weights. bf16 matrices are row-major [out, in] (the input
+ * dimension contiguous) unless stated. Unused entries are NULL. */
+typedef struct mk_layer_weights {
+  const void* attn_norm;           /* bf16 [d]                                                 */
+  const void* ffn_norm;            /* bf16 [d]                                                 */
+  /* GQA: wq [Hq*hd, d], wk/wv [Hkv*hd, d], wo [d, Hq*hd]
+   * GDN/KDA: wq/wk [H*dk, d], wv [H*dv, d], wa [H, d] (GDN) or [H*dk, d] (KDA), wb [H, d],
+   *          wo [d, H*dv]
+   * MLA: wo [d, H*v_head] */
+  const void *wq, *wk, *wv, *wo, *wa, *wb;
+  /* MLA: w_dq [q_lora, d], q_norm [q_lora], w_uq [H*(nope+rope), q_lora] (per head: nope then rope),
+   *      w_dkv [kv_lora+rope, d] (latent then rope key), kv_norm [kv_lora],
+   *      w_uk [H, kv_lora, nope] (k_nope = w_uk[h]^T c;  absorbed query = w_uk[h] q_nope),
+   *      w_uv [H, v_head, kv_lora] (v = w_uv[h] c) */
+  const void *w_dq, *q_norm, *w_uq, *w_dkv, *kv_norm, *w_uk, *w_uv;
+  /* dense SwiGLU: w_gate/w_up [F, d], w_down [d, F] */
+  const void *w_gate, *w_up, *w_down;
+  /* MoE: w_router bf16 [E, d]; router_bias fp32 [E] (may be NULL = zero bias)
+   * routed experts e_gate/e_up [E, F, d], e_down [E, d, F]; shared s_gate/s_up [S, F, d],
+   * s_down [S, d, F]. bf16: the pointers are bf16 tensors and the *_scales / *_gscale entries are
+   * NULL. NVFP4: the pointers are packed e2m1 codes (uint8, 2 per byte, element 2i in the low
+   * nibble, [.., in/2]), *_scales are e4m3 block scales (uint8 [.., in/16], one per 16 inputs) and
+   * *_gscale are fp32 per-expert tensor scales [E] or [S]; w = e2m1 * e4m3 * gscale. */
+  const void* w_router;
+  const float* router_bias;
+  const void *e_gate, *e_up, *e_down, *s_gate, *s_up, *s_down;
+  const uint8_t *e_gate_scales, *e_up_scales, *e_down_scales;
+  const uint8_t *s_gate_scales, *s_up_scales, *s_down_scales;
+  const float *e_gate_gscale, *e_up_gscale, *e_down_gscale;
+  const float *s_gate_gscale, *s_up_gscale, *s_down_gscale;
+} mk_layer_weights;
+
+typedef struct mk_weights {
+  const void* embed;       /* bf16 [vocab, d]                                              */
+  const void* final_norm;  /* bf16 [d]                                                     */
+  const void* lm_head;     /* bf16 [vocab, d]; NULL when tied_embedding                    */
+  mk_layer_weights layers[MK_MAX_LAYERS];
+} mk_weights;
+
+typedef struct mk_handle mk_handle;
+
+/* Read-only facts about a handle (for harnesses and byte accounting). */
+typedef struct mk_info {
+  int32_t n_sm;             /* CTAs per launch = SMs of the device                          */
+  int32_t threads_per_cta;
+  int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
+  int32_t ring_slots;       /* weight-ring slots per SM                                     */
+  int32_t ring_slot_bytes;
+  int32_t n_ops_last;       /* ops in the program of the last step                          */
+  int64_t device_bytes;     /* device memory owned by the handle                            */
+} mk_info;
+
+/* Creates a handle on `device`. The caller keeps ownership of every weight buffer and must keep
+ * them alive and unchanged until mk_destroy. The handle allocates (cudaMalloc) and owns the KV /
+ * latent caches, the recurrent states, activation scratch, instruction queues, counters and the
+ * status word. Synchronous. Errors: MK_ERR_INVALID_ARG (inconsistent shape, missing weight,
+ * alignment: every weight must be 16-byte aligned and every inner dimension a multiple of 8),
+ * MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA. */
+mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int device, mk_handle** out);
+
+/* Fills the caches and recurrent states of sequences 0..batch-1 from a context of n_tokens tokens
+ * each (device int32 [batch, n_tokens], row-major), discarding whatever they held. Afterwards each
+ * sequence has n_tokens committed tokens and the next mk_decode_step must pass positions[b] =
+ * n_tokens. Runs ceil(n_tokens / max_rows) launches of the decode kernel with all rows accepted and
+ * no LM head. Asynchronous on `stream`; `tokens` must stay valid until the work completes.
+ * Errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch, n_tokens outside 1..max_ctx). */
+mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_tokens, void* stream);
+
+/* One decode (rows = 1) or speculative-verify (rows = 2..max_rows) step for `batch` sequences.
+ *   tokens     device int32 [batch * rows]: row r of sequence b at index b*rows + r
+ *   positions  device int32 [batch]: position of row 0 of each sequence. Sequence b has c_b committed
+ *              tokens and u_b pending rows from its previous call (u_b = 0 after a prefill). The call
+ *              commits the first positions[b] - c_b pending rows and drops the rest, so
+ *              c_b <= positions[b] <= c_b + u_b is required (verify: positions advance by the accepted
+ *              length). Row r sits at position positions[b] + r and attends causally to positions
+ *              0 .. positions[b] + r; recurrent layers advance their state row by row.
+ *              After the call c_b = positions[b] and u_b = rows.
+ *   logits_out device fp32 [batch * rows, vocab] or NULL (no logits written)
+ *   argmax_out device int32 [batch * rows] or NULL: greedy token per row (lowest index on ties)
+ * The verify semantics follow the pages' speculative step: an anchor plus seven drafts are checked
+ * as eight rows of one sequence and only the accepted prefix is kept (Kimi K3's TPU megakernel,
+ * "What DSpark changes per step").
+ * One kernel launch. Asynchronous. Host errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch,
+ * rows outside 1..max_rows, both outputs NULL). Device errors via mk_get_status: MK_ERR_DEVICE
+ * (token outside [0, vocab), position outside the window, positions[b] + rows > max_ctx; the step is
+ * then skipped and no state changes), MK_ERR_TIMEOUT. */
+mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch,
+                         int rows, float* logits_out, int32_t* argmax_out, void* stream);
+
+/* The same step from HOST buffers: copies tokens_host [batch*rows] and positions_host [batch] to
+ * handle-owned device staging, runs the step, copies the greedy tokens back to argmax_host
+ * [batch*rows] (and, when logits_host is not NULL, the logits [batch*rows, vocab]), and waits for
+ * `stream`. Returns the device status of the step as mk_get_status would. */
+mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const int32_t* positions_host,
+                              int batch, int rows, float* logits_host, int32_t* argmax_host, void* stream);
+
+/* Waits for `stream`, returns the device status word of the work enqueued so far and clears it.
+ * After MK_ERR_TIMEOUT the handle's inter-SM counters are reset so it can be used again (the state
+ * of the interrupted step is undefined: run mk_prefill_kv again). */
+mk_status mk_get_status(mk_handle* h, void* stream);
+
+/* Human-readable description of the last error on this handle ("" if none). Owned by the handle. */
+const char* mk_last_error(const mk_handle* h);
+
+/* Fills `out`. */
+mk_status mk_get_info(const mk_handle* h, mk_info* out);
+
+/* Synchronises the device, frees everything the handle owns. NULL is ignored. */
+void mk_destroy(mk_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H_ */
