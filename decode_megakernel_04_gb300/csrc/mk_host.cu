@@ -1,0 +1,733 @@
+// Host side of libmk: the C ABI (include/mk.h), the device memory plan of a handle, and the scheduler
+// that compiles one decode step of the layer stack into per-SM instruction queues for the persistent
+// kernel (mk_kernel.cu).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+size_t kernel_smem_bytes();
+cudaError_t kernel_configure();
+cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream);
+cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream);
+cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t stream);
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+struct Program {
+  int B = 0, R = 0;
+  bool head = false;  // LM head + argmax partials
+  OpDesc* d_ops = nullptr;
+  Instr* d_instr = nullptr;
+  int32_t* d_qoff = nullptr;
+  int n_ops = 0;
+  int n_instr = 0;
+};
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+struct mk_handle {
+  mk_model_desc desc{};
+  mk_weights w{};
+  int device = 0;
+  int n_sm = 0;
+  std::string err;
+  std::vector<void*> allocs;
+  int64_t bytes = 0;
+  uint32_t epoch = 0;
+
+  // per-layer slot among layers of the same kind
+  std::vector<int> slot;
+  int n_gqa = 0, n_delta = 0, n_mla = 0;
+
+  int nmax = 0;
+  int proj_stride = 0, attn_stride = 0, hbuf_stride = 0;
+  float* x = nullptr;
+  float* proj = nullptr;
+  float* attn_out = nullptr;
+  float* hbuf = nullptr;
+  float* ssq = nullptr;
+  float2* amax_part = nullptr;
+  float* attn_part = nullptr;
+  int attn_part_stride = 0;
+  uint16_t* kcache = nullptr;
+  uint16_t* vcache = nullptr;
+  float* state = nullptr;
+  float* pend = nullptr;
+  int pend_rec = 0;
+  uint32_t* counters = nullptr;
+  uint32_t* arrive = nullptr;
+  int32_t* status = nullptr;
+  int32_t* abort_flag = nullptr;
+  SeqState* seq = nullptr;
+  float2* rope = nullptr;
+  int rot_dim = 0;
+  int32_t* pos_buf = nullptr;
+  int32_t* stage_tok = nullptr;
+  int32_t* stage_pos = nullptr;
+  int32_t* stage_argmax = nullptr;
+  float* stage_logits = nullptr;
+  int max_ops = 0;
+  int n_ops_last = 0;
+  std::vector<Program> programs;
+};
+
+namespace {
+
+mk_status fail(mk_handle* h, mk_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  return s;
+}
+
+mk_status cuda_fail(mk_handle* h, cudaError_t e, const char* what) {
+  return fail(h, e == cudaErrorMemoryAllocation ? MK_ERR_NOMEM : MK_ERR_CUDA, "%s: %s", what,
+              cudaGetErrorString(e));
+}
+
+template <typename T>
+mk_status dev_alloc(mk_handle* h, T** out, size_t count, const char* what) {
+  void* p = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return cuda_fail(h, e, what);
+  e = cudaMemset(p, 0, bytes);
+  if (e != cudaSuccess) return cuda_fail(h, e, what);
+  h->allocs.push_back(p);
+  h->bytes += (int64_t)bytes;
+  *out = reinterpret_cast<T*>(p);
+  return MK_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_delta(int m) { return m == MK_MIXER_GDN || m == MK_MIXER_KDA; }
+
+int delta_proj_cols(const mk_model_desc& d, int mixer) {
+  const int H = d.lin_heads;
+  return 2 * H * d.lin_dk + H * d.lin_dv + (mixer == MK_MIXER_KDA ? H * d.lin_dk : H) + H;
+}
+
+mk_status check_desc(mk_handle* h, const mk_model_desc& d, const mk_weights& w) {
+  if (d.n_layers < 1 || d.n_layers > MK_MAX_LAYERS) return fail(h, MK_ERR_INVALID_ARG, "n_layers %d", d.n_layers);
+  if (d.d_model < 8 || d.d_model % 8) return fail(h, MK_ERR_INVALID_ARG, "d_model %d must be a multiple of 8", d.d_model);
+  if (d.vocab < 1) return fail(h, MK_ERR_INVALID_ARG, "vocab %d", d.vocab);
+  if (d.max_batch < 1 || d.max_rows < 1 || d.max_rows > kMaxRows || d.max_batch * d.max_rows > kMaxN)
+    return fail(h, MK_ERR_UNSUPPORTED, "max_batch*max_rows must be <= %d and max_rows <= %d", kMaxN, kMaxRows);
+  if (d.max_ctx < d.max_rows) return fail(h, MK_ERR_INVALID_ARG, "max_ctx %d", d.max_ctx);
+  if (!w.embed || !w.final_norm || (!d.tied_embedding && !w.lm_head))
+    return fail(h, MK_ERR_INVALID_ARG, "embed / final_norm / lm_head missing");
+  if (!aligned16(w.embed) || !aligned16(w.final_norm) || (w.lm_head && !aligned16(w.lm_head)))
+    return fail(h, MK_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+  for (int i = 0; i < d.n_layers; ++i) {
+    const mk_layer_weights& L = w.layers[i];
+    const int m = d.mixer[i];
+    auto need = [&](const void* p, const char* name) -> mk_status {
+      if (!p) return fail(h, MK_ERR_INVALID_ARG, "layer %d: %s missing", i, name);
+      if (!aligned16(p)) return fail(h, MK_ERR_INVALID_ARG, "layer %d: %s not 16-byte aligned", i, name);
+      return MK_OK;
+    };
+    mk_status s;
+#define NEED(p) if ((s = need(L.p, #p)) != MK_OK) return s
+    NEED(attn_norm);
+    NEED(ffn_norm);
+    if (m == MK_MIXER_GQA) {
+      NEED(wq); NEED(wk); NEED(wv); NEED(wo);
+      if (d.n_kv_heads < 1 || d.n_q_heads % d.n_kv_heads)
+        return fail(h, MK_ERR_INVALID_ARG, "n_q_heads must be a multiple of n_kv_heads");
+      if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256)
+        return fail(h, MK_ERR_UNSUPPORTED, "head_dim %d (64, 128 or 256)", d.head_dim);
+      if (d.n_q_heads / d.n_kv_heads > 8) return fail(h, MK_ERR_UNSUPPORTED, "more than 8 q heads per kv head");
+    } else if (is_delta(m)) {
+      NEED(wq); NEED(wk); NEED(wv); NEED(wo); NEED(wa); NEED(wb);
+      if (d.lin_dk != 32 && d.lin_dk != 64 && d.lin_dk != 128)
+        return fail(h, MK_ERR_UNSUPPORTED, "lin_dk %d (32, 64 or 128)", d.lin_dk);
+      if (d.lin_dv % 8) return fail(h, MK_ERR_UNSUPPORTED, "lin_dv %d must be a multiple of 8", d.lin_dv);
+    } else if (m == MK_MIXER_MLA) {
+      return fail(h, MK_ERR_UNSUPPORTED, "layer %d: MLA is not built in this version", i);
+    } else {
+      return fail(h, MK_ERR_INVALID_ARG, "layer %d: mixer %d", i, m);
+    }
+    if (d.ffn_kind == MK_FFN_DENSE) {
+      NEED(w_gate); NEED(w_up); NEED(w_down);
+      if (d.ffn_dim < 8 || d.ffn_dim % 8) return fail(h, MK_ERR_INVALID_ARG, "ffn_dim %d", d.ffn_dim);
+    } else {
+      return fail(h, MK_ERR_UNSUPPORTED, "MoE is not built in this version");
+    }
+#undef NEED
+  }
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// scheduler
+// ------------------------------------------------------------------------------------------------
+struct Builder {
+  int n_sm;
+  std::vector<OpDesc> ops;
+  std::vector<std::vector<Instr>> q;
+  explicit Builder(int n) : n_sm(n), q(n) {}
+
+  int add(OpDesc d) {
+    const int idx = (int)ops.size();
+    if (idx > 0 && d.n_deps == 0) {
+      d.n_deps = 1;
+      d.deps[0] = idx - 1;
+    }
+    ops.push_back(d);
+    return idx;
+  }
+  void place(int op, int sm, int a, int b, int c) {
+    Instr in;
+    in.op = op;
+    in.a = a;
+    in.b = b;
+    in.c = c;
+    q[sm].push_back(in);
+    ops[op].n_instr += 1;
+  }
+};
+
+OpDesc blank(int type) {
+  OpDesc d;
+  std::memset(&d, 0, sizeof(d));
+  d.type = type;
+  d.layer = -1;
+  d.passes = 1;
+  return d;
+}
+
+// one instruction per SM over a balanced range of output rows
+void gemv_op(Builder& bld, OpDesc d, int N) {
+  d.type = OP_GEMV;
+  d.rg = (N <= 4) ? 16 : 8;
+  d.passes = (N <= 8) ? 1 : (N + 7) / 8;
+  const int op = bld.add(d);
+  for (int s = 0; s < bld.n_sm; ++s) {
+    const int r0 = (int)((int64_t)d.rows * s / bld.n_sm);
+    const int r1 = (int)((int64_t)d.rows * (s + 1) / bld.n_sm);
+    bld.place(op, s, r0, r1, 0);
+  }
+}
+
+OpDesc gemv_desc(int K, std::initializer_list<std::pair<const void*, int>> mats) {
+  OpDesc d = blank(OP_GEMV);
+  d.K = K;
+  for (auto& m : mats) {
+    d.w[d.n_mat] = reinterpret_cast<const uint16_t*>(m.first);
+    d.mat_rows[d.n_mat] = m.second;
+    d.rows += m.second;
+    d.n_mat++;
+  }
+  return d;
+}
+
+Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
+  const mk_model_desc& D = h->desc;
+  const int N = B * R;
+  const int d = D.d_model;
+  Builder bld(h->n_sm);
+
+  {  // embedding
+    OpDesc e = blank(OP_EMBED);
+    e.ssq_out = 0;
+    const int op = bld.add(e);
+    for (int s = 0; s < h->n_sm; ++s)
+      bld.place(op, s, (int)((int64_t)d * s / h->n_sm), (int)((int64_t)d * (s + 1) / h->n_sm), 0);
+  }
+  for (int i = 0; i < D.n_layers; ++i) {
+    const mk_layer_weights& L = h->w.layers[i];
+    const int m = D.mixer[i];
+    if (m == MK_MIXER_GQA) {
+      const int hq = D.n_q_heads, hkv = D.n_kv_heads, hd = D.head_dim, G = hq / hkv;
+      OpDesc qkv = gemv_desc(d, {{L.wq, hq * hd}, {L.wk, hkv * hd}, {L.wv, hkv * hd}});
+      qkv.layer = i;
+      qkv.in_kind = IN_NORM;
+      qkv.gain = reinterpret_cast<const uint16_t*>(L.attn_norm);
+      qkv.ssq_in = 2 * i;
+      qkv.out_kind = OUT_STORE;
+      qkv.out = h->proj;
+      qkv.out_stride = h->proj_stride;
+      gemv_op(bld, qkv, N);
+
+      OpDesc ra = blank(OP_ROPE_APPEND);
+      ra.layer = i;
+      ra.slot = h->slot[i];
+      ra.n_heads = hq;
+      ra.n_kv_heads = hkv;
+      ra.head_dim = hd;
+      ra.out = h->proj;
+      ra.out_stride = h->proj_stride;
+      const int op_ra = bld.add(ra);
+      for (int s = 0; s < h->n_sm; ++s) bld.place(op_ra, s, 0, 0, 0);
+
+      OpDesc at = blank(OP_ATTN);
+      at.layer = i;
+      at.slot = h->slot[i];
+      at.n_heads = hq;
+      at.n_kv_heads = hkv;
+      at.head_dim = hd;
+      at.groups = G;
+      at.in = h->proj;
+      at.in_stride = h->proj_stride;
+      at.out = h->attn_out;
+      at.out_stride = h->attn_stride;
+      // rows per instruction so that each warp owns at most 4 (row, head) pairs
+      const int rows_per = std::max(1, std::min(R, (4 * kConsumerWarps) / G));
+      const int nsplit = (R + rows_per - 1) / rows_per;
+      at.nchunk = std::max(1, h->n_sm / (B * hkv * nsplit));
+      const int op_at = bld.add(at);
+      int k = 0;
+      for (int b = 0; b < B; ++b)
+        for (int g = 0; g < hkv; ++g)
+          for (int c = 0; c < at.nchunk; ++c)
+            for (int sp = 0; sp < nsplit; ++sp, ++k) {
+              const int rlo = sp * rows_per, rhi = std::min(R, rlo + rows_per);
+              bld.place(op_at, k % h->n_sm, b * hkv + g, c, rlo | (rhi << 8));
+            }
+
+      OpDesc o = gemv_desc(hq * hd, {{L.wo, d}});
+      o.layer = i;
+      o.in_kind = IN_BUF;
+      o.in = h->attn_out;
+      o.in_stride = h->attn_stride;
+      o.out_kind = OUT_RESID;
+      o.ssq_out = 2 * i + 1;
+      gemv_op(bld, o, N);
+    } else {  // gated delta net / KDA
+      const int H = D.lin_heads, dk = D.lin_dk, dv = D.lin_dv;
+      const bool kda = m == MK_MIXER_KDA;
+      OpDesc pj = gemv_desc(d, {{L.wq, H * dk}, {L.wk, H * dk}, {L.wv, H * dv}, {L.wa, kda ? H * dk : H}, {L.wb, H}});
+      pj.layer = i;
+      pj.in_kind = IN_NORM;
+      pj.gain = reinterpret_cast<const uint16_t*>(L.attn_norm);
+      pj.ssq_in = 2 * i;
+      pj.out_kind = OUT_STORE;
+      pj.out = h->proj;
+      pj.out_stride = h->proj_stride;
+      gemv_op(bld, pj, N);
+
+      OpDesc dl = blank(OP_DELTA);
+      dl.layer = i;
+      dl.slot = h->slot[i];
+      dl.n_heads = H;
+      dl.dk = dk;
+      dl.dv = dv;
+      dl.per_channel_decay = kda ? 1 : 0;
+      dl.col_group = kConsumerWarps;
+      dl.in = h->proj;
+      dl.in_stride = h->proj_stride;
+      dl.out = h->attn_out;
+      dl.out_stride = h->attn_stride;
+      const int op_dl = bld.add(dl);
+      const int ngrp = (dv + kConsumerWarps - 1) / kConsumerWarps;
+      int k = 0;
+      for (int b = 0; b < B; ++b)
+        for (int hh = 0; hh < H; ++hh)
+          for (int jg = 0; jg < ngrp; ++jg, ++k) bld.place(op_dl, k % h->n_sm, b, hh, jg);
+
+      OpDesc o = gemv_desc(H * dv, {{L.wo, d}});
+      o.layer = i;
+      o.in_kind = IN_BUF;
+      o.in = h->attn_out;
+      o.in_stride = h->attn_stride;
+      o.out_kind = OUT_RESID;
+      o.ssq_out = 2 * i + 1;
+      gemv_op(bld, o, N);
+    }
+    // dense SwiGLU
+    OpDesc up = gemv_desc(d, {{L.w_gate, D.ffn_dim}, {L.w_up, D.ffn_dim}});
+    up.rows = D.ffn_dim;  // logical rows: each pairs a gate row with an up row
+    up.layer = i;
+    up.in_kind = IN_NORM;
+    up.gain = reinterpret_cast<const uint16_t*>(L.ffn_norm);
+    up.ssq_in = 2 * i + 1;
+    up.out_kind = OUT_SWIGLU;
+    up.out = h->hbuf;
+    up.out_stride = h->hbuf_stride;
+    gemv_op(bld, up, N);
+
+    OpDesc dn = gemv_desc(D.ffn_dim, {{L.w_down, d}});
+    dn.layer = i;
+    dn.in_kind = IN_BUF;
+    dn.in = h->hbuf;
+    dn.in_stride = h->hbuf_stride;
+    dn.out_kind = OUT_RESID;
+    dn.ssq_out = 2 * i + 2;
+    gemv_op(bld, dn, N);
+  }
+  if (head) {
+    OpDesc lm = gemv_desc(d, {{D.tied_embedding ? h->w.embed : h->w.lm_head, D.vocab}});
+    lm.in_kind = IN_NORM;
+    lm.gain = reinterpret_cast<const uint16_t*>(h->w.final_norm);
+    lm.ssq_in = 2 * D.n_layers;
+    lm.out_kind = OUT_LOGITS;
+    gemv_op(bld, lm, N);
+  }
+  {
+    OpDesc f = blank(OP_FINAL);
+    const int op = bld.add(f);
+    bld.place(op, 0, 0, 0, 0);
+  }
+
+  Program prog;
+  prog.B = B;
+  prog.R = R;
+  prog.head = head;
+  prog.n_ops = (int)bld.ops.size();
+  if (prog.n_ops > h->max_ops) {
+    *st = fail(h, MK_ERR_UNSUPPORTED, "program has %d ops, more than the %d counters allocated", prog.n_ops,
+               h->max_ops);
+    return prog;
+  }
+  std::vector<Instr> flat;
+  std::vector<int32_t> qoff(h->n_sm + 1, 0);
+  for (int s = 0; s < h->n_sm; ++s) {
+    qoff[s] = (int32_t)flat.size();
+    flat.insert(flat.end(), bld.q[s].begin(), bld.q[s].end());
+  }
+  qoff[h->n_sm] = (int32_t)flat.size();
+  prog.n_instr = (int)flat.size();
+  cudaError_t e;
+  if ((e = cudaMalloc(&prog.d_ops, sizeof(OpDesc) * prog.n_ops)) != cudaSuccess ||
+      (e = cudaMalloc(&prog.d_instr, sizeof(Instr) * std::max(1, prog.n_instr))) != cudaSuccess ||
+      (e = cudaMalloc(&prog.d_qoff, sizeof(int32_t) * (h->n_sm + 1))) != cudaSuccess) {
+    *st = cuda_fail(h, e, "program allocation");
+    return prog;
+  }
+  cudaMemcpy(prog.d_ops, bld.ops.data(), sizeof(OpDesc) * prog.n_ops, cudaMemcpyHostToDevice);
+  cudaMemcpy(prog.d_instr, flat.data(), sizeof(Instr) * prog.n_instr, cudaMemcpyHostToDevice);
+  e = cudaMemcpy(prog.d_qoff, qoff.data(), sizeof(int32_t) * (h->n_sm + 1), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) *st = cuda_fail(h, e, "program upload");
+  h->bytes += (int64_t)(sizeof(OpDesc) * prog.n_ops + sizeof(Instr) * prog.n_instr);
+  return prog;
+}
+
+Program* get_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
+  for (auto& p : h->programs)
+    if (p.B == B && p.R == R && p.head == head) return &p;
+  *st = MK_OK;
+  Program p = build_program(h, B, R, head, st);
+  if (*st != MK_OK) {
+    cudaFree(p.d_ops);
+    cudaFree(p.d_instr);
+    cudaFree(p.d_qoff);
+    return nullptr;
+  }
+  h->programs.push_back(p);
+  return &h->programs.back();
+}
+
+mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const int32_t* positions, int B, int R,
+                      float* logits, int32_t* argmax, bool commit_all, cudaStream_t stream) {
+  mk_status st = MK_OK;
+  const bool head = logits != nullptr || argmax != nullptr;
+  Program* prog = get_program(h, B, R, head, &st);
+  if (!prog) return st;
+  const mk_model_desc& D = h->desc;
+  KParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.ops = prog->d_ops;
+  p.instrs = prog->d_instr;
+  p.qoff = prog->d_qoff;
+  p.counters = h->counters;
+  p.arrive = h->arrive;
+  p.status = h->status;
+  p.abort_flag = h->abort_flag;
+  p.timeout_ns = 2000000000ull;
+  p.n_ops = prog->n_ops;
+  p.n_sm = h->n_sm;
+  p.tokens = tokens;
+  p.tok_stride = tok_stride;
+  p.positions = positions;
+  p.B = B;
+  p.R = R;
+  p.N = B * R;
+  p.epoch = ++h->epoch;
+  p.commit_all = commit_all ? 1 : 0;
+  p.logits = logits;
+  p.argmax = argmax;
+  p.d = D.d_model;
+  p.V = D.vocab;
+  p.max_ctx = D.max_ctx;
+  p.max_batch = D.max_batch;
+  p.max_rows = D.max_rows;
+  p.eps = D.norm_eps;
+  p.embed = reinterpret_cast<const uint16_t*>(h->w.embed);
+  p.x = h->x;
+  p.ssq = h->ssq;
+  p.amax_part = h->amax_part;
+  p.attn_part = h->attn_part;
+  p.attn_part_stride = h->attn_part_stride;
+  p.kcache = h->kcache;
+  p.vcache = h->vcache;
+  p.state = h->state;
+  p.pend = h->pend;
+  p.pend_rec = h->pend_rec;
+  p.seq = h->seq;
+  p.rope = h->rope;
+  p.rot_dim = h->rot_dim;
+  p.n_q_heads = D.n_q_heads;
+  p.n_kv_heads = D.n_kv_heads;
+  p.head_dim = D.head_dim;
+  p.lin_heads = D.lin_heads;
+  p.lin_dk = D.lin_dk;
+  p.lin_dv = D.lin_dv;
+  h->n_ops_last = prog->n_ops;
+  cudaError_t e = kernel_launch(p, h->n_sm, stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
+  return MK_OK;
+}
+
+}  // namespace
+
+// ==================================================================================================
+// C ABI
+// ==================================================================================================
+extern "C" {
+
+mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int device, mk_handle** out) {
+  if (!desc || !weights || !out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  mk_handle* h = new mk_handle();
+  h->desc = *desc;
+  h->w = *weights;
+  h->device = device;
+  mk_status st = check_desc(h, h->desc, h->w);
+  if (st != MK_OK) {
+    // keep the message for mk_last_error(NULL)-style callers: print it, then fail
+    fprintf(stderr, "mk_create: %s\n", h->err.c_str());
+    delete h;
+    return st;
+  }
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) {
+    delete h;
+    return MK_ERR_CUDA;
+  }
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
+  cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, device);
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (!coop || smem_optin < (int)kernel_smem_bytes()) {
+    fprintf(stderr, "mk_create: device lacks cooperative launch or %zu bytes of shared memory\n", kernel_smem_bytes());
+    delete h;
+    return MK_ERR_UNSUPPORTED;
+  }
+  if ((e = kernel_configure()) != cudaSuccess) {
+    fprintf(stderr, "mk_create: %s\n", cudaGetErrorString(e));
+    delete h;
+    return MK_ERR_CUDA;
+  }
+
+  const mk_model_desc& D = h->desc;
+  h->slot.resize(D.n_layers);
+  for (int i = 0; i < D.n_layers; ++i) {
+    if (D.mixer[i] == MK_MIXER_GQA) h->slot[i] = h->n_gqa++;
+    else if (D.mixer[i] == MK_MIXER_MLA) h->slot[i] = h->n_mla++;
+    else h->slot[i] = h->n_delta++;
+  }
+  const int Bm = D.max_batch, Rm = D.max_rows;
+  h->nmax = Bm * Rm;
+  int proj = 8, attn = 8;
+  for (int i = 0; i < D.n_layers; ++i) {
+    const int m = D.mixer[i];
+    if (m == MK_MIXER_GQA) {
+      proj = std::max(proj, (D.n_q_heads + 2 * D.n_kv_heads) * D.head_dim);
+      attn = std::max(attn, D.n_q_heads * D.head_dim);
+    } else if (is_delta(m)) {
+      proj = std::max(proj, delta_proj_cols(D, m));
+      attn = std::max(attn, D.lin_heads * D.lin_dv);
+    }
+  }
+  h->proj_stride = round_up(proj, 8);
+  h->attn_stride = round_up(attn, 8);
+  h->hbuf_stride = round_up(std::max(D.ffn_dim, 8), 8);
+  h->max_ops = 16 * D.n_layers + 16;
+
+#define ALLOC(ptr, count) \
+  if ((st = dev_alloc(h, &h->ptr, (size_t)(count), #ptr)) != MK_OK) goto fail_out
+  ALLOC(x, (size_t)kMaxN * D.d_model);
+  ALLOC(proj, (size_t)kMaxN * h->proj_stride);
+  ALLOC(attn_out, (size_t)kMaxN * h->attn_stride);
+  ALLOC(hbuf, (size_t)kMaxN * h->hbuf_stride);
+  ALLOC(ssq, (size_t)(2 * D.n_layers + 1) * h->n_sm * kMaxN);
+  ALLOC(amax_part, (size_t)h->n_sm * kMaxN);
+  ALLOC(counters, h->max_ops);
+  ALLOC(status, 4);
+  ALLOC(abort_flag, 4);
+  ALLOC(seq, Bm);
+  ALLOC(pos_buf, std::max(Bm, 8));
+  ALLOC(stage_tok, kMaxN);
+  ALLOC(stage_pos, std::max(Bm, 8));
+  ALLOC(stage_argmax, kMaxN);
+  ALLOC(stage_logits, (size_t)h->nmax * D.vocab);
+  if (h->n_gqa) {
+    const int hkv = D.n_kv_heads, hd = D.head_dim, G = D.n_q_heads / D.n_kv_heads;
+    const size_t cache = (size_t)h->n_gqa * Bm * hkv * D.max_ctx * hd;
+    ALLOC(kcache, cache);
+    ALLOC(vcache, cache);
+    h->attn_part_stride = hd + 4;
+    const size_t recs = (size_t)std::max(h->n_sm, Bm * hkv) * Rm * G * 2;
+    ALLOC(attn_part, recs * h->attn_part_stride);
+    ALLOC(arrive, (size_t)h->n_gqa * Bm * hkv);
+    h->rot_dim = hd;
+  }
+  if (h->n_delta) {
+    const int H = D.lin_heads, dk = D.lin_dk, dv = D.lin_dv;
+    ALLOC(state, (size_t)h->n_delta * Bm * H * dv * dk);
+    h->pend_rec = round_up(2 * dk + dv + 1, 4);
+    ALLOC(pend, (size_t)h->n_delta * 2 * Bm * Rm * H * h->pend_rec);
+  }
+  if (h->rot_dim) {
+    ALLOC(rope, (size_t)D.max_ctx * (h->rot_dim / 2));
+    if ((e = rope_table_launch(h->rope, D.max_ctx, h->rot_dim, (double)D.rope_theta, 0)) != cudaSuccess) {
+      st = cuda_fail(h, e, "rope table");
+      goto fail_out;
+    }
+  }
+#undef ALLOC
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+    st = cuda_fail(h, e, "create");
+    goto fail_out;
+  }
+  *out = h;
+  return MK_OK;
+fail_out:
+  fprintf(stderr, "mk_create: %s\n", h->err.c_str());
+  mk_destroy(h);
+  return st;
+}
+
+mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_tokens, void* stream) {
+  if (!h || !tokens) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d", batch);
+  if (n_tokens < 1 || n_tokens > D.max_ctx) return fail(h, MK_ERR_INVALID_ARG, "n_tokens %d", n_tokens);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  if ((e = cudaMemsetAsync(h->seq, 0, sizeof(SeqState) * batch, s)) != cudaSuccess) return cuda_fail(h, e, "reset");
+  if (h->n_delta) {
+    const size_t per_seq = (size_t)D.lin_heads * D.lin_dv * D.lin_dk;
+    for (int sl = 0; sl < h->n_delta; ++sl) {
+      e = cudaMemsetAsync(h->state + (size_t)sl * D.max_batch * per_seq, 0, sizeof(float) * per_seq * batch, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "state reset");
+    }
+  }
+  for (int c0 = 0; c0 < n_tokens; c0 += D.max_rows) {
+    const int rc = std::min(D.max_rows, n_tokens - c0);
+    if ((e = fill_i32_launch(h->pos_buf, batch, c0, s)) != cudaSuccess) return cuda_fail(h, e, "positions");
+    mk_status st = launch_step(h, tokens + c0, n_tokens, h->pos_buf, batch, rc, nullptr, nullptr,
+                               c0 + rc == n_tokens, s);
+    if (st != MK_OK) return st;
+  }
+  return MK_OK;
+}
+
+mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch, int rows,
+                         float* logits_out, int32_t* argmax_out, void* stream) {
+  if (!h || !tokens || !positions) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, D.max_batch);
+  if (rows < 1 || rows > D.max_rows) return fail(h, MK_ERR_INVALID_ARG, "rows %d outside 1..%d", rows, D.max_rows);
+  if (!logits_out && !argmax_out) return fail(h, MK_ERR_INVALID_ARG, "no output requested");
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  return launch_step(h, tokens, rows, positions, batch, rows, logits_out, argmax_out, false,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const int32_t* positions_host, int batch,
+                              int rows, float* logits_host, int32_t* argmax_host, void* stream) {
+  if (!h || !tokens_host || !positions_host || !argmax_host) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows)
+    return fail(h, MK_ERR_INVALID_ARG, "batch %d / rows %d out of range", batch, rows);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  const int n = batch * rows;
+  if ((e = cudaMemcpyAsync(h->stage_tok, tokens_host, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(h->stage_pos, positions_host, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s)) !=
+          cudaSuccess)
+    return cuda_fail(h, e, "host to device copy");
+  mk_status st = launch_step(h, h->stage_tok, rows, h->stage_pos, batch, rows, logits_host ? h->stage_logits : nullptr,
+                             h->stage_argmax, false, s);
+  if (st != MK_OK) return st;
+  if ((e = cudaMemcpyAsync(argmax_host, h->stage_argmax, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(h, e, "device to host copy");
+  if (logits_host &&
+      (e = cudaMemcpyAsync(logits_host, h->stage_logits, sizeof(float) * (size_t)n * D.vocab, cudaMemcpyDeviceToHost,
+                           s)) != cudaSuccess)
+    return cuda_fail(h, e, "device to host copy");
+  return mk_get_status(h, stream);
+}
+
+mk_status mk_get_status(mk_handle* h, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "stream synchronize");
+  int32_t code = 0;
+  if ((e = cudaMemcpy(&code, h->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(h, e, "status read");
+  if (code != 0) {
+    cudaMemset(h->status, 0, sizeof(int32_t));
+    cudaMemset(h->abort_flag, 0, sizeof(int32_t));
+    cudaMemset(h->counters, 0, sizeof(uint32_t) * h->max_ops);
+    if (h->arrive)
+      cudaMemset(h->arrive, 0, sizeof(uint32_t) * (size_t)h->n_gqa * h->desc.max_batch * h->desc.n_kv_heads);
+    cudaDeviceSynchronize();
+    h->err = code == MK_ERR_TIMEOUT ? "device watchdog timeout" : "device input check failed (token or position)";
+    return (mk_status)code;
+  }
+  return MK_OK;
+}
+
+const char* mk_last_error(const mk_handle* h) { return h ? h->err.c_str() : ""; }
+
+mk_status mk_get_info(const mk_handle* h, mk_info* out) {
+  if (!h || !out) return MK_ERR_INVALID_ARG;
+  out->n_sm = h->n_sm;
+  out->threads_per_cta = kThreads;
+  out->smem_bytes = (int32_t)kernel_smem_bytes();
+  out->ring_slots = kSlots;
+  out->ring_slot_bytes = kSlotBytes;
+  out->n_ops_last = h->n_ops_last;
+  out->device_bytes = h->bytes;
+  return MK_OK;
+}
+
+void mk_destroy(mk_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  for (auto& p : h->programs) {
+    cudaFree(p.d_ops);
+    cudaFree(p.d_instr);
+    cudaFree(p.d_qoff);
+  }
+  for (void* p : h->allocs) cudaFree(p);
+  delete h;
+}
+
+}  // extern "C"

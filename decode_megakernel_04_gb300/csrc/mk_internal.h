@@ -1,0 +1,146 @@
+// Internal layout shared by the host scheduler (mk_host.cu) and the persistent kernel (mk_kernel.cu).
+//
+// A decode step is compiled into a PROGRAM: a list of ops in topological order (embedding, then per
+// layer: projection GEMV, attention / delta-rule op, output GEMV, FFN GEMVs, then LM head and a final
+// op). Each op is split into work items ("instructions") placed on SMs; every SM runs its own queue of
+// instructions in op order. An op's instructions wait until the ops it depends on have counted all their
+// instructions done (per-op counters in global memory, release/acquire at GPU scope). A producer warp
+// per SM walks the same queue ahead of the consumers and streams each instruction's weights (and KV
+// prefix) into a shared-memory ring with bulk async copies, so weight traffic for op k+1 and later is
+// already in flight while op k computes or waits for its dependencies.
+#pragma once
+#include <stdint.h>
+
+namespace mk {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kSlots = 6;
+constexpr int kSlotBytes = 32768;
+constexpr int kMaxN = 64;        // rows per step (batch * rows)
+constexpr int kMaxRows = 8;      // query rows per sequence
+constexpr int kMaxOpMats = 6;
+constexpr int kMaxDeps = 2;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 16;
+
+enum OpType : int32_t {
+  OP_EMBED = 0,       // x = E[token] (fp32), RMS partials of x
+  OP_GEMV = 1,        // y = act(in) W^T, one instruction per SM over a range of output rows
+  OP_ROPE_APPEND = 2, // rotate q / k, append bf16 k, v to the KV cache
+  OP_ATTN = 3,        // GQA attention over one context chunk of one (sequence, kv head)
+  OP_DELTA = 4,       // gated delta rule (GDN / KDA) over a group of value columns of one head
+  OP_MLA_PREP = 5,    // MLA: norm + rope of the new latents, append to the latent cache, q rope
+  OP_MLA_ATTN = 6,    // MLA absorbed attention over one context chunk of one (sequence, head group)
+  OP_ROUTE = 7,       // MoE: sigmoid scores, biased top-k, renormalised weights, expert row lists
+  OP_MOE_UP = 8,      // MoE: gate/up GEMV of shared + routed experts, SwiGLU
+  OP_MOE_DOWN = 9,    // MoE: down GEMV of shared + routed experts, weighted sum, residual add
+  OP_FINAL = 10,      // greedy argmax, sequence bookkeeping, counter reset
+};
+
+enum InKind : int32_t { IN_NORM = 0, IN_BUF = 1 };
+enum OutKind : int32_t { OUT_STORE = 0, OUT_RESID = 1, OUT_SWIGLU = 2, OUT_LOGITS = 3 };
+
+struct OpDesc {
+  int32_t type;
+  int32_t n_instr;          // instructions of this op in one step (its counter's target)
+  int32_t n_deps;
+  int32_t deps[kMaxDeps];
+  int32_t layer;            // model layer (or -1)
+  int32_t slot;             // index of the layer among layers of its kind (cache / state slot)
+  // ---- GEMV ----
+  int32_t K;                // input features
+  int32_t rows;             // output rows (logical rows for SwiGLU)
+  int32_t rg;               // physical weight rows per row group (16 or 8)
+  int32_t passes;           // ceil(N / 8) when 8 activation rows are processed per pass, else 1
+  int32_t n_mat;
+  int32_t mat_rows[kMaxOpMats];
+  const uint16_t* w[kMaxOpMats];
+  int32_t in_kind;
+  int32_t in_stride;        // floats between activation rows (IN_BUF)
+  const float* in;
+  const uint16_t* gain;     // bf16 RMSNorm gain (IN_NORM)
+  int32_t ssq_in;           // RMS-partial slot read (IN_NORM)
+  int32_t out_kind;
+  int32_t out_stride;       // floats between output rows
+  float* out;
+  int32_t ssq_out;          // RMS-partial slot written (OUT_RESID, EMBED)
+  // ---- attention ----
+  int32_t nchunk;           // context chunks per (sequence, kv head)
+  int32_t groups;           // q heads per kv head (GQA) or heads per item (MLA)
+  int32_t head_dim;
+  int32_t n_heads;          // q heads (GQA) / heads (delta, MLA)
+  int32_t n_kv_heads;
+  // ---- delta rule ----
+  int32_t dk, dv;
+  int32_t per_channel_decay; // KDA
+  int32_t col_group;         // value columns per instruction
+  int32_t pad_[3];
+};
+
+struct Instr {
+  int32_t op;
+  int32_t a, b, c;
+};
+
+struct SeqState {
+  int32_t c_int;   // tokens absorbed into the recurrent state in HBM
+  int32_t u_int;   // pending rows of the previous call (stored for replay)
+  int32_t c_spec;  // lowest position the next call may pass (the committed prefix)
+  int32_t pad;
+};
+
+struct KParams {
+  const OpDesc* ops;
+  const Instr* instrs;
+  const int32_t* qoff;      // [n_sm + 1] per-SM queue offsets into instrs
+  uint32_t* counters;       // [n_ops] completed instructions per op in this launch
+  uint32_t* arrive;         // attention chunk arrival counters
+  int32_t* status;
+  int32_t* abort_flag;
+  unsigned long long timeout_ns;
+  int32_t n_ops;
+  int32_t n_sm;
+  // step inputs
+  const int32_t* tokens;
+  int32_t tok_stride;       // tokens of sequence b start at b * tok_stride
+  const int32_t* positions;
+  int32_t B, R, N;
+  uint32_t epoch;
+  int32_t commit_all;       // prefill: the rows of this call count as committed for c_spec
+  float* logits;
+  int32_t* argmax;
+  // model
+  int32_t d, V, max_ctx, max_batch, max_rows;
+  float eps;
+  const uint16_t* embed;
+  // activations
+  float* x;                 // [N, d] residual stream
+  float* ssq;               // [slots][n_sm][kMaxN] RMS partials (sum of squares)
+  float2* amax_part;        // [n_sm][kMaxN] (value, index) LM-head argmax partials
+  float* attn_part;         // attention chunk partials
+  int32_t attn_part_stride; // floats per partial record
+  // GQA caches: [slot][max_batch][Hkv][max_ctx][hd] bf16
+  uint16_t* kcache;
+  uint16_t* vcache;
+  // delta rule: state [slot][max_batch][H][dv][dk] fp32; pending [2][slot][max_batch][max_rows][H][rec]
+  float* state;
+  float* pend;
+  int32_t pend_rec;         // floats per pending record (k_hat, v, alpha, beta)
+  // MLA: latent cache [slot][max_batch][max_ctx][kv_lora + rope] bf16
+  uint16_t* latent;
+  // MoE routing: per layer-slot [N][top_k] expert ids / weights, per expert row lists
+  int32_t* route_idx;
+  float* route_w;
+  int32_t* expert_rows;     // [E][kMaxN] row ids routed to an expert (this step)
+  int32_t* expert_cnt;      // [E] + union list
+  SeqState* seq;
+  const float2* rope;       // [max_ctx][rot_dim / 2] (cos, sin)
+  int32_t rot_dim;
+  // model dims needed by several ops
+  int32_t n_q_heads, n_kv_heads, head_dim;
+  int32_t lin_heads, lin_dk, lin_dv;
+};
+
+}  // namespace mk

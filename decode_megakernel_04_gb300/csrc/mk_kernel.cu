@@ -1,0 +1,1042 @@
+// Persistent decode megakernel for GB300 (sm_103a): one CTA per SM, one launch per decode step.
+//
+// Each CTA runs 8 consumer warps and 1 producer warp. The producer walks the SM's instruction queue
+// ahead of the consumers and streams every weight tile (and every cached-KV block) that an instruction
+// will read into a 6 x 32 KB shared-memory ring with bulk async copies (cp.async.bulk, completion on an
+// mbarrier). Weights never depend on activations, so the producer runs across op and layer boundaries
+// while the consumers wait on inter-SM dependency counters: the next op's weights are already arriving
+// when its inputs become ready. This is the pages' central idea — a weight load is issued as early as
+// on-chip storage allows, not when the op that uses it starts (Kimi K3's TPU megakernel, "What a
+// megakernel is, and what it fixes on a TPU"; the cross-layer prefetch of Figure 4) — mapped onto the
+// GPU's per-SM shared memory instead of the TPU's single VMEM pool.
+//
+// Every spin-wait is bounded by %globaltimer; on expiry the kernel records MK_ERR_TIMEOUT, raises an
+// abort flag that every other wait also polls, drains its in-flight copies and returns.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+constexpr int kStatusTimeout = 5;
+constexpr int kStatusDevice = 6;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------------------------------------
+// small device helpers
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ unsigned long long global_timer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ float bf2f(uint32_t h16) { return __uint_as_float(h16 << 16); }
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* ptr, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// --- mbarrier / bulk copy -------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// --- bounded waits --------------------------------------------------------------------------------
+struct Spin {
+  unsigned long long t0 = 0;
+  uint32_t n = 0;
+  // false = give up (abort raised elsewhere, or this wait timed out and raised it)
+  __device__ __forceinline__ bool ok(const KParams& p) {
+    if ((++n & 63u) != 0u) return true;
+    if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) return false;
+    const unsigned long long now = global_timer();
+    if (t0 == 0) {
+      t0 = now;
+      return true;
+    }
+    if (now - t0 > p.timeout_ns) {
+      atomicCAS(p.status, 0, kStatusTimeout);
+      atomicExch(p.abort_flag, 1);
+      return false;
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KParams& p) {
+  Spin s;
+  while (!mbar_try_wait(bar, parity)) {
+    if (!s.ok(p)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, const KParams& p) {
+  Spin s;
+  while (ld_acquire(ctr) < target) {
+    if (!s.ok(p)) return false;
+    __nanosleep(20);
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------------------------
+// shared memory
+// ------------------------------------------------------------------------------------------------
+struct CSmem {
+  float red[kConsumerWarps][64];
+  float val[64];
+  float sq[64];
+  float inv_rms[kMaxN];
+  float ssq_acc[kMaxN];
+  float best_val[kMaxN];
+  int32_t best_idx[kMaxN];
+  int32_t flag;
+  int32_t last;
+  int32_t pad[2];
+  uint16_t knew[kMaxRows * 256];
+  uint16_t vnew[kMaxRows * 256];
+};
+
+struct Ring {
+  uint8_t* base;
+  uint64_t* full;
+  uint64_t* empty;
+  __device__ __forceinline__ uint8_t* slot_ptr(uint32_t chunk) const {
+    return base + (chunk % kSlots) * kSlotBytes;
+  }
+};
+
+constexpr size_t kSmemBytes = (size_t)kSlots * kSlotBytes + 2 * kSlots * sizeof(uint64_t) + sizeof(CSmem);
+
+// consumer side of one ring chunk
+__device__ __forceinline__ bool ring_wait_full(const Ring& rg, uint32_t chunk, const KParams& p) {
+  return wait_bar(&rg.full[chunk % kSlots], (chunk / kSlots) & 1u, p);
+}
+__device__ __forceinline__ void ring_release(const Ring& rg, uint32_t chunk, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&rg.empty[chunk % kSlots]);
+}
+
+// producer side: wait until the slot of `chunk` is free, arm its full barrier with `bytes`
+__device__ __forceinline__ bool ring_acquire(const Ring& rg, uint32_t chunk, uint32_t bytes, const KParams& p,
+                                             int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const uint32_t k = chunk / kSlots;
+    if (k > 0) ok = wait_bar(&rg.empty[chunk % kSlots], (k - 1) & 1u, p) ? 1 : 0;
+    if (ok) mbar_arrive_expect_tx(&rg.full[chunk % kSlots], bytes);
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+// ------------------------------------------------------------------------------------------------
+// cross-lane reduction of V independent partial sums (V = 16, 32 or 64)
+// After the call lane L holds, in v[0 .. F-1] with F = max(V/32, 1), the warp totals of indices
+// [L*F, L*F + F) when V >= 32, or of index L / (32/V) when V < 32.
+// ------------------------------------------------------------------------------------------------
+template <int C, int O>
+struct MultiReduce {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (C > 1) {
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < C / 2; ++i) {
+        const float send = upper ? v[i] : v[i + C / 2];
+        const float keep = upper ? v[i + C / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      MultiReduce<C / 2, O / 2>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      MultiReduce<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+// block-wide: totals of V values land in cs.val[0..V-1]
+template <int V>
+__device__ __forceinline__ void block_reduce(float* v, CSmem& cs, int warp, int lane, int ctid) {
+  MultiReduce<V, 16>::run(v, lane);
+  if constexpr (V >= 32) {
+    constexpr int F = V / 32;
+#pragma unroll
+    for (int f = 0; f < F; ++f) cs.red[warp][lane * F + f] = v[f];
+  } else {
+    constexpr int S = 32 / V;
+    if (lane % S == 0) cs.red[warp][lane / S] = v[0];
+  }
+  consumer_sync();
+  if (ctid < V) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) t += cs.red[w][ctid];
+    cs.val[ctid] = t;
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------------------------------------
+// GEMV: out rows [a, b) of  act(in) @ W^T. Weight rows stream through the ring in chunks of
+// RG rows x KC inputs (32 KB of bf16). Thread t owns inputs [t*CPL, t*CPL + CPL) of each chunk and keeps
+// RG x NR partial sums in registers across the K slices of a row group; one block reduction per group.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ const uint16_t* gemv_row_src(const OpDesc& op, int g0, int i, int nl, bool swiglu) {
+  if (swiglu) {
+    return (i < nl) ? op.w[0] + (size_t)(g0 + i) * op.K : op.w[1] + (size_t)(g0 + i - nl) * op.K;
+  }
+  int row = g0 + i;
+#pragma unroll 1
+  for (int m = 0; m < op.n_mat; ++m) {
+    if (row < op.mat_rows[m]) return op.w[m] + (size_t)row * op.K;
+    row -= op.mat_rows[m];
+  }
+  return op.w[0];
+}
+
+__device__ bool gemv_produce(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                             uint32_t& chunk, int lane) {
+  const int KC = kSlotBytes / 2 / op.rg;
+  const bool swiglu = op.out_kind == OUT_SWIGLU;
+  const int glog = swiglu ? op.rg / 2 : op.rg;
+  const int nks = (op.K + KC - 1) / KC;
+  const uint32_t ring_base = smem_u32(rg.base);
+  for (int pass = 0; pass < op.passes; ++pass) {
+    for (int g0 = in.a; g0 < in.b; g0 += glog) {
+      const int nl = min(glog, in.b - g0);
+      const int nphys = swiglu ? 2 * nl : nl;
+      for (int ks = 0; ks < nks; ++ks) {
+        const int k0 = ks * KC;
+        const int kw = min(KC, op.K - k0);
+        if (!ring_acquire(rg, chunk, (uint32_t)(nphys * kw * 2), p, lane)) return false;
+        if (lane < nphys) {
+          const uint16_t* src = gemv_row_src(op, g0, lane, nl, swiglu) + k0;
+          bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + lane * kw * 2, src, (uint32_t)(kw * 2),
+                   &rg.full[chunk % kSlots]);
+        }
+        ++chunk;
+      }
+    }
+  }
+  return true;
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_f32(const float* src, float (&dst)[CPL]) {
+#pragma unroll
+  for (int c = 0; c < CPL; c += 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + c));
+    dst[c] = v.x;
+    dst[c + 1] = v.y;
+    dst[c + 2] = v.z;
+    dst[c + 3] = v.w;
+  }
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_bf16_row(const uint8_t* src, float (&dst)[CPL]) {
+  if constexpr (CPL == 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    dst[0] = bf_lo(w.x); dst[1] = bf_hi(w.x); dst[2] = bf_lo(w.y); dst[3] = bf_hi(w.y);
+    dst[4] = bf_lo(w.z); dst[5] = bf_hi(w.z); dst[6] = bf_lo(w.w); dst[7] = bf_hi(w.w);
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    dst[0] = bf_lo(w.x); dst[1] = bf_hi(w.x); dst[2] = bf_lo(w.y); dst[3] = bf_hi(w.y);
+  }
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_bf16_global(const uint16_t* src, float (&dst)[CPL]) {
+  if constexpr (CPL == 8) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+    dst[0] = bf_lo(w.x); dst[1] = bf_hi(w.x); dst[2] = bf_lo(w.y); dst[3] = bf_hi(w.y);
+    dst[4] = bf_lo(w.z); dst[5] = bf_hi(w.z); dst[6] = bf_lo(w.w); dst[7] = bf_hi(w.w);
+  } else {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+    dst[0] = bf_lo(w.x); dst[1] = bf_hi(w.x); dst[2] = bf_lo(w.y); dst[3] = bf_hi(w.y);
+  }
+}
+
+template <int RG, int NR>
+__device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                             uint32_t& chunk, CSmem& cs, int ctid) {
+  constexpr int CPL = kSlotBytes / 2 / RG / kConsumerThreads;  // 4 or 8 inputs per thread
+  constexpr int KC = CPL * kConsumerThreads;
+  constexpr int V = RG * NR;
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int sm = blockIdx.x;
+  const bool swiglu = op.out_kind == OUT_SWIGLU;
+  const int glog = swiglu ? RG / 2 : RG;
+  const int K = op.K;
+  const int nks = (K + KC - 1) / KC;
+  const int N = p.N;
+
+  if (op.in_kind == IN_NORM && ctid < N) {
+    float s = 0.f;
+    for (int q = 0; q < p.n_sm; ++q) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + ctid]);
+    cs.inv_rms[ctid] = rsqrtf(s / (float)K + p.eps);
+  }
+  if (ctid < kMaxN) {
+    cs.ssq_acc[ctid] = 0.f;
+    cs.best_val[ctid] = -CUDART_INF_F;
+    cs.best_idx[ctid] = 0;
+  }
+  consumer_sync();
+
+  for (int pass = 0; pass < op.passes; ++pass) {
+    const int nbase = pass * NR;
+    for (int g0 = in.a; g0 < in.b; g0 += glog) {
+      const int nl = min(glog, in.b - g0);
+      const int nphys = swiglu ? 2 * nl : nl;
+      float acc[RG][NR];
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int n = 0; n < NR; ++n) acc[i][n] = 0.f;
+
+      for (int ks = 0; ks < nks; ++ks) {
+        const int k0 = ks * KC;
+        const int kw = min(KC, K - k0);
+        ring_wait_full(rg, chunk, p);
+        const int col = ctid * CPL;
+        if (col < kw) {
+          float a[NR][CPL];
+          float gsc[CPL];
+          if (op.in_kind == IN_NORM) load_bf16_global<CPL>(op.gain + k0 + col, gsc);
+#pragma unroll
+          for (int n = 0; n < NR; ++n) {
+            const int row = nbase + n;
+            if (row < N) {
+              if (op.in_kind == IN_NORM) {
+                load_f32<CPL>(p.x + (size_t)row * p.d + k0 + col, a[n]);
+                const float s = cs.inv_rms[row];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) a[n][c] *= s * gsc[c];
+              } else {
+                load_f32<CPL>(op.in + (size_t)row * op.in_stride + k0 + col, a[n]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
+            }
+          }
+          const uint8_t* wbase = rg.slot_ptr(chunk) + col * 2;
+#pragma unroll
+          for (int i = 0; i < RG; ++i) {
+            if (i < nphys) {
+              float wf[CPL];
+              load_bf16_row<CPL>(wbase + (size_t)i * kw * 2, wf);
+#pragma unroll
+              for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[c], a[n][c], acc[i][n]);
+            }
+          }
+        }
+        ring_release(rg, chunk, lane);
+        ++chunk;
+      }
+
+      float v[V];
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int n = 0; n < NR; ++n) v[i * NR + n] = acc[i][n];
+      block_reduce<V>(v, cs, warp, lane, ctid);
+
+      // epilogue: cs.val[i * NR + n] is the dot product of physical row i with activation row nbase + n
+      if (op.out_kind == OUT_SWIGLU) {
+        if (ctid < nl * NR) {
+          const int j = ctid / NR, n = ctid % NR, row = nbase + n;
+          if (row < N) {
+            const float g = cs.val[j * NR + n];
+            const float u = cs.val[(nl + j) * NR + n];
+            op.out[(size_t)row * op.out_stride + g0 + j] = g / (1.0f + expf(-g)) * u;
+          }
+        }
+      } else if (ctid < V) {
+        const int i = ctid / NR, n = ctid % NR, row = nbase + n;
+        const bool ok = (i < nl) && (row < N);
+        const float val = cs.val[ctid];
+        if (op.out_kind == OUT_STORE) {
+          if (ok) op.out[(size_t)row * op.out_stride + g0 + i] = val;
+        } else if (op.out_kind == OUT_RESID) {
+          float xn = 0.f;
+          if (ok) {
+            float* xp = p.x + (size_t)row * p.d + g0 + i;
+            xn = __ldcg(xp) + val;
+            __stcg(xp, xn);
+          }
+          cs.sq[ctid] = xn * xn;
+        } else {  // OUT_LOGITS
+          if (ok && p.logits) p.logits[(size_t)row * p.V + g0 + i] = val;
+        }
+      }
+      if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
+        consumer_sync();
+        if (ctid < NR && nbase + ctid < N) {
+          const int row = nbase + ctid;
+          if (op.out_kind == OUT_RESID) {
+            float s = 0.f;
+            for (int i = 0; i < nl; ++i) s += cs.sq[i * NR + ctid];
+            cs.ssq_acc[row] += s;
+          } else {
+            float bv = cs.best_val[row];
+            int bi = cs.best_idx[row];
+            for (int i = 0; i < nl; ++i) {
+              const float vv = cs.val[i * NR + ctid];
+              if (vv > bv) { bv = vv; bi = g0 + i; }
+            }
+            cs.best_val[row] = bv;
+            cs.best_idx[row] = bi;
+          }
+        }
+      }
+      consumer_sync();
+    }
+  }
+  if (op.out_kind == OUT_RESID && ctid < N)
+    __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], cs.ssq_acc[ctid]);
+  if (op.out_kind == OUT_LOGITS && ctid < N)
+    p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(cs.best_val[ctid], __int_as_float(cs.best_idx[ctid]));
+}
+
+// ------------------------------------------------------------------------------------------------
+// embedding: x[n, a:b] = E[token_n, a:b] (fp32) and the RMS partial of this SM's columns
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ int token_of(const KParams& p, int n) {
+  return p.tokens[(n / p.R) * p.tok_stride + (n % p.R)];
+}
+
+__device__ void embed_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  for (int n = warp; n < p.N; n += kConsumerWarps) {
+    const int tok = token_of(p, n);
+    const uint16_t* e = p.embed + (size_t)tok * p.d;
+    float s = 0.f;
+    for (int c = in.a + lane; c < in.b; c += 32) {
+      const float v = bf2f(e[c]);
+      __stcg(&p.x[(size_t)n * p.d + c], v);
+      s += v * v;
+    }
+    s = warp_sum(s);
+    if (lane == 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + blockIdx.x) * kMaxN + n], s);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// GQA: RoPE on q and k of the new rows, bf16 k / v appended to the cache at positions p_b + r
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ size_t kv_index(const KParams& p, const OpDesc& op, int b, int g, int t) {
+  return ((((size_t)op.slot * p.max_batch + b) * op.n_kv_heads + g) * p.max_ctx + t) * op.head_dim;
+}
+
+__device__ void rope_append_consume(const KParams& p, const OpDesc& op, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int hq = op.n_heads, hkv = op.n_kv_heads, hd = op.head_dim, half = hd / 2;
+  const int per_row = hq + 2 * hkv;
+  const int total = p.N * per_row;
+  for (int it = blockIdx.x * kConsumerWarps + warp; it < total; it += p.n_sm * kConsumerWarps) {
+    const int n = it / per_row, h = it % per_row;
+    const int b = n / p.R, r = n % p.R;
+    const int pos = p.positions[b] + r;
+    float* vec = op.out + (size_t)n * op.out_stride + (size_t)h * hd;
+    const float2* cs = p.rope + (size_t)pos * (p.rot_dim / 2);
+    if (h < hq + hkv) {
+      for (int i = lane; i < half; i += 32) {
+        const float x1 = __ldcg(vec + i), x2 = __ldcg(vec + i + half);
+        const float2 t = cs[i];
+        const float y1 = x1 * t.x - x2 * t.y, y2 = x2 * t.x + x1 * t.y;
+        if (h < hq) {
+          __stcg(vec + i, y1);
+          __stcg(vec + i + half, y2);
+        } else {
+          uint16_t* kc = p.kcache + kv_index(p, op, b, h - hq, pos);
+          kc[i] = f2bf(y1);
+          kc[i + half] = f2bf(y2);
+        }
+      }
+    } else {
+      uint16_t* vc = p.vcache + kv_index(p, op, b, h - hq - hkv, pos);
+      for (int i = lane; i < hd; i += 32) vc[i] = f2bf(__ldcg(vec + i));
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// GQA attention. Instruction (a = b * Hkv + g, b = chunk c, c = first row | last row << 8).
+// Chunk c covers prefix positions [c*TC, min((c+1)*TC, p_b)), TC = ceil(p_b / nchunk); the last chunk
+// also takes the block's own rows p_b .. p_b + R - 1 (causal). Scores are kept in log2 units.
+// Each warp owns up to J (row, head) pairs; lane L owns dims [L*E, L*E + E) of the head.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void attn_range(const KParams& p, const OpDesc& op, int b, int c, int& t0, int& t1) {
+  const int pos0 = p.positions[b];
+  const int tc = (pos0 + op.nchunk - 1) / op.nchunk;
+  t0 = min(c * tc, pos0);
+  t1 = min(t0 + tc, pos0);
+}
+
+__device__ bool attn_produce(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+                             int lane) {
+  const int hkv = op.n_kv_heads, hd = op.head_dim;
+  const int b = in.a / hkv, g = in.a % hkv;
+  int t0, t1;
+  attn_range(p, op, b, in.b, t0, t1);
+  const int P = kSlotBytes / (4 * hd);
+  const uint32_t ring_base = smem_u32(rg.base);
+  for (int t = t0; t < t1; t += P) {
+    const int np = min(P, t1 - t);
+    const uint32_t bytes = (uint32_t)(np * hd * 2);
+    if (!ring_acquire(rg, chunk, 2 * bytes, p, lane)) return false;
+    const uint32_t dst = ring_base + (chunk % kSlots) * kSlotBytes;
+    if (lane == 0) bulk_g2s(dst, p.kcache + kv_index(p, op, b, g, t), bytes, &rg.full[chunk % kSlots]);
+    if (lane == 1) bulk_g2s(dst + kSlotBytes / 2, p.vcache + kv_index(p, op, b, g, t), bytes, &rg.full[chunk % kSlots]);
+    ++chunk;
+  }
+  return true;
+}
+
+template <int E>
+__device__ __forceinline__ void load_head_slice(const uint16_t* row, int lane, float (&out)[E]) {
+  const uint16_t* s = row + lane * E;
+  if constexpr (E == 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(s);
+    out[0] = bf_lo(w.x); out[1] = bf_hi(w.x); out[2] = bf_lo(w.y); out[3] = bf_hi(w.y);
+    out[4] = bf_lo(w.z); out[5] = bf_hi(w.z); out[6] = bf_lo(w.w); out[7] = bf_hi(w.w);
+  } else if constexpr (E == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(s);
+    out[0] = bf_lo(w.x); out[1] = bf_hi(w.x); out[2] = bf_lo(w.y); out[3] = bf_hi(w.y);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(s);
+    out[0] = bf_lo(w); out[1] = bf_hi(w);
+  }
+}
+
+// One block of up to 32 keys (rows of K/V in shared memory) folded into the running softmax state.
+// causal_base >= 0: key jj is the block row causal_base + jj and row r sees it iff jj <= r - causal_base.
+template <int E, int J>
+__device__ __forceinline__ void attn_block(const uint16_t* Ks, const uint16_t* Vs, int nb, int hd, int lane,
+                                           int npair_w, const int (&prow)[J], int causal_base,
+                                           const float (&q)[J][E], float (&m)[J], float (&l)[J],
+                                           float (&o)[J][E]) {
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (j >= npair_w) break;
+    float part[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      float acc = 0.f;
+      if (jj < nb) {
+        float kv[E];
+        load_head_slice<E>(Ks + (size_t)jj * hd, lane, kv);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc = fmaf(q[j][e], kv[e], acc);
+      }
+      part[jj] = acc;
+    }
+    MultiReduce<32, 16>::run(part, lane);
+    bool valid = lane < nb;
+    if (causal_base >= 0) valid = valid && (lane <= prow[j]);
+    const float s = valid ? part[0] : -CUDART_INF_F;
+    const float mx = warp_max(s);
+    const float m_new = fmaxf(m[j], mx);
+    if (m_new == -CUDART_INF_F) continue;
+    const float corr = exp2f(m[j] - m_new);
+    const float pj = valid ? exp2f(s - m_new) : 0.f;
+    l[j] = l[j] * corr + warp_sum(pj);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[j][e] *= corr;
+    for (int jj = 0; jj < nb; ++jj) {
+      const float pp = __shfl_sync(0xffffffffu, pj, jj);
+      float vv[E];
+      load_head_slice<E>(Vs + (size_t)jj * hd, lane, vv);
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[j][e] = fmaf(pp, vv[e], o[j][e]);
+    }
+    m[j] = m_new;
+  }
+}
+
+template <int E, int J>
+__device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+                             CSmem& cs, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int hd = E * 32;
+  const int hkv = op.n_kv_heads, G = op.groups;
+  const int b = in.a / hkv, g = in.a % hkv, c = in.b;
+  const int rlo = in.c & 0xff, rhi = in.c >> 8;
+  const int npairs = (rhi - rlo) * G;
+  const int R = p.R;
+  int t0, t1;
+  attn_range(p, op, b, c, t0, t1);
+  const int pos0 = p.positions[b];
+  const int P = kSlotBytes / (4 * hd);
+  const float qscale = rsqrtf((float)hd) * kLog2e;
+
+  float q[J][E], o[J][E], m[J], l[J];
+  int prow[J];
+  int npair_w = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int pr = warp + j * kConsumerWarps;
+    m[j] = -CUDART_INF_F;
+    l[j] = 0.f;
+    prow[j] = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) { o[j][e] = 0.f; q[j][e] = 0.f; }
+    if (pr < npairs) {
+      npair_w = j + 1;
+      const int r = rlo + pr / G, h = pr % G;
+      prow[j] = r;
+      const float* qp = op.in + (size_t)(b * R + r) * op.in_stride + (size_t)(g * G + h) * hd + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) q[j][e] = __ldcg(qp + e) * qscale;
+    }
+  }
+
+  for (int t = t0; t < t1; t += P) {
+    const int np = min(P, t1 - t);
+    ring_wait_full(rg, chunk, p);
+    const uint16_t* Ks = reinterpret_cast<const uint16_t*>(rg.slot_ptr(chunk));
+    const uint16_t* Vs = Ks + kSlotBytes / 4;
+    for (int tb = 0; tb < np; tb += 32)
+      attn_block<E, J>(Ks + (size_t)tb * hd, Vs + (size_t)tb * hd, min(32, np - tb), hd, lane, npair_w, prow, -1,
+                       q, m, l, o);
+    ring_release(rg, chunk, lane);
+    ++chunk;
+  }
+  if (c == op.nchunk - 1) {
+    // the block's own rows, written by the RoPE/append op of this step
+    for (int i = ctid; i < R * hd; i += kConsumerThreads) {
+      const int r = i / hd, e = i % hd;
+      cs.knew[i] = __ldcg(p.kcache + kv_index(p, op, b, g, pos0 + r) + e);
+      cs.vnew[i] = __ldcg(p.vcache + kv_index(p, op, b, g, pos0 + r) + e);
+    }
+    consumer_sync();
+    attn_block<E, J>(cs.knew, cs.vnew, R, hd, lane, npair_w, prow, 0, q, m, l, o);
+    consumer_sync();
+  }
+
+  // partial record of every pair: o (hd floats), then m, l
+  const int stride = p.attn_part_stride;
+  const size_t base_rec = ((size_t)(b * hkv + g) * op.nchunk + c) * R;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (j < npair_w) {
+      const int pr = warp + j * kConsumerWarps;
+      const int r = rlo + pr / G, h = pr % G;
+      float* rec = p.attn_part + ((base_rec + r) * G + h) * stride;
+#pragma unroll
+      for (int e = 0; e < E; ++e) __stcg(rec + lane * E + e, o[j][e]);
+      if (lane == 0) {
+        __stcg(rec + hd, m[j]);
+        __stcg(rec + hd + 1, l[j]);
+      }
+    }
+  }
+  consumer_sync();
+  const int n_split = (R + (rhi - rlo) - 1) / (rhi - rlo);
+  if (ctid == 0) {
+    __threadfence();
+    uint32_t* ctr = p.arrive + ((size_t)op.slot * p.max_batch + b) * hkv + g;
+    const uint32_t old = atomicAdd(ctr, 1u);
+    const int last = (old == (uint32_t)(op.nchunk * n_split - 1)) ? 1 : 0;
+    if (last) {
+      *ctr = 0u;
+      __threadfence();
+    }
+    cs.last = last;
+  }
+  consumer_sync();
+  if (!cs.last) return;
+  // the last arriving chunk combines all partials of (b, g)
+  for (int pr = warp; pr < R * G; pr += kConsumerWarps) {
+    const int r = pr / G, h = pr % G;
+    float M = -CUDART_INF_F;
+    for (int cc = 0; cc < op.nchunk; ++cc) {
+      const float* rec = p.attn_part + ((((size_t)(b * hkv + g) * op.nchunk + cc) * R + r) * G + h) * stride;
+      M = fmaxf(M, __ldcg(rec + hd));
+    }
+    float L = 0.f;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int cc = 0; cc < op.nchunk; ++cc) {
+      const float* rec = p.attn_part + ((((size_t)(b * hkv + g) * op.nchunk + cc) * R + r) * G + h) * stride;
+      const float mc = __ldcg(rec + hd);
+      if (mc == -CUDART_INF_F) continue;
+      const float w = exp2f(mc - M);
+      L += w * __ldcg(rec + hd + 1);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, __ldcg(rec + lane * E + e), acc[e]);
+    }
+    const float inv = 1.0f / L;
+    float* dst = op.out + (size_t)(b * R + r) * op.out_stride + (size_t)(g * G + h) * hd + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) __stcg(dst + e, acc[e] * inv);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Gated delta rule for value columns [jg*8, jg*8+8) of head h of sequence b (warp w owns column
+// jg*8 + w; lane L owns key rows [L*E, L*E+E) of that column). First the rows the caller accepted from
+// the previous call are replayed into the stored state and the result is written back (the committed
+// state); then the new rows advance a register copy and produce outputs, and are stored for replay.
+//   S <- Diag(alpha) S;  u = v - S^T k_hat;  S <- S + beta k_hat u^T;  o = S^T q_hat
+// ------------------------------------------------------------------------------------------------
+__device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int b = in.a, h = in.b, jg = in.c;
+  const int H = op.n_heads, dk = op.dk, dv = op.dv;
+  const int E = dk / 32;  // 1, 2 or 4
+  const int j = jg * op.col_group + warp;
+  if (warp >= op.col_group || j >= dv) return;
+  const bool kda = op.per_channel_decay != 0;
+  const int R = p.R;
+  const int pos0 = p.positions[b];
+  const int a = pos0 - p.seq[b].c_int;
+  const int rec = p.pend_rec;
+  const uint32_t cur = p.epoch & 1u, prev = cur ^ 1u;
+  auto pend_at = [&](uint32_t par, int r) -> float* {
+    return p.pend + (((((size_t)op.slot * 2 + par) * p.max_batch + b) * p.max_rows + r) * H + h) * rec;
+  };
+  float* Sp = p.state + ((((size_t)op.slot * p.max_batch + b) * H + h) * dv + j) * dk + lane * E;
+  float S[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int e = 0; e < E; ++e) S[e] = __ldcg(Sp + e);
+
+  // replay accepted rows of the previous call
+  for (int r = 0; r < a; ++r) {
+    const float* pr = pend_at(prev, r);
+    const float vj = __ldcg(pr + dk + j);
+    const float beta = __ldcg(pr + 2 * dk + dv);
+    float kh[4], al[4];
+    for (int e = 0; e < E; ++e) {
+      kh[e] = __ldcg(pr + lane * E + e);
+      al[e] = kda ? __ldcg(pr + dk + dv + lane * E + e) : __ldcg(pr + dk + dv);
+    }
+    float dot = 0.f;
+    for (int e = 0; e < E; ++e) {
+      S[e] *= al[e];
+      dot = fmaf(S[e], kh[e], dot);
+    }
+    const float u = vj - warp_sum(dot);
+    for (int e = 0; e < E; ++e) S[e] = fmaf(beta * kh[e], u, S[e]);
+  }
+  if (a > 0)
+    for (int e = 0; e < E; ++e) __stcg(Sp + e, S[e]);
+
+  const int offk = H * dk, offv = 2 * H * dk, offa = 2 * H * dk + H * dv;
+  const int offb = offa + (kda ? H * dk : H);
+  const float qs = rsqrtf((float)dk);
+  for (int r = 0; r < R; ++r) {
+    const int n = b * R + r;
+    const float* row = op.in + (size_t)n * op.in_stride;
+    float qv[4], kv[4], al[4];
+    float sq = 0.f, sk = 0.f;
+    for (int e = 0; e < E; ++e) {
+      qv[e] = __ldcg(row + h * dk + lane * E + e);
+      kv[e] = __ldcg(row + offk + h * dk + lane * E + e);
+      sq = fmaf(qv[e], qv[e], sq);
+      sk = fmaf(kv[e], kv[e], sk);
+    }
+    const float iq = rsqrtf(warp_sum(sq) + 1e-6f) * qs;
+    const float ik = rsqrtf(warp_sum(sk) + 1e-6f);
+    const float vj = __ldcg(row + offv + h * dv + j);
+    const float beta = sigmoidf_(__ldcg(row + offb + h));
+    const float alpha_h = kda ? 0.f : sigmoidf_(__ldcg(row + offa + h));
+    float dot = 0.f;
+    for (int e = 0; e < E; ++e) {
+      qv[e] *= iq;
+      kv[e] *= ik;
+      al[e] = kda ? sigmoidf_(__ldcg(row + offa + h * dk + lane * E + e)) : alpha_h;
+      S[e] *= al[e];
+      dot = fmaf(S[e], kv[e], dot);
+    }
+    const float u = vj - warp_sum(dot);
+    float od = 0.f;
+    for (int e = 0; e < E; ++e) {
+      S[e] = fmaf(beta * kv[e], u, S[e]);
+      od = fmaf(S[e], qv[e], od);
+    }
+    const float o = warp_sum(od);
+    if (lane == 0) __stcg(op.out + (size_t)n * op.out_stride + h * dv + j, o);
+    // store the row for replay by the next call
+    float* pw = pend_at(cur, r);
+    if (lane == 0) __stcg(pw + dk + j, vj);
+    if (jg == 0 && warp == 0) {
+      for (int e = 0; e < E; ++e) {
+        __stcg(pw + lane * E + e, kv[e]);
+        if (kda) __stcg(pw + dk + dv + lane * E + e, al[e]);
+      }
+      if (lane == 0) {
+        if (!kda) __stcg(pw + dk + dv, alpha_h);
+        __stcg(pw + 2 * dk + dv, beta);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// final op: greedy argmax over the LM-head partials, sequence bookkeeping, counter reset
+// ------------------------------------------------------------------------------------------------
+__device__ void final_consume(const KParams& p, int ctid) {
+  if (p.argmax) {
+    for (int n = ctid; n < p.N; n += kConsumerThreads) {
+      float bv = -CUDART_INF_F;
+      int bi = 0x7fffffff;
+      for (int q = 0; q < p.n_sm; ++q) {
+        const float2 c = __ldcg(&p.amax_part[(size_t)q * kMaxN + n]);
+        const int ci = __float_as_int(c.y);
+        if (c.x > bv || (c.x == bv && ci < bi)) { bv = c.x; bi = ci; }
+      }
+      p.argmax[n] = bi;
+    }
+  }
+  if (ctid < p.B) {
+    const int pos = p.positions[ctid];
+    SeqState s;
+    s.c_int = pos;
+    s.u_int = p.R;
+    s.c_spec = p.commit_all ? pos + p.R : pos;
+    s.pad = 0;
+    p.seq[ctid] = s;
+  }
+  for (int i = ctid; i < p.n_ops; i += kConsumerThreads) p.counters[i] = 0u;
+}
+
+// ------------------------------------------------------------------------------------------------
+// the two roles
+// ------------------------------------------------------------------------------------------------
+__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
+  const int lane = threadIdx.x & 31;
+  uint32_t chunk = 0;
+  for (int qi = q0; qi < q1; ++qi) {
+    const Instr in = p.instrs[qi];
+    const OpDesc& op = p.ops[in.op];
+    bool ok = true;
+    if (op.type == OP_GEMV) ok = gemv_produce(p, op, in, rg, chunk, lane);
+    else if (op.type == OP_ATTN) ok = attn_produce(p, op, in, rg, chunk, lane);
+    if (!ok) break;
+  }
+  // every issued copy must land before the CTA may exit
+  if (lane == 0) {
+    const uint32_t first = chunk > (uint32_t)kSlots ? chunk - kSlots : 0u;
+    for (uint32_t c = first; c < chunk; ++c) {
+      const unsigned long long t0 = global_timer();
+      while (!mbar_try_wait(&rg.full[c % kSlots], (c / kSlots) & 1u)) {
+        if (global_timer() - t0 > 200000000ull) break;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <int RG, int NR>
+__device__ __forceinline__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                                              uint32_t& chunk, CSmem& cs, int ctid) {
+  gemv_consume<RG, NR>(p, op, in, rg, chunk, cs, ctid);
+}
+
+__device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, int q0, int q1, int ctid) {
+  uint32_t chunk = 0;
+  const int nr = p.N <= 1 ? 1 : p.N <= 2 ? 2 : p.N <= 4 ? 4 : 8;
+  for (int qi = q0; qi < q1; ++qi) {
+    const Instr in = p.instrs[qi];
+    const OpDesc& op = p.ops[in.op];
+    if (ctid == 0) {
+      int ok = 1;
+      for (int d = 0; d < op.n_deps && ok; ++d) {
+        const int dop = op.deps[d];
+        ok = wait_counter(&p.counters[dop], (uint32_t)p.ops[dop].n_instr, p) ? 1 : 0;
+      }
+      if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) ok = 0;
+      cs.flag = ok;
+    }
+    consumer_sync();
+    if (!cs.flag) break;
+    switch (op.type) {
+      case OP_EMBED: embed_consume(p, op, in, ctid); break;
+      case OP_GEMV:
+        if (nr == 1) gemv_dispatch<16, 1>(p, op, in, rg, chunk, cs, ctid);
+        else if (nr == 2) gemv_dispatch<16, 2>(p, op, in, rg, chunk, cs, ctid);
+        else if (nr == 4) gemv_dispatch<16, 4>(p, op, in, rg, chunk, cs, ctid);
+        else gemv_dispatch<8, 8>(p, op, in, rg, chunk, cs, ctid);
+        break;
+      case OP_ROPE_APPEND: rope_append_consume(p, op, ctid); break;
+      case OP_ATTN: {
+        const int pairs = ((in.c >> 8) - (in.c & 0xff)) * op.groups;
+        const int J = (pairs + kConsumerWarps - 1) / kConsumerWarps;
+        if (op.head_dim == 256) {
+          if (J <= 1) attn_consume<8, 1>(p, op, in, rg, chunk, cs, ctid);
+          else if (J <= 2) attn_consume<8, 2>(p, op, in, rg, chunk, cs, ctid);
+          else attn_consume<8, 4>(p, op, in, rg, chunk, cs, ctid);
+        } else if (op.head_dim == 128) {
+          if (J <= 1) attn_consume<4, 1>(p, op, in, rg, chunk, cs, ctid);
+          else if (J <= 2) attn_consume<4, 2>(p, op, in, rg, chunk, cs, ctid);
+          else attn_consume<4, 4>(p, op, in, rg, chunk, cs, ctid);
+        } else {
+          if (J <= 1) attn_consume<2, 1>(p, op, in, rg, chunk, cs, ctid);
+          else if (J <= 2) attn_consume<2, 2>(p, op, in, rg, chunk, cs, ctid);
+          else attn_consume<2, 4>(p, op, in, rg, chunk, cs, ctid);
+        }
+        break;
+      }
+      case OP_DELTA: delta_consume(p, op, in, ctid); break;
+      case OP_FINAL: final_consume(p, ctid); break;
+      default: break;
+    }
+    consumer_sync();
+    if (ctid == 0 && op.type != OP_FINAL) {
+      __threadfence();
+      red_release_add(&p.counters[in.op], 1u);
+    }
+  }
+}
+
+// 1 = run, 0 = invalid input, 2 = abort already raised
+__device__ int validate(const KParams& p) {
+  if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) return 2;
+  for (int b = 0; b < p.B; ++b) {
+    const int pos = p.positions[b];
+    const SeqState s = p.seq[b];
+    if (pos < 0 || pos < s.c_spec || pos > s.c_int + s.u_int || pos + p.R > p.max_ctx) return 0;
+    for (int r = 0; r < p.R; ++r) {
+      const int t = p.tokens[b * p.tok_stride + r];
+      if (t < 0 || t >= p.V) return 0;
+    }
+  }
+  return 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ring rg;
+  rg.base = smem;
+  rg.full = reinterpret_cast<uint64_t*>(smem + (size_t)kSlots * kSlotBytes);
+  rg.empty = rg.full + kSlots;
+  CSmem& cs = *reinterpret_cast<CSmem*>(rg.empty + kSlots);
+  __shared__ int s_state;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_state = validate(p);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&rg.full[i], 1);
+      mbar_init(&rg.empty[i], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (s_state != 1) {
+    if (s_state == 0 && blockIdx.x == 0 && tid == 0) atomicCAS(p.status, 0, kStatusDevice);
+    return;
+  }
+  const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
+  if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1);
+  else run_consumer(p, rg, cs, q0, q1, tid);
+}
+
+// ------------------------------------------------------------------------------------------------
+// helper kernels (set-up, not on the decode path)
+// ------------------------------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* tab, int max_ctx, int rot_dim, double theta) {
+  const int half = rot_dim / 2;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= max_ctx * half) return;
+  const int pos = i / half, k = i % half;
+  const double ang = (double)pos * pow(theta, -2.0 * (double)k / (double)rot_dim);
+  double s, c;
+  sincos(ang, &s, &c);
+  tab[i] = make_float2((float)c, (float)s);
+}
+
+__global__ void fill_i32_kernel(int32_t* dst, int n, int32_t value) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = value;
+}
+
+}  // namespace mk
+
+// ---- host-side launch wrappers (used by mk_host.cu) ---------------------------------------------
+namespace mk {
+
+size_t kernel_smem_bytes() { return kSmemBytes; }
+
+cudaError_t kernel_configure() {
+  return cudaFuncSetAttribute(megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream) {
+  void* args[] = {const_cast<KParams*>(&p)};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(megakernel), dim3(n_sm), dim3(kThreads), args,
+                                     kSmemBytes, stream);
+}
+
+cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream) {
+  const int n = max_ctx * (rot_dim / 2);
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(tab, max_ctx, rot_dim, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t stream) {
+  fill_i32_kernel<<<(n + 255) / 256, 256, 0, stream>>>(dst, n, value);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

@@ -1,0 +1,110 @@
+"""Shared driver for the GPU parity tests: runs the CUDA megakernel (through the C ABI) and the oracle
+on the same seeded inputs and compares every step.
+
+Comparison rules (floating point decides an integer here, so near-ties are handled explicitly):
+  * logits: max |gpu - oracle| <= tol over every row of every step;
+  * greedy tokens: equal, unless the oracle's top-1 / top-2 gap is below 2 * tol, in which case either
+    token is accepted; the oracle's token is fed to both sides (teacher forcing), so one near-tie never
+    makes the two runs diverge.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import Oracle
+from synthetic import make_tokens, make_weights
+
+
+class Report:
+    def __init__(self):
+        self.max_err = 0.0
+        self.steps = 0
+        self.token_mismatch = 0
+        self.near_ties = 0
+        self.errors = []
+
+
+def compare_logits(gpu: np.ndarray, ref: np.ndarray, tol: float, rep: Report, what: str):
+    err = float(np.max(np.abs(gpu.astype(np.float64) - ref)))
+    rep.max_err = max(rep.max_err, err)
+    if not np.isfinite(err) or err > tol:
+        rep.errors.append(f"{what}: max |diff| {err:.4g} > {tol}")
+    g_arg = gpu.argmax(-1)
+    o_sorted = np.sort(ref, axis=-1)
+    gap = o_sorted[..., -1] - o_sorted[..., -2]
+    o_arg = ref.argmax(-1)
+    for idx in np.ndindex(o_arg.shape):
+        if g_arg[idx] != o_arg[idx]:
+            if gap[idx] < 2 * tol:
+                rep.near_ties += 1
+            else:
+                rep.token_mismatch += 1
+                rep.errors.append(f"{what} row {idx}: greedy {g_arg[idx]} vs oracle {o_arg[idx]} (gap {gap[idx]:.3g})")
+
+
+def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_verify: int = 8,
+             seed: int = 0, tol: float = 2e-2, max_ctx: int | None = None, check_argmax: bool = True):
+    """Prefill T context tokens per sequence, then `decode_steps` greedy single-row steps, then one
+    R_verify-row verify step per entry of verify_accepts (the entry is the accepted length of that block,
+    applied by the next call's positions)."""
+    from decode_megakernel_04_gb300 import Megakernel
+
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=seed, device=dev)
+    rows_max = R_verify if verify_accepts else 1
+    extra = decode_steps + (len(verify_accepts) + 1) * R_verify + 8
+    max_ctx = max_ctx or (T + extra)
+    mk = Megakernel(cfg, w, max_batch=B, max_rows=max(rows_max, 8), max_ctx=max_ctx)
+    orc = Oracle(cfg, w, B, max_ctx)
+    rep = Report()
+    ctx = make_tokens(seed, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
+    mk.prefill(ctx)
+    orc.prefill(ctx.cpu().numpy())
+    pos = np.full(B, T, dtype=np.int64)
+    tok = make_tokens(seed, "start", (B, 1), cfg.vocab).numpy().astype(np.int64)
+    V = cfg.vocab
+    for s in range(decode_steps):
+        logits = torch.empty((B, V), device=dev, dtype=torch.float32)
+        am = torch.empty((B,), device=dev, dtype=torch.int32)
+        mk.step(torch.from_numpy(tok.astype(np.int32)).to(dev), torch.from_numpy(pos.astype(np.int32)).to(dev),
+                logits, am)
+        ref = orc.step(tok, pos)[:, 0]
+        st = mk.status()
+        assert st == 0, f"device status {st}"
+        g = logits.cpu().numpy()
+        compare_logits(g, ref, tol, rep, f"decode step {s}")
+        if check_argmax:
+            # the kernel's own argmax must be the argmax of the logits it wrote
+            assert np.array_equal(am.cpu().numpy(), g.argmax(-1)), "in-kernel argmax differs from logits argmax"
+        tok = ref.argmax(-1)[:, None].astype(np.int64)
+        pos = pos + 1
+        rep.steps += 1
+    for vi, acc in enumerate(verify_accepts):
+        drafts = make_tokens(seed, f"draft{vi}", (B, R_verify - 1), cfg.vocab).numpy().astype(np.int64)
+        block = np.concatenate([tok, drafts], axis=1)
+        logits = torch.empty((B * R_verify, V), device=dev, dtype=torch.float32)
+        am = torch.empty((B * R_verify,), device=dev, dtype=torch.int32)
+        mk.step(torch.from_numpy(block.astype(np.int32)).to(dev).contiguous(),
+                torch.from_numpy(pos.astype(np.int32)).to(dev), logits, am)
+        ref = orc.step(block, pos)
+        st = mk.status()
+        assert st == 0, f"device status {st}"
+        g = logits.cpu().numpy().reshape(B, R_verify, V)
+        compare_logits(g, ref, tol, rep, f"verify block {vi}")
+        if check_argmax:
+            assert np.array_equal(am.cpu().numpy().reshape(B, R_verify), g.argmax(-1))
+        # accept `acc` rows: the next anchor is the oracle's greedy token after the last accepted row
+        tok = ref[:, acc - 1].argmax(-1)[:, None].astype(np.int64)
+        pos = pos + acc
+        rep.steps += 1
+    # one more decode step to check the commit of the last verify block
+    if verify_accepts:
+        logits = torch.empty((B, V), device=dev, dtype=torch.float32)
+        mk.step(torch.from_numpy(tok.astype(np.int32)).to(dev), torch.from_numpy(pos.astype(np.int32)).to(dev),
+                logits, None)
+        ref = orc.step(tok, pos)[:, 0]
+        assert mk.status() == 0
+        compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
+    mk.close()
+    return rep

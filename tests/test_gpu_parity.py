@@ -1,0 +1,109 @@
+"""GPU parity: the CUDA megakernel (called through the C ABI) against the oracle, element by element, on
+the same seeded inputs. Logits within 2e-2 max-abs (bf16 weights, fp32 accumulation) and identical
+greedy tokens except at oracle near-ties (see tests/gpu_harness.py)."""
+import numpy as np
+import pytest
+import torch
+
+from synthetic import config, make_tokens, make_weights
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from decode_megakernel_04_gb300 import _build
+    _build.build()
+
+
+def _check(rep):
+    assert not rep.errors, "\n".join(rep.errors[:10])
+    assert rep.token_mismatch == 0
+
+
+def test_tiny_dense_greedy_16_steps():
+    """The tiny dense workload as specified: batch 1, 128-token context, 16 greedy steps."""
+    from gpu_harness import run_case
+    rep = run_case(config("tiny_dense"), B=1, T=128, decode_steps=16, tol=TOL_BF16)
+    _check(rep)
+
+
+def test_tiny_dense_batch_and_verify():
+    """Batch 3, ragged context (37, not a multiple of the 8-row prefill chunk), decode then 8-row verify
+    blocks with accepted lengths 3, 8, 1 and 6."""
+    from gpu_harness import run_case
+    rep = run_case(config("tiny_dense"), B=3, T=37, decode_steps=2, verify_accepts=(3, 8, 1, 6), tol=TOL_BF16)
+    _check(rep)
+
+
+def test_tiny_dense_single_token_context():
+    from gpu_harness import run_case
+    rep = run_case(config("tiny_dense"), B=2, T=1, decode_steps=3, tol=TOL_BF16)
+    _check(rep)
+
+
+def test_hybrid_gdn_gqa_full_width_4_layers():
+    """Full-width hybrid stack (d 5120, GQA 24/4 x 256, GDN 16 x 128, FFN 17408, vocab 151936), cut to 4
+    layers (3 GDN + 1 GQA), batch 2, 61-token context, greedy decode and verify blocks."""
+    from gpu_harness import run_case
+    cfg = config("hybrid_gdn_gqa", n_layers=4)
+    rep = run_case(cfg, B=2, T=61, decode_steps=2, verify_accepts=(3, 6), tol=TOL_BF16)
+    _check(rep)
+
+
+def test_hybrid_batch8_decode():
+    from gpu_harness import run_case
+    cfg = config("hybrid_gdn_gqa", n_layers=4)
+    rep = run_case(cfg, B=8, T=20, decode_steps=2, tol=TOL_BF16)
+    _check(rep)
+
+
+def test_invalid_inputs_set_device_status():
+    """A token outside the vocabulary and a position outside the committed window are rejected on the
+    device (MK_ERR_DEVICE) without a fault; the handle keeps working afterwards."""
+    from decode_megakernel_04_gb300 import Megakernel
+    cfg = config("tiny_dense")
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=0, device=dev)
+    mk = Megakernel(cfg, w, max_batch=1, max_rows=8, max_ctx=64)
+    mk.prefill(make_tokens(0, "ctx", (1, 10), cfg.vocab, device=dev))
+    logits = torch.empty((1, cfg.vocab), device=dev)
+    bad_tok = torch.tensor([[cfg.vocab]], dtype=torch.int32, device=dev)
+    mk.step(bad_tok, torch.tensor([10], dtype=torch.int32, device=dev), logits)
+    assert mk.status() == 6
+    good = torch.tensor([[5]], dtype=torch.int32, device=dev)
+    mk.step(good, torch.tensor([12], dtype=torch.int32, device=dev), logits)   # beyond c + u = 10
+    assert mk.status() == 6
+    mk.step(good, torch.tensor([10], dtype=torch.int32, device=dev), logits)
+    assert mk.status() == 0
+    assert torch.isfinite(logits).all()
+    mk.close()
+
+
+def test_host_entry_point_matches_device_entry_point():
+    """mk_decode_step_host (host buffers, copies inside) returns the same greedy tokens and logits as
+    mk_decode_step on an identically prepared handle."""
+    from decode_megakernel_04_gb300 import Megakernel
+    cfg = config("tiny_dense")
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=1, device=dev)
+    ctx = make_tokens(1, "ctx", (2, 16), cfg.vocab, device=dev)
+    a = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64)
+    b = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64)
+    a.prefill(ctx)
+    b.prefill(ctx)
+    tok = np.array([[3], [9]], dtype=np.int32)
+    pos = np.array([16, 16], dtype=np.int32)
+    la = torch.empty((2, cfg.vocab), device=dev)
+    ama = torch.empty((2,), dtype=torch.int32, device=dev)
+    a.step(torch.from_numpy(tok).to(dev), torch.from_numpy(pos).to(dev), la, ama)
+    assert a.status() == 0
+    amb = np.zeros(2, dtype=np.int32)
+    lb = np.zeros((2, cfg.vocab), dtype=np.float32)
+    b.step_host(tok, pos, amb, lb)
+    np.testing.assert_array_equal(ama.cpu().numpy(), amb)
+    np.testing.assert_array_equal(la.cpu().numpy(), lb)
+    a.close()
+    b.close()
