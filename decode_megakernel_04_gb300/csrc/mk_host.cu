@@ -176,6 +176,39 @@ mk_status check_desc(mk_handle* h, const mk_model_desc& d, const mk_weights& w) 
   return MK_OK;
 }
 
+// Layer slots and activation strides of a handle, derived from its model description alone.
+void derive_layout(mk_handle* h) {
+  const mk_model_desc& D = h->desc;
+  h->slot.resize(D.n_layers);
+  h->n_gqa = h->n_delta = h->n_mla = 0;
+  for (int i = 0; i < D.n_layers; ++i) {
+    if (D.mixer[i] == MK_MIXER_GQA) h->slot[i] = h->n_gqa++;
+    else if (D.mixer[i] == MK_MIXER_MLA) h->slot[i] = h->n_mla++;
+    else h->slot[i] = h->n_delta++;
+  }
+  h->nmax = D.max_batch * D.max_rows;
+  int proj = 8, attn = 8;
+  for (int i = 0; i < D.n_layers; ++i) {
+    const int m = D.mixer[i];
+    if (m == MK_MIXER_GQA) {
+      proj = std::max(proj, (D.n_q_heads + 2 * D.n_kv_heads) * D.head_dim);
+      attn = std::max(attn, D.n_q_heads * D.head_dim);
+    } else if (is_delta(m)) {
+      proj = std::max(proj, delta_proj_cols(D, m));
+      attn = std::max(attn, D.lin_heads * D.lin_dv);
+    }
+  }
+  h->proj_stride = round_up(proj, 8);
+  h->attn_stride = round_up(attn, 8);
+  h->hbuf_stride = round_up(std::max(D.ffn_dim, 8), 8);
+  h->max_ops = 16 * D.n_layers + 16;
+  if (h->n_gqa) {
+    h->attn_part_stride = D.head_dim + 4;
+    h->rot_dim = D.head_dim;
+  }
+  if (h->n_delta) h->pend_rec = round_up(2 * D.lin_dk + D.lin_dv + 1, 4);
+}
+
 // ------------------------------------------------------------------------------------------------
 // scheduler
 // ------------------------------------------------------------------------------------------------
@@ -239,7 +272,15 @@ OpDesc gemv_desc(int K, std::initializer_list<std::pair<const void*, int>> mats)
   return d;
 }
 
-Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
+// Host-side program of one (batch, rows, head) shape: the op list, the flattened per-SM queues and their
+// offsets. Reads the handle's shape, weights, slots and activation buffer pointers; touches no device.
+struct HostProgram {
+  std::vector<OpDesc> ops;
+  std::vector<Instr> flat;
+  std::vector<int32_t> qoff;
+};
+
+mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& hp) {
   const mk_model_desc& D = h->desc;
   const int N = B * R;
   const int d = D.d_model;
@@ -387,23 +428,31 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     bld.place(op, 0, 0, 0, 0);
   }
 
+  if ((int)bld.ops.size() > h->max_ops)
+    return fail(h, MK_ERR_UNSUPPORTED, "program has %d ops, more than the %d counters allocated",
+                (int)bld.ops.size(), h->max_ops);
+  hp.ops = std::move(bld.ops);
+  hp.flat.clear();
+  hp.qoff.assign(h->n_sm + 1, 0);
+  for (int s = 0; s < h->n_sm; ++s) {
+    hp.qoff[s] = (int32_t)hp.flat.size();
+    hp.flat.insert(hp.flat.end(), bld.q[s].begin(), bld.q[s].end());
+  }
+  hp.qoff[h->n_sm] = (int32_t)hp.flat.size();
+  return MK_OK;
+}
+
+Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
   Program prog;
   prog.B = B;
   prog.R = R;
   prog.head = head;
-  prog.n_ops = (int)bld.ops.size();
-  if (prog.n_ops > h->max_ops) {
-    *st = fail(h, MK_ERR_UNSUPPORTED, "program has %d ops, more than the %d counters allocated", prog.n_ops,
-               h->max_ops);
-    return prog;
-  }
-  std::vector<Instr> flat;
-  std::vector<int32_t> qoff(h->n_sm + 1, 0);
-  for (int s = 0; s < h->n_sm; ++s) {
-    qoff[s] = (int32_t)flat.size();
-    flat.insert(flat.end(), bld.q[s].begin(), bld.q[s].end());
-  }
-  qoff[h->n_sm] = (int32_t)flat.size();
+  HostProgram hp;
+  *st = construct_program(h, B, R, head, hp);
+  if (*st != MK_OK) return prog;
+  const std::vector<Instr>& flat = hp.flat;
+  const std::vector<int32_t>& qoff = hp.qoff;
+  prog.n_ops = (int)hp.ops.size();
   prog.n_instr = (int)flat.size();
   cudaError_t e;
   if ((e = cudaMalloc(&prog.d_ops, sizeof(OpDesc) * prog.n_ops)) != cudaSuccess ||
@@ -412,7 +461,7 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     *st = cuda_fail(h, e, "program allocation");
     return prog;
   }
-  cudaMemcpy(prog.d_ops, bld.ops.data(), sizeof(OpDesc) * prog.n_ops, cudaMemcpyHostToDevice);
+  cudaMemcpy(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * prog.n_ops, cudaMemcpyHostToDevice);
   cudaMemcpy(prog.d_instr, flat.data(), sizeof(Instr) * prog.n_instr, cudaMemcpyHostToDevice);
   e = cudaMemcpy(prog.d_qoff, qoff.data(), sizeof(int32_t) * (h->n_sm + 1), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) *st = cuda_fail(h, e, "program upload");
@@ -435,12 +484,10 @@ Program* get_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
   return &h->programs.back();
 }
 
-mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const int32_t* positions, int B, int R,
-                      float* logits, int32_t* argmax, bool commit_all, cudaStream_t stream) {
-  mk_status st = MK_OK;
-  const bool head = logits != nullptr || argmax != nullptr;
-  Program* prog = get_program(h, B, R, head, &st);
-  if (!prog) return st;
+// Fills the kernel parameters from the handle's buffers and the device copy of a program; launches.
+mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* tokens, int tok_stride,
+                         const int32_t* positions, int B, int R, float* logits, int32_t* argmax, bool commit_all,
+                         cudaStream_t stream) {
   const mk_model_desc& D = h->desc;
   KParams p;
   std::memset(&p, 0, sizeof(p));
@@ -496,6 +543,15 @@ mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const
   return MK_OK;
 }
 
+mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const int32_t* positions, int B, int R,
+                      float* logits, int32_t* argmax, bool commit_all, cudaStream_t stream) {
+  mk_status st = MK_OK;
+  const bool head = logits != nullptr || argmax != nullptr;
+  Program* prog = get_program(h, B, R, head, &st);
+  if (!prog) return st;
+  return launch_program(h, prog, tokens, tok_stride, positions, B, R, logits, argmax, commit_all, stream);
+}
+
 }  // namespace
 
 // ==================================================================================================
@@ -539,29 +595,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
   }
 
   const mk_model_desc& D = h->desc;
-  h->slot.resize(D.n_layers);
-  for (int i = 0; i < D.n_layers; ++i) {
-    if (D.mixer[i] == MK_MIXER_GQA) h->slot[i] = h->n_gqa++;
-    else if (D.mixer[i] == MK_MIXER_MLA) h->slot[i] = h->n_mla++;
-    else h->slot[i] = h->n_delta++;
-  }
+  derive_layout(h);
   const int Bm = D.max_batch, Rm = D.max_rows;
-  h->nmax = Bm * Rm;
-  int proj = 8, attn = 8;
-  for (int i = 0; i < D.n_layers; ++i) {
-    const int m = D.mixer[i];
-    if (m == MK_MIXER_GQA) {
-      proj = std::max(proj, (D.n_q_heads + 2 * D.n_kv_heads) * D.head_dim);
-      attn = std::max(attn, D.n_q_heads * D.head_dim);
-    } else if (is_delta(m)) {
-      proj = std::max(proj, delta_proj_cols(D, m));
-      attn = std::max(attn, D.lin_heads * D.lin_dv);
-    }
-  }
-  h->proj_stride = round_up(proj, 8);
-  h->attn_stride = round_up(attn, 8);
-  h->hbuf_stride = round_up(std::max(D.ffn_dim, 8), 8);
-  h->max_ops = 16 * D.n_layers + 16;
 
 #define ALLOC(ptr, count) \
   if ((st = dev_alloc(h, &h->ptr, (size_t)(count), #ptr)) != MK_OK) goto fail_out
@@ -585,16 +620,13 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const size_t cache = (size_t)h->n_gqa * Bm * hkv * D.max_ctx * hd;
     ALLOC(kcache, cache);
     ALLOC(vcache, cache);
-    h->attn_part_stride = hd + 4;
     const size_t recs = (size_t)std::max(h->n_sm, Bm * hkv) * Rm * G * 2;
     ALLOC(attn_part, recs * h->attn_part_stride);
     ALLOC(arrive, (size_t)h->n_gqa * Bm * hkv);
-    h->rot_dim = hd;
   }
   if (h->n_delta) {
     const int H = D.lin_heads, dk = D.lin_dk, dv = D.lin_dv;
     ALLOC(state, (size_t)h->n_delta * Bm * H * dv * dk);
-    h->pend_rec = round_up(2 * dk + dv + 1, 4);
     ALLOC(pend, (size_t)h->n_delta * 2 * Bm * Rm * H * h->pend_rec);
   }
   if (h->rot_dim) {
