@@ -53,8 +53,13 @@ class Info(C.Structure):
                 ("ring_slot_bytes", _I), ("n_ops_last", _I), ("device_bytes", C.c_int64)]
 
 
+class StateBuffers(C.Structure):
+    """Caller-owned persistent buffers of mk_decode_step_static (see include/mk.h)."""
+    _fields_ = [("kcache", _P), ("vcache", _P), ("state", _P), ("pending", _P), ("seq", _P), ("epoch", C.c_uint32)]
+
+
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
-           "mk_last_error", "mk_get_info", "mk_destroy"]
+           "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static"]
 
 _lib = None
 
@@ -82,7 +87,10 @@ def load(path: str | None = None) -> C.CDLL:
     lib.mk_get_info.argtypes = [_P, C.POINTER(Info)]
     lib.mk_destroy.argtypes = [_P]
     lib.mk_destroy.restype = None
-    for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info"):
+    lib.mk_decode_step_static.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.POINTER(StateBuffers),
+                                          _P, _P, C.c_int, C.c_int, _P, _P, _P]
+    for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
+              "mk_decode_step_static"):
         getattr(lib, f).restype = C.c_int
     if path is None:
         _lib = lib

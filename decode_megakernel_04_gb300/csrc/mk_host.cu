@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -763,3 +764,175 @@ void mk_destroy(mk_handle* h) {
 }
 
 }  // extern "C"
+
+// ==================================================================================================
+// mk_decode_step_static: the same step with no device allocation. Its working memory is one static
+// device array of MK_STATIC_SCRATCH_BYTES; the caller owns the persistent buffers (caches, states).
+// ==================================================================================================
+namespace {
+
+constexpr int kMaxStaticDevices = 64;
+
+// Working memory of mk_decode_step_static. In host code this name is only a host-side stand-in for
+// the device array: its device address comes from cudaGetSymbolAddress (static_scratch_address).
+static __device__ __align__(256) unsigned char g_static_scratch[MK_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_addr[kMaxStaticDevices] = {};
+
+// Device address of the static array on `device`, which must be current. Resolved once per device.
+mk_status static_scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxStaticDevices) return MK_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[device]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess || !ptr) {
+      fprintf(stderr, "mk_decode_step_static: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
+      return MK_ERR_CUDA;
+    }
+    g_static_addr[device] = ptr;
+  }
+  *out = g_static_addr[device];
+  return MK_OK;
+}
+
+size_t carve(size_t& off, size_t bytes) {
+  off = (off + 255) & ~size_t(255);
+  const size_t at = off;
+  off += std::max<size_t>(bytes, 16);
+  return at;
+}
+
+}  // namespace
+
+extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_weights* weights,
+                                           mk_state_buffers* state, const int32_t* tokens,
+                                           const int32_t* positions, int batch, int rows, float* logits_out,
+                                           int32_t* argmax_out, void* stream) {
+  if (!desc || !weights || !state || !tokens || !positions) return MK_ERR_INVALID_ARG;
+  if (!logits_out && !argmax_out) return MK_ERR_INVALID_ARG;
+  mk_handle tmp;  // describes the step; every buffer pointer below is the caller's or in the static array
+  tmp.desc = *desc;
+  tmp.w = *weights;
+  mk_status st = check_desc(&tmp, tmp.desc, tmp.w);
+  if (st != MK_OK) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
+    return st;
+  }
+  const mk_model_desc& D = tmp.desc;
+  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows) return MK_ERR_INVALID_ARG;
+  cudaError_t e = cudaGetDevice(&tmp.device);
+  if (e != cudaSuccess) return MK_ERR_CUDA;
+  int coop = 0, smem_optin = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, tmp.device);
+  cudaDeviceGetAttribute(&tmp.n_sm, cudaDevAttrMultiProcessorCount, tmp.device);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, tmp.device);
+  if (!coop || smem_optin < (int)kernel_smem_bytes()) return MK_ERR_UNSUPPORTED;
+  if (kernel_configure() != cudaSuccess) return MK_ERR_CUDA;
+  derive_layout(&tmp);
+  if (!state->seq || (tmp.n_gqa && (!state->kcache || !state->vcache)) ||
+      (tmp.n_delta && (!state->state || !state->pending))) {
+    fprintf(stderr, "mk_decode_step_static: a persistent buffer this model needs is NULL\n");
+    return MK_ERR_INVALID_ARG;
+  }
+  void* base_v = nullptr;
+  if ((st = static_scratch_address(tmp.device, &base_v)) != MK_OK) return st;
+  unsigned char* base = static_cast<unsigned char*>(base_v);
+
+  // carve the working memory of this step out of the static array
+  const int N = batch * rows;
+  const int hkv = std::max(D.n_kv_heads, 1);
+  size_t off = 0;
+  const size_t o_counters = carve(off, sizeof(uint32_t) * tmp.max_ops);
+  const size_t arrive_bytes = sizeof(uint32_t) * (size_t)tmp.n_gqa * D.max_batch * hkv;
+  const size_t o_arrive = carve(off, arrive_bytes);
+  const size_t o_status = carve(off, 16);
+  const size_t o_abort = carve(off, 16);
+  const size_t o_x = carve(off, sizeof(float) * (size_t)N * D.d_model);
+  const size_t o_proj = carve(off, sizeof(float) * (size_t)N * tmp.proj_stride);
+  const size_t o_attn = carve(off, sizeof(float) * (size_t)N * tmp.attn_stride);
+  const size_t o_hbuf = carve(off, sizeof(float) * (size_t)N * tmp.hbuf_stride);
+  const size_t o_ssq = carve(off, sizeof(float) * (size_t)(2 * D.n_layers + 1) * tmp.n_sm * kMaxN);
+  const size_t o_amax = carve(off, sizeof(float2) * (size_t)tmp.n_sm * kMaxN);
+  size_t o_apart = 0, o_rope = 0;
+  if (tmp.n_gqa) {
+    const int G = D.n_q_heads / D.n_kv_heads;
+    const size_t recs = (size_t)std::max(tmp.n_sm, batch * hkv) * rows * G * 2;
+    o_apart = carve(off, sizeof(float) * recs * tmp.attn_part_stride);
+  }
+  if (tmp.rot_dim) o_rope = carve(off, sizeof(float2) * (size_t)D.max_ctx * (tmp.rot_dim / 2));
+  tmp.counters = reinterpret_cast<uint32_t*>(base + o_counters);
+  tmp.arrive = tmp.n_gqa ? reinterpret_cast<uint32_t*>(base + o_arrive) : nullptr;
+  tmp.status = reinterpret_cast<int32_t*>(base + o_status);
+  tmp.abort_flag = reinterpret_cast<int32_t*>(base + o_abort);
+  tmp.x = reinterpret_cast<float*>(base + o_x);
+  tmp.proj = reinterpret_cast<float*>(base + o_proj);
+  tmp.attn_out = reinterpret_cast<float*>(base + o_attn);
+  tmp.hbuf = reinterpret_cast<float*>(base + o_hbuf);
+  tmp.ssq = reinterpret_cast<float*>(base + o_ssq);
+  tmp.amax_part = reinterpret_cast<float2*>(base + o_amax);
+  tmp.attn_part = tmp.n_gqa ? reinterpret_cast<float*>(base + o_apart) : nullptr;
+  tmp.rope = tmp.rot_dim ? reinterpret_cast<float2*>(base + o_rope) : nullptr;
+  tmp.kcache = static_cast<uint16_t*>(state->kcache);
+  tmp.vcache = static_cast<uint16_t*>(state->vcache);
+  tmp.state = state->state;
+  tmp.pend = state->pending;
+  tmp.seq = reinterpret_cast<SeqState*>(state->seq);
+  tmp.epoch = state->epoch;
+
+  const bool head = logits_out != nullptr || argmax_out != nullptr;
+  HostProgram hp;
+  if ((st = construct_program(&tmp, batch, rows, head, hp)) != MK_OK) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
+    return st;
+  }
+  const size_t o_ops = carve(off, sizeof(OpDesc) * hp.ops.size());
+  const size_t o_instr = carve(off, sizeof(Instr) * hp.flat.size());
+  const size_t o_qoff = carve(off, sizeof(int32_t) * hp.qoff.size());
+  if (off > (size_t)MK_STATIC_SCRATCH_BYTES) {
+    fprintf(stderr,
+            "mk_decode_step_static: this step needs %zu bytes of working memory, more than the %u-byte static "
+            "array (use mk_create / mk_decode_step, or fewer rows per call)\n",
+            off, (unsigned)MK_STATIC_SCRATCH_BYTES);
+    return MK_ERR_UNSUPPORTED;
+  }
+  Program prog;
+  prog.B = batch;
+  prog.R = rows;
+  prog.head = head;
+  prog.d_ops = reinterpret_cast<OpDesc*>(base + o_ops);
+  prog.d_instr = reinterpret_cast<Instr*>(base + o_instr);
+  prog.d_qoff = reinterpret_cast<int32_t*>(base + o_qoff);
+  prog.n_ops = (int)hp.ops.size();
+  prog.n_instr = (int)hp.flat.size();
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((e = cudaMemcpyAsync(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * hp.ops.size(), cudaMemcpyHostToDevice, s)) !=
+          cudaSuccess ||
+      (e = cudaMemcpyAsync(prog.d_instr, hp.flat.data(), sizeof(Instr) * hp.flat.size(), cudaMemcpyHostToDevice,
+                           s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(prog.d_qoff, hp.qoff.data(), sizeof(int32_t) * hp.qoff.size(), cudaMemcpyHostToDevice,
+                           s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(tmp.counters, 0, sizeof(uint32_t) * tmp.max_ops, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(tmp.status, 0, 16, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(tmp.abort_flag, 0, 16, s)) != cudaSuccess ||
+      (tmp.arrive && (e = cudaMemsetAsync(tmp.arrive, 0, arrive_bytes, s)) != cudaSuccess)) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
+    return MK_ERR_CUDA;
+  }
+  if (tmp.rot_dim && (e = rope_table_launch(tmp.rope, D.max_ctx, tmp.rot_dim, (double)D.rope_theta, s)) != cudaSuccess) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
+    return MK_ERR_CUDA;
+  }
+  st = launch_program(&tmp, &prog, tokens, rows, positions, batch, rows, logits_out, argmax_out, false, s);
+  state->epoch = tmp.epoch;
+  if (st != MK_OK) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
+    return st;
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return MK_ERR_CUDA;
+  int32_t code = 0;
+  if ((e = cudaMemcpy(&code, tmp.status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess) return MK_ERR_CUDA;
+  return (mk_status)code;
+}

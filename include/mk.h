@@ -192,6 +192,52 @@ mk_status mk_get_info(const mk_handle* h, mk_info* out);
 /* Synchronises the device, frees everything the handle owns. NULL is ignored. */
 void mk_destroy(mk_handle* h);
 
+/* ---- A decode step that allocates no device memory ---------------------------------------------
+ * The source pages have no counterpart for this call; it is a convenience of this library.
+ * Some callers cannot call cudaMalloc at decode time: a serving process that hands all free HBM to its
+ * own pool up front (so a later cudaMalloc fails or breaks the pool's accounting), a plug-in that runs
+ * inside a host framework which owns device memory, or a latency-critical loop that cannot afford
+ * cudaMalloc's implicit device synchronisation. mk_decode_step_static runs the same kernel as
+ * mk_decode_step without a handle: the caller passes the model, the weights, its own persistent buffers
+ * (below) and the step's inputs and outputs, and the step's working memory (activations, partial
+ * results, inter-SM counters, the instruction queues, the RoPE table) lives in one statically sized
+ * device array inside libmk, MK_STATIC_SCRATCH_BYTES long, which every GPU that loads the library keeps
+ * until the process exits.
+ *
+ * Persistent buffers, device memory owned by the caller, zero-filled before the first call for a set of
+ * sequences (their sizes use the fields of `desc`; n_gqa / n_lin = number of GQA / GDN+KDA layers):
+ *   kcache, vcache  bf16 [n_gqa][max_batch][n_kv_heads][max_ctx][head_dim]      (NULL when n_gqa = 0)
+ *   state           fp32 [n_lin][max_batch][lin_heads][lin_dv][lin_dk]           (NULL when n_lin = 0)
+ *   pending         fp32 [n_lin][2][max_batch][max_rows][lin_heads][rec], rec = 2*lin_dk + lin_dv + 1
+ *                   rounded up to a multiple of 4                                (NULL when n_lin = 0)
+ *   seq             int32 [max_batch][4]
+ *   epoch           host-side call counter: 0 before the first call; each call advances it
+ * The step semantics (positions, committed and pending rows, outputs) are those of mk_decode_step.
+ *
+ * Behaviour: the first call on a device resolves the device address of the static array (with that
+ * device current), so make that first call before any stream capture begins. Every call shares the one
+ * array and it keeps the last call's contents; the call clears what must start at zero. Calls whose GPU
+ * work overlaps (two host threads, or two streams that are not ordered) race on the array and give
+ * wrong results. The call waits for `stream` and returns the device status of the step (as
+ * mk_get_status would). Errors: MK_ERR_INVALID_ARG (as mk_create / mk_decode_step, or a missing
+ * persistent buffer), MK_ERR_UNSUPPORTED when the step needs more working memory than
+ * MK_STATIC_SCRATCH_BYTES (a message on stderr gives both sizes), MK_ERR_CUDA, MK_ERR_DEVICE,
+ * MK_ERR_TIMEOUT. No MoE or MLA model is accepted (as mk_create). */
+#define MK_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+typedef struct mk_state_buffers {
+  void* kcache;
+  void* vcache;
+  float* state;
+  float* pending;
+  int32_t* seq;
+  uint32_t epoch;
+} mk_state_buffers;
+
+mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_weights* weights, mk_state_buffers* state,
+                                const int32_t* tokens, const int32_t* positions, int batch, int rows,
+                                float* logits_out, int32_t* argmax_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

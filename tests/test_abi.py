@@ -44,9 +44,11 @@ int main(void) {
   printf("mk_layer_weights %zu\n", sizeof(mk_layer_weights));
   printf("mk_weights %zu\n", sizeof(mk_weights));
   printf("mk_info %zu\n", sizeof(mk_info));
+  printf("mk_state_buffers %zu\n", sizeof(mk_state_buffers));
   F(mk_model_desc, mixer) F(mk_model_desc, n_q_heads) F(mk_model_desc, route_scale) F(mk_model_desc, max_ctx)
   F(mk_layer_weights, w_dq) F(mk_layer_weights, w_router) F(mk_layer_weights, e_gate_scales)
   F(mk_layer_weights, s_down_gscale) F(mk_weights, layers) F(mk_info, device_bytes)
+  F(mk_state_buffers, seq) F(mk_state_buffers, epoch)
   return 0;
 }
 """
@@ -65,12 +67,14 @@ def test_struct_layout_matches_header():
     assert C.sizeof(binding.LayerWeights) == c["mk_layer_weights"]
     assert C.sizeof(binding.Weights) == c["mk_weights"]
     assert C.sizeof(binding.Info) == c["mk_info"]
+    assert C.sizeof(binding.StateBuffers) == c["mk_state_buffers"]
     for key, off in c.items():
         if "." not in key:
             continue
         struct, field = key.split(".")
         cls = {"mk_model_desc": binding.ModelDesc, "mk_layer_weights": binding.LayerWeights,
-               "mk_weights": binding.Weights, "mk_info": binding.Info}[struct]
+               "mk_weights": binding.Weights, "mk_info": binding.Info,
+               "mk_state_buffers": binding.StateBuffers}[struct]
         assert getattr(cls, field).offset == off, key
 
 
