@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -84,6 +85,11 @@ struct mk_handle {
   int max_ops = 0;
   int n_ops_last = 0;
   std::vector<Program> programs;
+  // optional per-instruction timestamp trace of the last step (env MK_TRACE=<file>), written at destroy
+  std::string trace_path;
+  unsigned long long* trace = nullptr;
+  size_t trace_cap = 0;  // instructions
+  const Program* last_prog = nullptr;
 };
 
 namespace {
@@ -248,16 +254,36 @@ OpDesc blank(int type) {
   return d;
 }
 
-// one instruction per SM over a balanced range of output rows
+// One instruction per SM over a balanced range of output rows. With at most 2 activation rows the input
+// rows are staged in shared memory (fp32) for the whole instruction; a residual-add GEMV whose input does
+// not fit the staging area is split along K into sequential ops that each add their part to x (the last
+// one also writes the RMS partials of the new x).
 void gemv_op(Builder& bld, OpDesc d, int N) {
   d.type = OP_GEMV;
   d.rg = (N <= 4) ? 16 : 8;
   d.passes = (N <= 8) ? 1 : (N + 7) / 8;
-  const int op = bld.add(d);
-  for (int s = 0; s < bld.n_sm; ++s) {
-    const int r0 = (int)((int64_t)d.rows * s / bld.n_sm);
-    const int r1 = (int)((int64_t)d.rows * (s + 1) / bld.n_sm);
-    bld.place(op, s, r0, r1, 0);
+  d.ldw = d.K;
+  d.k_begin = 0;
+  // a residual-add instruction also keeps its slice of x (N x its rows) in the staging area
+  const int64_t xrows = d.out_kind == OUT_RESID ? (d.rows + bld.n_sm - 1) / bld.n_sm : 0;
+  int parts = 1;
+  if (N <= 2 && d.out_kind == OUT_RESID) {
+    while ((int64_t)N * (round_up((d.K + parts - 1) / parts, 8) + xrows) * 4 > kActBytes) ++parts;
+  }
+  const int kpart = round_up((d.K + parts - 1) / parts, 8);
+  const int ssq_out = d.ssq_out;
+  for (int part = 0; part < parts; ++part) {
+    OpDesc q = d;
+    q.k_begin = part * kpart;
+    q.K = std::min(kpart, d.ldw - q.k_begin);
+    q.ssq_out = (part == parts - 1) ? ssq_out : -1;
+    q.staged = (N <= 2 && (int64_t)N * (q.K + xrows) * 4 <= kActBytes) ? 1 : 0;
+    const int op = bld.add(q);
+    for (int s = 0; s < bld.n_sm; ++s) {
+      const int r0 = (int)((int64_t)q.rows * s / bld.n_sm);
+      const int r1 = (int)((int64_t)q.rows * (s + 1) / bld.n_sm);
+      bld.place(op, s, r0, r1, 0);
+    }
   }
 }
 
@@ -345,6 +371,16 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
               bld.place(op_at, k % h->n_sm, b * hkv + g, c, rlo | (rhi << 8));
             }
 
+      OpDesc cb = at;
+      cb.type = OP_ATTN_COMBINE;
+      cb.n_instr = 0;
+      cb.n_deps = 0;
+      const int op_cb = bld.add(cb);
+      k = 0;
+      for (int b = 0; b < B; ++b)
+        for (int r = 0; r < R; ++r)
+          for (int hh = 0; hh < hq; ++hh, ++k) bld.place(op_cb, k % h->n_sm, b, r, hh);
+
       OpDesc o = gemv_desc(hq * hd, {{L.wo, d}});
       o.layer = i;
       o.in_kind = IN_BUF;
@@ -373,13 +409,17 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
       dl.dk = dk;
       dl.dv = dv;
       dl.per_channel_decay = kda ? 1 : 0;
-      dl.col_group = kConsumerWarps;
+      // value columns per instruction: 8, 16 or 32 (1, 2 or 4 per warp), the fewest that keep the
+      // instruction count within one per SM
+      int cw = 1;
+      while (cw < 4 && (int64_t)B * H * ((dv + kConsumerWarps * cw - 1) / (kConsumerWarps * cw)) > h->n_sm) cw *= 2;
+      dl.col_group = kConsumerWarps * cw;
       dl.in = h->proj;
       dl.in_stride = h->proj_stride;
       dl.out = h->attn_out;
       dl.out_stride = h->attn_stride;
       const int op_dl = bld.add(dl);
-      const int ngrp = (dv + kConsumerWarps - 1) / kConsumerWarps;
+      const int ngrp = (dv + dl.col_group - 1) / dl.col_group;
       int k = 0;
       for (int b = 0; b < B; ++b)
         for (int hh = 0; hh < H; ++hh)
@@ -429,6 +469,13 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
     bld.place(op, 0, 0, 0, 0);
   }
 
+  for (const OpDesc& o : bld.ops) {
+    if (o.type != OP_GEMV || o.out_kind != OUT_RESID) continue;
+    const int64_t xrows = (o.rows + h->n_sm - 1) / h->n_sm;
+    if ((int64_t)N * ((o.staged ? o.K : 0) + xrows) * 4 > kActBytes)
+      return fail(h, MK_ERR_UNSUPPORTED, "residual slice of %d rows x %lld outputs exceeds the staging area", N,
+                  (long long)xrows);
+  }
   if ((int)bld.ops.size() > h->max_ops)
     return fail(h, MK_ERR_UNSUPPORTED, "program has %d ops, more than the %d counters allocated",
                 (int)bld.ops.size(), h->max_ops);
@@ -538,6 +585,10 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.lin_heads = D.lin_heads;
   p.lin_dk = D.lin_dk;
   p.lin_dv = D.lin_dv;
+  if (h->trace && (size_t)prog->n_instr <= h->trace_cap) {
+    p.trace = h->trace;
+    h->last_prog = prog;
+  }
   h->n_ops_last = prog->n_ops;
   cudaError_t e = kernel_launch(p, h->n_sm, stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
@@ -636,6 +687,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
       st = cuda_fail(h, e, "rope table");
       goto fail_out;
     }
+  }
+  if (const char* tp = getenv("MK_TRACE")) {
+    h->trace_path = tp;
+    h->trace_cap = (size_t)h->n_sm * 64 * D.n_layers + 4096;
+    ALLOC(trace, h->trace_cap * kTraceWords);
   }
 #undef ALLOC
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
@@ -754,6 +810,28 @@ void mk_destroy(mk_handle* h) {
   if (!h) return;
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
+  if (h->trace && h->last_prog && !h->trace_path.empty()) {
+    // layout: int32 n_sm, n_ops, n_instr; int32 op type [n_ops]; int32 qoff [n_sm+1]; Instr [n_instr];
+    // uint64 trace [n_instr][kTraceWords]
+    const Program& pr = *h->last_prog;
+    std::vector<OpDesc> ops(pr.n_ops);
+    std::vector<Instr> ins(pr.n_instr);
+    std::vector<int32_t> qoff(h->n_sm + 1);
+    std::vector<unsigned long long> tr((size_t)pr.n_instr * kTraceWords);
+    cudaMemcpy(ops.data(), pr.d_ops, sizeof(OpDesc) * pr.n_ops, cudaMemcpyDeviceToHost);
+    cudaMemcpy(ins.data(), pr.d_instr, sizeof(Instr) * pr.n_instr, cudaMemcpyDeviceToHost);
+    cudaMemcpy(qoff.data(), pr.d_qoff, sizeof(int32_t) * (h->n_sm + 1), cudaMemcpyDeviceToHost);
+    cudaMemcpy(tr.data(), h->trace, sizeof(unsigned long long) * tr.size(), cudaMemcpyDeviceToHost);
+    if (FILE* f = fopen(h->trace_path.c_str(), "wb")) {
+      const int32_t hdr[3] = {h->n_sm, pr.n_ops, pr.n_instr};
+      fwrite(hdr, sizeof(hdr), 1, f);
+      for (const OpDesc& o : ops) fwrite(&o.type, sizeof(int32_t), 1, f);
+      fwrite(qoff.data(), sizeof(int32_t), qoff.size(), f);
+      fwrite(ins.data(), sizeof(Instr), ins.size(), f);
+      fwrite(tr.data(), sizeof(unsigned long long), tr.size(), f);
+      fclose(f);
+    }
+  }
   for (auto& p : h->programs) {
     cudaFree(p.d_ops);
     cudaFree(p.d_instr);

@@ -16,7 +16,14 @@ namespace mk {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kSlots = 6;
+#ifndef MK_RING_SLOTS
+#define MK_RING_SLOTS 4
+#endif
+#ifndef MK_ACT_KB
+#define MK_ACT_KB 72
+#endif
+constexpr int kSlots = MK_RING_SLOTS;
+constexpr int kActBytes = MK_ACT_KB * 1024;  // shared-memory activation / staging area
 constexpr int kSlotBytes = 32768;
 constexpr int kMaxN = 64;        // rows per step (batch * rows)
 constexpr int kMaxRows = 8;      // query rows per sequence
@@ -37,6 +44,7 @@ enum OpType : int32_t {
   OP_MOE_UP = 8,      // MoE: gate/up GEMV of shared + routed experts, SwiGLU
   OP_MOE_DOWN = 9,    // MoE: down GEMV of shared + routed experts, weighted sum, residual add
   OP_FINAL = 10,      // greedy argmax, sequence bookkeeping, counter reset
+  OP_ATTN_COMBINE = 11,  // GQA: merge the context-chunk partials of one (sequence, row, q head)
 };
 
 enum InKind : int32_t { IN_NORM = 0, IN_BUF = 1 };
@@ -53,6 +61,9 @@ struct OpDesc {
   int32_t K;                // input features
   int32_t rows;             // output rows (logical rows for SwiGLU)
   int32_t rg;               // physical weight rows per row group (16 or 8)
+  int32_t ldw;              // elements between weight rows (the full input width)
+  int32_t k_begin;          // first input column of this op (an op may cover a K range of the matrix)
+  int32_t staged;           // 1: input rows staged in shared memory as bf16 for the whole instruction
   int32_t passes;           // ceil(N / 8) when 8 activation rows are processed per pass, else 1
   int32_t n_mat;
   int32_t mat_rows[kMaxOpMats];
@@ -65,7 +76,7 @@ struct OpDesc {
   int32_t out_kind;
   int32_t out_stride;       // floats between output rows
   float* out;
-  int32_t ssq_out;          // RMS-partial slot written (OUT_RESID, EMBED)
+  int32_t ssq_out;          // RMS-partial slot written (OUT_RESID, EMBED); -1 = none
   // ---- attention ----
   int32_t nchunk;           // context chunks per (sequence, kv head)
   int32_t groups;           // q heads per kv head (GQA) or heads per item (MLA)
@@ -76,7 +87,6 @@ struct OpDesc {
   int32_t dk, dv;
   int32_t per_channel_decay; // KDA
   int32_t col_group;         // value columns per instruction
-  int32_t pad_[3];
 };
 
 struct Instr {
@@ -141,6 +151,11 @@ struct KParams {
   // model dims needed by several ops
   int32_t n_q_heads, n_kv_heads, head_dim;
   int32_t lin_heads, lin_dk, lin_dv;
+  // optional %globaltimer trace, kTraceWords per instruction (NULL = off)
+  unsigned long long* trace;
 };
+
+// trace words per instruction: consumer begin, dependencies met, done; producer first / last issue
+constexpr int kTraceWords = 5;
 
 }  // namespace mk

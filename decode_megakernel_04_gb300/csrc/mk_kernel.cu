@@ -148,8 +148,6 @@ struct CSmem {
   int32_t flag;
   int32_t last;
   int32_t pad[2];
-  uint16_t knew[kMaxRows * 256];
-  uint16_t vnew[kMaxRows * 256];
 };
 
 struct Ring {
@@ -161,7 +159,11 @@ struct Ring {
   }
 };
 
-constexpr size_t kSmemBytes = (size_t)kSlots * kSlotBytes + 2 * kSlots * sizeof(uint64_t) + sizeof(CSmem);
+constexpr size_t kCSmemOff = (size_t)kSlots * kSlotBytes + 2 * kSlots * sizeof(uint64_t);
+constexpr size_t kActOff = (kCSmemOff + sizeof(CSmem) + 127) / 128 * 128;
+// ring | barriers | consumer scratch | activation / staging area (GEMV input rows as bf16; the attention
+// block's own K/V rows; the delta rule's row inputs)
+constexpr size_t kSmemBytes = kActOff + kActBytes;
 
 // consumer side of one ring chunk
 __device__ __forceinline__ bool ring_wait_full(const Ring& rg, uint32_t chunk, const KParams& p) {
@@ -238,33 +240,43 @@ __device__ __forceinline__ void block_reduce(float* v, CSmem& cs, int warp, int 
 // RG rows x KC inputs (32 KB of bf16). Thread t owns inputs [t*CPL, t*CPL + CPL) of each chunk and keeps
 // RG x NR partial sums in registers across the K slices of a row group; one block reduction per group.
 // ------------------------------------------------------------------------------------------------
+// first weight of physical row i of a row group, at the op's first input column
 __device__ __forceinline__ const uint16_t* gemv_row_src(const OpDesc& op, int g0, int i, int nl, bool swiglu) {
   if (swiglu) {
-    return (i < nl) ? op.w[0] + (size_t)(g0 + i) * op.K : op.w[1] + (size_t)(g0 + i - nl) * op.K;
+    return ((i < nl) ? op.w[0] + (size_t)(g0 + i) * op.ldw : op.w[1] + (size_t)(g0 + i - nl) * op.ldw) + op.k_begin;
   }
   int row = g0 + i;
 #pragma unroll 1
   for (int m = 0; m < op.n_mat; ++m) {
-    if (row < op.mat_rows[m]) return op.w[m] + (size_t)row * op.K;
+    if (row < op.mat_rows[m]) return op.w[m] + (size_t)row * op.ldw + op.k_begin;
     row -= op.mat_rows[m];
   }
   return op.w[0];
 }
 
+// Row groups of a GEMV instruction: its rows are split into ceil(n / glog) groups of near-equal size (so no
+// group is left with a few rows and tiny chunks), and each group's K range into slices of KC inputs.
+__device__ __forceinline__ int gemv_ngroups(int n, int glog) { return (n + glog - 1) / glog; }
+__device__ __forceinline__ int gemv_group_row(int r0, int n, int ng, int g) {
+  return r0 + (int)((long long)g * n / ng);
+}
+
+
 __device__ bool gemv_produce(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
                              uint32_t& chunk, int lane) {
-  const int KC = kSlotBytes / 2 / op.rg;
   const bool swiglu = op.out_kind == OUT_SWIGLU;
   const int glog = swiglu ? op.rg / 2 : op.rg;
-  const int nks = (op.K + KC - 1) / KC;
+  const int n = in.b - in.a;
+  const int ng = gemv_ngroups(n, glog);
   const uint32_t ring_base = smem_u32(rg.base);
   for (int pass = 0; pass < op.passes; ++pass) {
-    for (int g0 = in.a; g0 < in.b; g0 += glog) {
-      const int nl = min(glog, in.b - g0);
+    for (int g = 0; g < ng; ++g) {
+      const int g0 = gemv_group_row(in.a, n, ng, g);
+      const int nl = gemv_group_row(in.a, n, ng, g + 1) - g0;
       const int nphys = swiglu ? 2 * nl : nl;
-      for (int ks = 0; ks < nks; ++ks) {
-        const int k0 = ks * KC;
-        const int kw = min(KC, op.K - k0);
+      const int kc = kSlotBytes / 2 / op.rg;
+      for (int k0 = 0; k0 < op.K; k0 += kc) {
+        const int kw = min(kc, op.K - k0);
         if (!ring_acquire(rg, chunk, (uint32_t)(nphys * kw * 2), p, lane)) return false;
         if (lane < nphys) {
           const uint16_t* src = gemv_row_src(op, g0, lane, nl, swiglu) + k0;
@@ -314,24 +326,67 @@ __device__ __forceinline__ void load_bf16_global(const uint16_t* src, float (&ds
   }
 }
 
-template <int RG, int NR>
+// The activation rows of a staged GEMV instruction: RMSNorm (when the op normalises its input) applied
+// once and kept in shared memory as fp32 for the whole instruction, so the inner loop reads only shared
+// memory. (Rounding them to bf16 instead costs up to ~5e-2 in the logits at full model width.)
+__device__ __forceinline__ void stage_activations(const KParams& p, const OpDesc& op, CSmem& cs, float* act,
+                                                  int ctid) {
+  const bool norm = op.in_kind == IN_NORM;
+  const int K = op.K, N = p.N;
+  const int total4 = N * K / 4;
+  for (int i = ctid; i < total4; i += kConsumerThreads) {
+    const int e = i * 4;
+    const int n = e / K, k = e % K;
+    const float* src = norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
+    float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+    if (norm) {
+      const uint2 g = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+      const float s = cs.inv_rms[n];
+      v.x *= s * bf_lo(g.x);
+      v.y *= s * bf_hi(g.x);
+      v.z *= s * bf_lo(g.y);
+      v.w *= s * bf_hi(g.y);
+    }
+    *reinterpret_cast<float4*>(act + (size_t)n * K + k) = v;
+  }
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_f32_smem(const float* src, float (&dst)[CPL]) {
+#pragma unroll
+  for (int c = 0; c < CPL; c += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + c);
+    dst[c] = v.x;
+    dst[c + 1] = v.y;
+    dst[c + 2] = v.z;
+    dst[c + 3] = v.w;
+  }
+}
+
+// STAGED: activations from shared memory (fp32, N*K*4 <= kActBytes); otherwise each chunk loads
+// its activation slice from global memory (L2).
+template <int RG, int NR, bool STAGED>
 __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                             uint32_t& chunk, CSmem& cs, int ctid) {
+                             uint32_t& chunk, CSmem& cs, float* act, int ctid) {
   constexpr int CPL = kSlotBytes / 2 / RG / kConsumerThreads;  // 4 or 8 inputs per thread
   constexpr int KC = CPL * kConsumerThreads;
   constexpr int V = RG * NR;
   const int warp = ctid >> 5, lane = ctid & 31;
   const int sm = blockIdx.x;
   const bool swiglu = op.out_kind == OUT_SWIGLU;
+  const bool norm = op.in_kind == IN_NORM;
   const int glog = swiglu ? RG / 2 : RG;
   const int K = op.K;
-  const int nks = (K + KC - 1) / KC;
   const int N = p.N;
 
-  if (op.in_kind == IN_NORM && ctid < N) {
-    float s = 0.f;
-    for (int q = 0; q < p.n_sm; ++q) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + ctid]);
-    cs.inv_rms[ctid] = rsqrtf(s / (float)K + p.eps);
+  if (norm) {
+    // 1/rms of each input row from the per-SM partial sums of squares: warp per row, lanes over SMs
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      float s = 0.f;
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      s = warp_sum(s);
+      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
+    }
   }
   if (ctid < kMaxN) {
     cs.ssq_acc[ctid] = 0.f;
@@ -339,11 +394,23 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
     cs.best_idx[ctid] = 0;
   }
   consumer_sync();
+  // residual-add ops read the x slice they update once, with the staging (this SM owns x[:, a:b))
+  float* xres = act + (STAGED ? N * K : 0);
+  if (STAGED && in.b > in.a) stage_activations(p, op, cs, act, ctid);
+  if (op.out_kind == OUT_RESID) {
+    const int nr_ = in.b - in.a;
+    for (int i = ctid; i < N * nr_; i += kConsumerThreads)
+      xres[i] = __ldcg(p.x + (size_t)(i / nr_) * p.d + in.a + i % nr_);
+  }
+  if ((STAGED && in.b > in.a) || op.out_kind == OUT_RESID) consumer_sync();
 
+  const int nrows = in.b - in.a;
+  const int ng = gemv_ngroups(nrows, glog);
   for (int pass = 0; pass < op.passes; ++pass) {
     const int nbase = pass * NR;
-    for (int g0 = in.a; g0 < in.b; g0 += glog) {
-      const int nl = min(glog, in.b - g0);
+    for (int grp = 0; grp < ng; ++grp) {
+      const int g0 = gemv_group_row(in.a, nrows, ng, grp);
+      const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
       const int nphys = swiglu ? 2 * nl : nl;
       float acc[RG][NR];
 #pragma unroll
@@ -351,44 +418,55 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
 #pragma unroll
         for (int n = 0; n < NR; ++n) acc[i][n] = 0.f;
 
-      for (int ks = 0; ks < nks; ++ks) {
-        const int k0 = ks * KC;
+      for (int k0 = 0; k0 < K; k0 += KC) {
         const int kw = min(KC, K - k0);
-        ring_wait_full(rg, chunk, p);
         const int col = ctid * CPL;
+        float a[NR][CPL];
         if (col < kw) {
-          float a[NR][CPL];
-          float gsc[CPL];
-          if (op.in_kind == IN_NORM) load_bf16_global<CPL>(op.gain + k0 + col, gsc);
+          if (STAGED) {
 #pragma unroll
-          for (int n = 0; n < NR; ++n) {
-            const int row = nbase + n;
-            if (row < N) {
-              if (op.in_kind == IN_NORM) {
-                load_f32<CPL>(p.x + (size_t)row * p.d + k0 + col, a[n]);
-                const float s = cs.inv_rms[row];
+            for (int n = 0; n < NR; ++n) {
+              if (n < N) load_f32_smem<CPL>(act + (size_t)n * K + k0 + col, a[n]);
+              else
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) a[n][c] *= s * gsc[c];
+                for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
+            }
+          } else {
+            float gsc[CPL];
+            if (norm) load_bf16_global<CPL>(op.gain + op.k_begin + k0 + col, gsc);
+#pragma unroll
+            for (int n = 0; n < NR; ++n) {
+              const int row = nbase + n;
+              if (row < N) {
+                if (norm) {
+                  load_f32<CPL>(p.x + (size_t)row * p.d + op.k_begin + k0 + col, a[n]);
+                  const float s = cs.inv_rms[row];
+#pragma unroll
+                  for (int c = 0; c < CPL; ++c) a[n][c] *= s * gsc[c];
+                } else {
+                  load_f32<CPL>(op.in + (size_t)row * op.in_stride + op.k_begin + k0 + col, a[n]);
+                }
               } else {
-                load_f32<CPL>(op.in + (size_t)row * op.in_stride + k0 + col, a[n]);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
               }
-            } else {
-#pragma unroll
-              for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
             }
           }
+        }
+        ring_wait_full(rg, chunk, p);
+        if (col < kw) {
+          // all RG rows, branch-free, so the shared-memory loads of every row issue back to back; rows past
+          // nphys read stale bytes that still lie inside this slot and their sums are discarded below
           const uint8_t* wbase = rg.slot_ptr(chunk) + col * 2;
+          float wf[RG][CPL];
 #pragma unroll
-          for (int i = 0; i < RG; ++i) {
-            if (i < nphys) {
-              float wf[CPL];
-              load_bf16_row<CPL>(wbase + (size_t)i * kw * 2, wf);
+          for (int i = 0; i < RG; ++i) load_bf16_row<CPL>(wbase + (size_t)i * kw * 2, wf[i]);
 #pragma unroll
-              for (int c = 0; c < CPL; ++c)
+          for (int i = 0; i < RG; ++i)
 #pragma unroll
-                for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[c], a[n][c], acc[i][n]);
-            }
-          }
+            for (int c = 0; c < CPL; ++c)
+#pragma unroll
+              for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[i][c], a[n][c], acc[i][n]);
         }
         ring_release(rg, chunk, lane);
         ++chunk;
@@ -402,7 +480,7 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
       block_reduce<V>(v, cs, warp, lane, ctid);
 
       // epilogue: cs.val[i * NR + n] is the dot product of physical row i with activation row nbase + n
-      if (op.out_kind == OUT_SWIGLU) {
+      if (swiglu) {
         if (ctid < nl * NR) {
           const int j = ctid / NR, n = ctid % NR, row = nbase + n;
           if (row < N) {
@@ -420,9 +498,8 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
         } else if (op.out_kind == OUT_RESID) {
           float xn = 0.f;
           if (ok) {
-            float* xp = p.x + (size_t)row * p.d + g0 + i;
-            xn = __ldcg(xp) + val;
-            __stcg(xp, xn);
+            xn = xres[row * (in.b - in.a) + (g0 - in.a) + i] + val;
+            __stcg(p.x + (size_t)row * p.d + g0 + i, xn);
           }
           cs.sq[ctid] = xn * xn;
         } else {  // OUT_LOGITS
@@ -452,7 +529,7 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
       consumer_sync();
     }
   }
-  if (op.out_kind == OUT_RESID && ctid < N)
+  if (op.out_kind == OUT_RESID && op.ssq_out >= 0 && ctid < N)
     __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], cs.ssq_acc[ctid]);
   if (op.out_kind == OUT_LOGITS && ctid < N)
     p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(cs.best_val[ctid], __int_as_float(cs.best_idx[ctid]));
@@ -616,7 +693,7 @@ __device__ __forceinline__ void attn_block(const uint16_t* Ks, const uint16_t* V
 
 template <int E, int J>
 __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
-                             CSmem& cs, int ctid) {
+                             CSmem& cs, uint16_t* stage_u16, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hd = E * 32;
   const int hkv = op.n_kv_heads, G = op.groups;
@@ -664,13 +741,15 @@ __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in
   }
   if (c == op.nchunk - 1) {
     // the block's own rows, written by the RoPE/append op of this step
+    uint16_t* knew = stage_u16;
+    uint16_t* vnew = knew + kMaxRows * 256;
     for (int i = ctid; i < R * hd; i += kConsumerThreads) {
       const int r = i / hd, e = i % hd;
-      cs.knew[i] = __ldcg(p.kcache + kv_index(p, op, b, g, pos0 + r) + e);
-      cs.vnew[i] = __ldcg(p.vcache + kv_index(p, op, b, g, pos0 + r) + e);
+      knew[i] = __ldcg(p.kcache + kv_index(p, op, b, g, pos0 + r) + e);
+      vnew[i] = __ldcg(p.vcache + kv_index(p, op, b, g, pos0 + r) + e);
     }
     consumer_sync();
-    attn_block<E, J>(cs.knew, cs.vnew, R, hd, lane, npair_w, prow, 0, q, m, l, o);
+    attn_block<E, J>(knew, vnew, R, hd, lane, npair_w, prow, 0, q, m, l, o);
     consumer_sync();
   }
 
@@ -691,64 +770,101 @@ __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in
       }
     }
   }
-  consumer_sync();
-  const int n_split = (R + (rhi - rlo) - 1) / (rhi - rlo);
-  if (ctid == 0) {
-    __threadfence();
-    uint32_t* ctr = p.arrive + ((size_t)op.slot * p.max_batch + b) * hkv + g;
-    const uint32_t old = atomicAdd(ctr, 1u);
-    const int last = (old == (uint32_t)(op.nchunk * n_split - 1)) ? 1 : 0;
-    if (last) {
-      *ctr = 0u;
-      __threadfence();
+}
+
+// ------------------------------------------------------------------------------------------------
+// GQA attention, combine: instruction (a = b, b = r, c = q head) merges the context-chunk partials
+// (m, l, o) of that row and head. Warp w folds chunks w, w+8, ... with the online-softmax rule (one batch
+// of independent loads per 4 chunks); the 8 warp results are merged through shared memory.
+// ------------------------------------------------------------------------------------------------
+template <int E>
+__device__ void attn_combine_consume(const KParams& p, const OpDesc& op, const Instr& in, float* stage, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int hd = E * 32;
+  const int hkv = op.n_kv_heads, G = op.groups, NC = op.nchunk;
+  const int b = in.a, r = in.b, hq = in.c;
+  const int g = hq / G, h = hq % G;
+  const int R = p.R;
+  const int stride = p.attn_part_stride;
+  const size_t rec_bg = (size_t)(b * hkv + g) * NC;
+  float m = -CUDART_INF_F, l = 0.f, o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  for (int c0 = warp; c0 < NC; c0 += 4 * kConsumerWarps) {
+    float mc[4], lc[4], oc[4][E];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cc = c0 + u * kConsumerWarps;
+      mc[u] = -CUDART_INF_F;
+      lc[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) oc[u][e] = 0.f;
+      if (cc < NC) {
+        const float* rec = p.attn_part + (((rec_bg + cc) * R + r) * G + h) * stride;
+        mc[u] = __ldcg(rec + hd);
+        lc[u] = __ldcg(rec + hd + 1);
+#pragma unroll
+        for (int e = 0; e < E; ++e) oc[u][e] = __ldcg(rec + lane * E + e);
+      }
     }
-    cs.last = last;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (mc[u] == -CUDART_INF_F) continue;
+      const float mn = fmaxf(m, mc[u]);
+      const float sa = exp2f(m - mn), sb = exp2f(mc[u] - mn);
+      l = l * sa + lc[u] * sb;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[e] = o[e] * sa + oc[u][e] * sb;
+      m = mn;
+    }
+  }
+  // merge the warps: stage[w][0..hd) = o, stage[w][hd] = m, stage[w][hd+1] = l
+  float* mine = stage + warp * (hd + 2);
+#pragma unroll
+  for (int e = 0; e < E; ++e) mine[lane * E + e] = o[e];
+  if (lane == 0) {
+    mine[hd] = m;
+    mine[hd + 1] = l;
   }
   consumer_sync();
-  if (!cs.last) return;
-  // the last arriving chunk combines all partials of (b, g)
-  for (int pr = warp; pr < R * G; pr += kConsumerWarps) {
-    const int r = pr / G, h = pr % G;
+  if (ctid < hd) {
     float M = -CUDART_INF_F;
-    for (int cc = 0; cc < op.nchunk; ++cc) {
-      const float* rec = p.attn_part + ((((size_t)(b * hkv + g) * op.nchunk + cc) * R + r) * G + h) * stride;
-      M = fmaxf(M, __ldcg(rec + hd));
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stage[w * (hd + 2) + hd]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = stage[w * (hd + 2) + hd];
+      if (mw == -CUDART_INF_F) continue;
+      const float s = exp2f(mw - M);
+      L += s * stage[w * (hd + 2) + hd + 1];
+      acc += s * stage[w * (hd + 2) + ctid];
     }
-    float L = 0.f;
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int cc = 0; cc < op.nchunk; ++cc) {
-      const float* rec = p.attn_part + ((((size_t)(b * hkv + g) * op.nchunk + cc) * R + r) * G + h) * stride;
-      const float mc = __ldcg(rec + hd);
-      if (mc == -CUDART_INF_F) continue;
-      const float w = exp2f(mc - M);
-      L += w * __ldcg(rec + hd + 1);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, __ldcg(rec + lane * E + e), acc[e]);
-    }
-    const float inv = 1.0f / L;
-    float* dst = op.out + (size_t)(b * R + r) * op.out_stride + (size_t)(g * G + h) * hd + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) __stcg(dst + e, acc[e] * inv);
+    __stcg(op.out + (size_t)(b * R + r) * op.out_stride + (size_t)hq * hd + ctid, acc / L);
   }
 }
 
 // ------------------------------------------------------------------------------------------------
-// Gated delta rule for value columns [jg*8, jg*8+8) of head h of sequence b (warp w owns column
-// jg*8 + w; lane L owns key rows [L*E, L*E+E) of that column). First the rows the caller accepted from
-// the previous call are replayed into the stored state and the result is written back (the committed
-// state); then the new rows advance a register copy and produce outputs, and are stored for replay.
+// Gated delta rule for value columns [j0, j0 + 8*CW) of head h of sequence b (instruction a = b, b = h,
+// c = column group; warp w owns columns j0 + w*CW .. + CW; lane L owns key rows [L*E, L*E+E)).
+// First the rows the caller accepted from the previous call are replayed into the stored state and the
+// result is written back (the committed state); then the new rows advance a register copy, produce the
+// outputs, and are stored for replay by the next call.
 //   S <- Diag(alpha) S;  u = v - S^T k_hat;  S <- S + beta k_hat u^T;  o = S^T q_hat
+// Every input of the instruction (new rows from the projection, accepted rows from the pending store)
+// is staged in shared memory by one round of independent loads before the arithmetic starts.
 // ------------------------------------------------------------------------------------------------
-__device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+template <int CW>
+__device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, CSmem& cs,
+                                          float* stage, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int b = in.a, h = in.b, jg = in.c;
   const int H = op.n_heads, dk = op.dk, dv = op.dv;
   const int E = dk / 32;  // 1, 2 or 4
-  const int j = jg * op.col_group + warp;
-  if (warp >= op.col_group || j >= dv) return;
+  const int C = kConsumerWarps * CW;
+  const int j0 = jg * C;
   const bool kda = op.per_channel_decay != 0;
+  const int na = kda ? dk : 1;
   const int R = p.R;
   const int pos0 = p.positions[b];
   const int a = pos0 - p.seq[b].c_int;
@@ -757,76 +873,145 @@ __device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& i
   auto pend_at = [&](uint32_t par, int r) -> float* {
     return p.pend + (((((size_t)op.slot * 2 + par) * p.max_batch + b) * p.max_rows + r) * H + h) * rec;
   };
-  float* Sp = p.state + ((((size_t)op.slot * p.max_batch + b) * H + h) * dv + j) * dk + lane * E;
-  float S[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int e = 0; e < E; ++e) S[e] = __ldcg(Sp + e);
-
-  // replay accepted rows of the previous call
-  for (int r = 0; r < a; ++r) {
-    const float* pr = pend_at(prev, r);
-    const float vj = __ldcg(pr + dk + j);
-    const float beta = __ldcg(pr + 2 * dk + dv);
-    float kh[4], al[4];
-    for (int e = 0; e < E; ++e) {
-      kh[e] = __ldcg(pr + lane * E + e);
-      al[e] = kda ? __ldcg(pr + dk + dv + lane * E + e) : __ldcg(pr + dk + dv);
-    }
-    float dot = 0.f;
-    for (int e = 0; e < E; ++e) {
-      S[e] *= al[e];
-      dot = fmaf(S[e], kh[e], dot);
-    }
-    const float u = vj - warp_sum(dot);
-    for (int e = 0; e < E; ++e) S[e] = fmaf(beta * kh[e], u, S[e]);
-  }
-  if (a > 0)
-    for (int e = 0; e < E; ++e) __stcg(Sp + e, S[e]);
-
   const int offk = H * dk, offv = 2 * H * dk, offa = 2 * H * dk + H * dv;
   const int offb = offa + (kda ? H * dk : H);
+
+  // staging layout (floats)
+  float* sq_ = stage;                 // [R][dk] raw q
+  float* sk_ = sq_ + R * dk;          // [R][dk] raw k
+  float* sa_ = sk_ + R * dk;          // [R][na] alpha (sigmoid applied)
+  float* sb_ = sa_ + R * na;          // [R]     beta (sigmoid applied)
+  float* sv_ = sb_ + R;               // [R][C]  v of this instruction's columns
+  float* pk_ = sv_ + R * C;           // [a][dk] accepted k_hat
+  float* pa_ = pk_ + a * dk;          // [a][na] accepted alpha
+  float* pb_ = pa_ + a * na;          // [a]     accepted beta
+  float* pv_ = pb_ + a;               // [a][C]  accepted v
+
+  // the state columns this warp owns (independent of the staging)
+  float S[CW][4];
+  float* Sp[CW];
+#pragma unroll
+  for (int c = 0; c < CW; ++c) {
+    const int j = j0 + warp * CW + c;
+    Sp[c] = p.state + ((((size_t)op.slot * p.max_batch + b) * H + h) * dv + j) * dk + lane * E;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp[c] + e) : 0.f;
+  }
+  for (int i = ctid; i < R * dk; i += kConsumerThreads) {
+    const int r = i / dk, e = i % dk;
+    const float* row = op.in + (size_t)(b * R + r) * op.in_stride;
+    sq_[i] = __ldcg(row + h * dk + e);
+    sk_[i] = __ldcg(row + offk + h * dk + e);
+    if (kda) sa_[i] = sigmoidf_(__ldcg(row + offa + h * dk + e));
+  }
+  for (int i = ctid; i < R * C; i += kConsumerThreads) {
+    const int r = i / C, c = i % C;
+    const float* row = op.in + (size_t)(b * R + r) * op.in_stride;
+    sv_[i] = (j0 + c < dv) ? __ldcg(row + offv + h * dv + j0 + c) : 0.f;
+  }
+  if (ctid < R) {
+    const float* row = op.in + (size_t)(b * R + ctid) * op.in_stride;
+    if (!kda) sa_[ctid] = sigmoidf_(__ldcg(row + offa + h));
+    sb_[ctid] = sigmoidf_(__ldcg(row + offb + h));
+  }
+  for (int i = ctid; i < a * dk; i += kConsumerThreads) {
+    const int r = i / dk, e = i % dk;
+    const float* pr = pend_at(prev, r);
+    pk_[i] = __ldcg(pr + e);
+    if (kda) pa_[i] = __ldcg(pr + dk + dv + e);
+  }
+  for (int i = ctid; i < a * C; i += kConsumerThreads) {
+    const int r = i / C, c = i % C;
+    pv_[i] = (j0 + c < dv) ? __ldcg(pend_at(prev, r) + dk + j0 + c) : 0.f;
+  }
+  if (ctid < a) {
+    const float* pr = pend_at(prev, ctid);
+    if (!kda) pa_[ctid] = __ldcg(pr + dk + dv);
+    pb_[ctid] = __ldcg(pr + 2 * dk + dv);
+  }
+  consumer_sync();
+
+  const int jw = j0 + warp * CW;  // first column of this warp
+  // replay accepted rows of the previous call
+  for (int r = 0; r < a; ++r) {
+    float kh[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      kh[e] = e < E ? pk_[r * dk + lane * E + e] : 0.f;
+      al[e] = e < E ? (kda ? pa_[r * dk + lane * E + e] : pa_[r]) : 1.f;
+    }
+    const float beta = pb_[r];
+#pragma unroll
+    for (int c = 0; c < CW; ++c) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        S[c][e] *= al[e];
+        dot = fmaf(S[c][e], kh[e], dot);
+      }
+      const float u = pv_[r * C + warp * CW + c] - warp_sum(dot);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S[c][e] = fmaf(beta * kh[e], u, S[c][e]);
+    }
+  }
+  if (a > 0) {
+#pragma unroll
+    for (int c = 0; c < CW; ++c)
+      if (jw + c < dv)
+        for (int e = 0; e < E; ++e) __stcg(Sp[c] + e, S[c][e]);
+  }
+
   const float qs = rsqrtf((float)dk);
   for (int r = 0; r < R; ++r) {
     const int n = b * R + r;
-    const float* row = op.in + (size_t)n * op.in_stride;
     float qv[4], kv[4], al[4];
-    float sq = 0.f, sk = 0.f;
-    for (int e = 0; e < E; ++e) {
-      qv[e] = __ldcg(row + h * dk + lane * E + e);
-      kv[e] = __ldcg(row + offk + h * dk + lane * E + e);
-      sq = fmaf(qv[e], qv[e], sq);
-      sk = fmaf(kv[e], kv[e], sk);
+    float sqs = 0.f, sks = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qv[e] = e < E ? sq_[r * dk + lane * E + e] : 0.f;
+      kv[e] = e < E ? sk_[r * dk + lane * E + e] : 0.f;
+      al[e] = e < E ? (kda ? sa_[r * dk + lane * E + e] : sa_[r]) : 1.f;
+      sqs = fmaf(qv[e], qv[e], sqs);
+      sks = fmaf(kv[e], kv[e], sks);
     }
-    const float iq = rsqrtf(warp_sum(sq) + 1e-6f) * qs;
-    const float ik = rsqrtf(warp_sum(sk) + 1e-6f);
-    const float vj = __ldcg(row + offv + h * dv + j);
-    const float beta = sigmoidf_(__ldcg(row + offb + h));
-    const float alpha_h = kda ? 0.f : sigmoidf_(__ldcg(row + offa + h));
-    float dot = 0.f;
-    for (int e = 0; e < E; ++e) {
+    const float iq = rsqrtf(warp_sum(sqs) + 1e-6f) * qs;
+    const float ik = rsqrtf(warp_sum(sks) + 1e-6f);
+    const float beta = sb_[r];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
       qv[e] *= iq;
       kv[e] *= ik;
-      al[e] = kda ? sigmoidf_(__ldcg(row + offa + h * dk + lane * E + e)) : alpha_h;
-      S[e] *= al[e];
-      dot = fmaf(S[e], kv[e], dot);
     }
-    const float u = vj - warp_sum(dot);
-    float od = 0.f;
-    for (int e = 0; e < E; ++e) {
-      S[e] = fmaf(beta * kv[e], u, S[e]);
-      od = fmaf(S[e], qv[e], od);
-    }
-    const float o = warp_sum(od);
-    if (lane == 0) __stcg(op.out + (size_t)n * op.out_stride + h * dv + j, o);
-    // store the row for replay by the next call
     float* pw = pend_at(cur, r);
-    if (lane == 0) __stcg(pw + dk + j, vj);
+#pragma unroll
+    for (int c = 0; c < CW; ++c) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        S[c][e] *= al[e];
+        dot = fmaf(S[c][e], kv[e], dot);
+      }
+      const float vj = sv_[r * C + warp * CW + c];
+      const float u = vj - warp_sum(dot);
+      float od = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        S[c][e] = fmaf(beta * kv[e], u, S[c][e]);
+        od = fmaf(S[c][e], qv[e], od);
+      }
+      const float o = warp_sum(od);
+      if (lane == 0 && jw + c < dv) {
+        __stcg(op.out + (size_t)n * op.out_stride + h * dv + jw + c, o);
+        __stcg(pw + dk + jw + c, vj);  // stored for replay by the next call
+      }
+    }
     if (jg == 0 && warp == 0) {
       for (int e = 0; e < E; ++e) {
         __stcg(pw + lane * E + e, kv[e]);
         if (kda) __stcg(pw + dk + dv + lane * E + e, al[e]);
       }
       if (lane == 0) {
-        if (!kda) __stcg(pw + dk + dv, alpha_h);
+        if (!kda) __stcg(pw + dk + dv, al[0]);
         __stcg(pw + 2 * dk + dv, beta);
       }
     }
@@ -838,15 +1023,22 @@ __device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& i
 // ------------------------------------------------------------------------------------------------
 __device__ void final_consume(const KParams& p, int ctid) {
   if (p.argmax) {
-    for (int n = ctid; n < p.N; n += kConsumerThreads) {
+    const int warp = ctid >> 5, lane = ctid & 31;
+    for (int n = warp; n < p.N; n += kConsumerWarps) {
       float bv = -CUDART_INF_F;
       int bi = 0x7fffffff;
-      for (int q = 0; q < p.n_sm; ++q) {
+      for (int q = lane; q < p.n_sm; q += 32) {
         const float2 c = __ldcg(&p.amax_part[(size_t)q * kMaxN + n]);
         const int ci = __float_as_int(c.y);
         if (c.x > bv || (c.x == bv && ci < bi)) { bv = c.x; bi = ci; }
       }
-      p.argmax[n] = bi;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) p.argmax[n] = bi;
     }
   }
   if (ctid < p.B) {
@@ -871,8 +1063,10 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
     const Instr in = p.instrs[qi];
     const OpDesc& op = p.ops[in.op];
     bool ok = true;
+    if (p.trace && lane == 0) p.trace[(size_t)qi * kTraceWords + 3] = global_timer();
     if (op.type == OP_GEMV) ok = gemv_produce(p, op, in, rg, chunk, lane);
     else if (op.type == OP_ATTN) ok = attn_produce(p, op, in, rg, chunk, lane);
+    if (p.trace && lane == 0) p.trace[(size_t)qi * kTraceWords + 4] = global_timer();
     if (!ok) break;
   }
   // every issued copy must land before the CTA may exit
@@ -888,25 +1082,28 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
   __syncwarp();
 }
 
-template <int RG, int NR>
-__device__ __forceinline__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                                              uint32_t& chunk, CSmem& cs, int ctid) {
-  gemv_consume<RG, NR>(p, op, in, rg, chunk, cs, ctid);
+template <int RG, int NR, bool STAGED>
+__device__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                                           uint32_t& chunk, CSmem& cs, float* act, int ctid) {
+  gemv_consume<RG, NR, STAGED>(p, op, in, rg, chunk, cs, act, ctid);
 }
 
-__device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, int q0, int q1, int ctid) {
+__device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16_t* act, int q0, int q1, int ctid) {
   uint32_t chunk = 0;
+  float* actf = reinterpret_cast<float*>(act);
   const int nr = p.N <= 1 ? 1 : p.N <= 2 ? 2 : p.N <= 4 ? 4 : 8;
   for (int qi = q0; qi < q1; ++qi) {
     const Instr in = p.instrs[qi];
     const OpDesc& op = p.ops[in.op];
     if (ctid == 0) {
       int ok = 1;
+      if (p.trace) p.trace[(size_t)qi * kTraceWords + 0] = global_timer();
       for (int d = 0; d < op.n_deps && ok; ++d) {
         const int dop = op.deps[d];
         ok = wait_counter(&p.counters[dop], (uint32_t)p.ops[dop].n_instr, p) ? 1 : 0;
       }
       if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) ok = 0;
+      if (p.trace) p.trace[(size_t)qi * kTraceWords + 1] = global_timer();
       cs.flag = ok;
     }
     consumer_sync();
@@ -914,31 +1111,45 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, int q0
     switch (op.type) {
       case OP_EMBED: embed_consume(p, op, in, ctid); break;
       case OP_GEMV:
-        if (nr == 1) gemv_dispatch<16, 1>(p, op, in, rg, chunk, cs, ctid);
-        else if (nr == 2) gemv_dispatch<16, 2>(p, op, in, rg, chunk, cs, ctid);
-        else if (nr == 4) gemv_dispatch<16, 4>(p, op, in, rg, chunk, cs, ctid);
-        else gemv_dispatch<8, 8>(p, op, in, rg, chunk, cs, ctid);
+        if (op.staged) {
+          if (nr == 1) gemv_dispatch<16, 1, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else gemv_dispatch<16, 2, true>(p, op, in, rg, chunk, cs, actf, ctid);
+        } else {
+          if (nr == 1) gemv_dispatch<16, 1, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 2) gemv_dispatch<16, 2, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 4) gemv_dispatch<16, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else gemv_dispatch<8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
+        }
         break;
       case OP_ROPE_APPEND: rope_append_consume(p, op, ctid); break;
       case OP_ATTN: {
         const int pairs = ((in.c >> 8) - (in.c & 0xff)) * op.groups;
         const int J = (pairs + kConsumerWarps - 1) / kConsumerWarps;
         if (op.head_dim == 256) {
-          if (J <= 1) attn_consume<8, 1>(p, op, in, rg, chunk, cs, ctid);
-          else if (J <= 2) attn_consume<8, 2>(p, op, in, rg, chunk, cs, ctid);
-          else attn_consume<8, 4>(p, op, in, rg, chunk, cs, ctid);
+          if (J <= 1) attn_consume<8, 1>(p, op, in, rg, chunk, cs, act, ctid);
+          else if (J <= 2) attn_consume<8, 2>(p, op, in, rg, chunk, cs, act, ctid);
+          else attn_consume<8, 4>(p, op, in, rg, chunk, cs, act, ctid);
         } else if (op.head_dim == 128) {
-          if (J <= 1) attn_consume<4, 1>(p, op, in, rg, chunk, cs, ctid);
-          else if (J <= 2) attn_consume<4, 2>(p, op, in, rg, chunk, cs, ctid);
-          else attn_consume<4, 4>(p, op, in, rg, chunk, cs, ctid);
+          if (J <= 1) attn_consume<4, 1>(p, op, in, rg, chunk, cs, act, ctid);
+          else if (J <= 2) attn_consume<4, 2>(p, op, in, rg, chunk, cs, act, ctid);
+          else attn_consume<4, 4>(p, op, in, rg, chunk, cs, act, ctid);
         } else {
-          if (J <= 1) attn_consume<2, 1>(p, op, in, rg, chunk, cs, ctid);
-          else if (J <= 2) attn_consume<2, 2>(p, op, in, rg, chunk, cs, ctid);
-          else attn_consume<2, 4>(p, op, in, rg, chunk, cs, ctid);
+          if (J <= 1) attn_consume<2, 1>(p, op, in, rg, chunk, cs, act, ctid);
+          else if (J <= 2) attn_consume<2, 2>(p, op, in, rg, chunk, cs, act, ctid);
+          else attn_consume<2, 4>(p, op, in, rg, chunk, cs, act, ctid);
         }
         break;
       }
-      case OP_DELTA: delta_consume(p, op, in, ctid); break;
+      case OP_ATTN_COMBINE:
+        if (op.head_dim == 256) attn_combine_consume<8>(p, op, in, actf, ctid);
+        else if (op.head_dim == 128) attn_combine_consume<4>(p, op, in, actf, ctid);
+        else attn_combine_consume<2>(p, op, in, actf, ctid);
+        break;
+      case OP_DELTA:
+        if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
+        else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
+        else delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
+        break;
       case OP_FINAL: final_consume(p, ctid); break;
       default: break;
     }
@@ -947,6 +1158,7 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, int q0
       __threadfence();
       red_release_add(&p.counters[in.op], 1u);
     }
+    if (ctid == 0 && p.trace) p.trace[(size_t)qi * kTraceWords + 2] = global_timer();
   }
 }
 
@@ -971,7 +1183,8 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   rg.base = smem;
   rg.full = reinterpret_cast<uint64_t*>(smem + (size_t)kSlots * kSlotBytes);
   rg.empty = rg.full + kSlots;
-  CSmem& cs = *reinterpret_cast<CSmem*>(rg.empty + kSlots);
+  CSmem& cs = *reinterpret_cast<CSmem*>(smem + kCSmemOff);
+  uint16_t* act = reinterpret_cast<uint16_t*>(smem + kActOff);
   __shared__ int s_state;
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -989,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   }
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
   if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1);
-  else run_consumer(p, rg, cs, q0, q1, tid);
+  else run_consumer(p, rg, cs, act, q0, q1, tid);
 }
 
 // ------------------------------------------------------------------------------------------------
