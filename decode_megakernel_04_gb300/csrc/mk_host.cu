@@ -254,10 +254,13 @@ OpDesc blank(int type) {
   return d;
 }
 
-// One instruction per SM over a balanced range of output rows. With at most 2 activation rows the input
-// rows are staged in shared memory (fp32) for the whole instruction; a residual-add GEMV whose input does
-// not fit the staging area is split along K into sequential ops that each add their part to x (the last
-// one also writes the RMS partials of the new x).
+// One instruction per SM over a balanced range of output rows. Up to 4 activation rows take the tensor-core
+// path (inputs staged in shared memory as bf16 hi/lo pairs) when they fit the staging area; up to 2 rows
+// otherwise use the CUDA-core path with fp32 inputs staged; more rows read their inputs from L2 per chunk.
+// A residual-add GEMV whose input does not fit is split along K into sequential ops that each add their
+// part to x (the last one also writes the RMS partials of the new x).
+constexpr int kMmaSlice = 1024;  // 64 k-steps of 16; 16 rows x (1024 * 2 + 16) bytes fit one slot
+
 void gemv_op(Builder& bld, OpDesc d, int N) {
   d.type = OP_GEMV;
   d.rg = (N <= 4) ? 16 : 8;
@@ -266,18 +269,24 @@ void gemv_op(Builder& bld, OpDesc d, int N) {
   d.k_begin = 0;
   // a residual-add instruction also keeps its slice of x (N x its rows) in the staging area
   const int64_t xrows = d.out_kind == OUT_RESID ? (d.rows + bld.n_sm - 1) / bld.n_sm : 0;
+  const int64_t cap = kActBytes / 4 - 8;  // floats
+  auto fits_mma = [&](int k) { return N <= 4 && k % 16 == 0 && (int64_t)N * (k + 8 + xrows) <= cap; };
+  auto fits_staged = [&](int k) { return N <= 2 && (int64_t)N * (k + xrows) <= cap; };
   int parts = 1;
-  if (N <= 2 && d.out_kind == OUT_RESID) {
-    while ((int64_t)N * (round_up((d.K + parts - 1) / parts, 8) + xrows) * 4 > kActBytes) ++parts;
+  if (d.out_kind == OUT_RESID && N <= 4 && d.K % 16 == 0) {
+    while (!fits_mma(round_up((d.K + parts - 1) / parts, 16)) && parts < 16) ++parts;
+    if (!fits_mma(round_up((d.K + parts - 1) / parts, 16))) parts = 1;
   }
-  const int kpart = round_up((d.K + parts - 1) / parts, 8);
+  const int kpart = round_up((d.K + parts - 1) / parts, 16);
   const int ssq_out = d.ssq_out;
   for (int part = 0; part < parts; ++part) {
     OpDesc q = d;
     q.k_begin = part * kpart;
     q.K = std::min(kpart, d.ldw - q.k_begin);
     q.ssq_out = (part == parts - 1) ? ssq_out : -1;
-    q.staged = (N <= 2 && (int64_t)N * (q.K + xrows) * 4 <= kActBytes) ? 1 : 0;
+    q.mma = fits_mma(q.K) ? 1 : 0;
+    q.staged = (!q.mma && fits_staged(q.K)) ? 1 : 0;
+    q.kc = q.mma ? kMmaSlice : kChunkBytes / 2 / q.rg;
     const int op = bld.add(q);
     for (int s = 0; s < bld.n_sm; ++s) {
       const int r0 = (int)((int64_t)q.rows * s / bld.n_sm);

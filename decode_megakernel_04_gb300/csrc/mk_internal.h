@@ -24,7 +24,8 @@ constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 #endif
 constexpr int kSlots = MK_RING_SLOTS;
 constexpr int kActBytes = MK_ACT_KB * 1024;  // shared-memory activation / staging area
-constexpr int kSlotBytes = 32768;
+constexpr int kSlotBytes = 33 * 1024;   // ring slot allocation (payload <= kChunkBytes + row padding)
+constexpr int kChunkBytes = 32768;      // weight bytes per chunk
 constexpr int kMaxN = 64;        // rows per step (batch * rows)
 constexpr int kMaxRows = 8;      // query rows per sequence
 constexpr int kMaxOpMats = 6;
@@ -63,7 +64,9 @@ struct OpDesc {
   int32_t rg;               // physical weight rows per row group (16 or 8)
   int32_t ldw;              // elements between weight rows (the full input width)
   int32_t k_begin;          // first input column of this op (an op may cover a K range of the matrix)
-  int32_t staged;           // 1: input rows staged in shared memory as bf16 for the whole instruction
+  int32_t staged;           // 1: input rows staged in shared memory (fp32) for the whole instruction
+  int32_t mma;              // 1: tensor-core path (inputs staged as bf16 hi/lo pairs, padded weight rows)
+  int32_t kc;               // inputs per weight slice (chunk width)
   int32_t passes;           // ceil(N / 8) when 8 activation rows are processed per pass, else 1
   int32_t n_mat;
   int32_t mat_rows[kMaxOpMats];

@@ -148,6 +148,7 @@ struct CSmem {
   int32_t flag;
   int32_t last;
   int32_t pad[2];
+  float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
 };
 
 struct Ring {
@@ -262,33 +263,6 @@ __device__ __forceinline__ int gemv_group_row(int r0, int n, int ng, int g) {
 }
 
 
-__device__ bool gemv_produce(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                             uint32_t& chunk, int lane) {
-  const bool swiglu = op.out_kind == OUT_SWIGLU;
-  const int glog = swiglu ? op.rg / 2 : op.rg;
-  const int n = in.b - in.a;
-  const int ng = gemv_ngroups(n, glog);
-  const uint32_t ring_base = smem_u32(rg.base);
-  for (int pass = 0; pass < op.passes; ++pass) {
-    for (int g = 0; g < ng; ++g) {
-      const int g0 = gemv_group_row(in.a, n, ng, g);
-      const int nl = gemv_group_row(in.a, n, ng, g + 1) - g0;
-      const int nphys = swiglu ? 2 * nl : nl;
-      const int kc = kSlotBytes / 2 / op.rg;
-      for (int k0 = 0; k0 < op.K; k0 += kc) {
-        const int kw = min(kc, op.K - k0);
-        if (!ring_acquire(rg, chunk, (uint32_t)(nphys * kw * 2), p, lane)) return false;
-        if (lane < nphys) {
-          const uint16_t* src = gemv_row_src(op, g0, lane, nl, swiglu) + k0;
-          bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + lane * kw * 2, src, (uint32_t)(kw * 2),
-                   &rg.full[chunk % kSlots]);
-        }
-        ++chunk;
-      }
-    }
-  }
-  return true;
-}
 
 template <int CPL>
 __device__ __forceinline__ void load_f32(const float* src, float (&dst)[CPL]) {
@@ -323,6 +297,213 @@ __device__ __forceinline__ void load_bf16_global(const uint16_t* src, float (&ds
   } else {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
     dst[0] = bf_lo(w.x); dst[1] = bf_hi(w.x); dst[2] = bf_lo(w.y); dst[3] = bf_hi(w.y);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core GEMV for up to 4 activation rows (mma.sync m16n8k16, bf16 x bf16 -> fp32).
+// A = a 16-row weight group straight from the ring (ldmatrix; rows padded by 16 bytes in the slot so the
+// eight rows of an 8x8 matrix fall in distinct banks). B = the activations, staged once per instruction
+// as a bf16 "hi" and a bf16 "lo" part (hi = bf16(v), lo = bf16(v - hi)), so the pair carries ~16
+// mantissa bits and the product keeps fp32-level accuracy: columns 0..3 of the n8 tile are hi of rows
+// 0..3, columns 4..7 lo of rows 0..3. Warps split the 16-wide k steps of a chunk; one cross-warp
+// reduction (one barrier) per row group.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// hi/lo bf16 columns of the staged activations: slot n (n < N) = hi of row n, slot N + n = lo of row n,
+// each K + 8 elements long (the 8 pad elements put successive slots in different banks)
+__device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, CSmem& cs, uint16_t* cols, int ctid) {
+  const bool norm = op.in_kind == IN_NORM;
+  const int K = op.K, N = p.N, cp = op.K + 8;
+  const int total4 = N * K / 4;
+  for (int i = ctid; i < total4; i += kConsumerThreads) {
+    const int e = i * 4;
+    const int n = e / K, k = e % K;
+    const float* src = norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
+    float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+    if (norm) {
+      const uint2 g = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+      const float s = cs.inv_rms[n];
+      v.x *= s * bf_lo(g.x);
+      v.y *= s * bf_hi(g.x);
+      v.z *= s * bf_lo(g.y);
+      v.w *= s * bf_hi(g.y);
+    }
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint16_t hi[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hi[j] = f2bf(f[j]);
+      lo[j] = f2bf(f[j] - bf2f(hi[j]));
+    }
+    *reinterpret_cast<uint2*>(cols + (size_t)n * cp + k) =
+        make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+    *reinterpret_cast<uint2*>(cols + (size_t)(N + n) * cp + k) =
+        make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+  }
+}
+
+__device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+                                 CSmem& cs, float* act, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int sm = blockIdx.x;
+  const bool swiglu = op.out_kind == OUT_SWIGLU;
+  const bool norm = op.in_kind == IN_NORM;
+  const int glog = swiglu ? 8 : 16;
+  const int K = op.K, N = p.N, KC = op.kc;
+  const int cpitch = K + 8;
+  uint16_t* cols = reinterpret_cast<uint16_t*>(act);
+  // the residual slice follows the staged columns
+  float* xres = act + (2 * N * cpitch + 1) / 2 + 4;
+
+  if (norm) {
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      float s = 0.f;
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      s = warp_sum(s);
+      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
+    }
+  }
+  consumer_sync();
+  if (in.b > in.a) stage_hilo(p, op, cs, cols, ctid);
+  if (op.out_kind == OUT_RESID) {
+    const int nr_ = in.b - in.a;
+    for (int i = ctid; i < N * nr_; i += kConsumerThreads)
+      xres[i] = __ldcg(p.x + (size_t)(i / nr_) * p.d + in.a + i % nr_);
+  }
+  consumer_sync();
+
+  // this lane's B column: hi of row g, lo of row g - 4, or zero
+  const int g = lane >> 2, t = lane & 3;
+  const int bslot = (g < N) ? g : ((g >= 4 && g - 4 < N) ? N + (g - 4) : -1);
+  const uint16_t* bcol = cols + (size_t)(bslot < 0 ? 0 : bslot) * cpitch + 2 * t;
+  // ldmatrix row / k offset of this lane inside a 16x16 tile
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int lk = ((lane >> 4) & 1) * 8;
+  const uint32_t ring_s = smem_u32(rg.base);
+
+  // per-thread epilogue state: thread t < 16 * N owns (row i, activation row n), i = t / N, n = t % N
+  float best_v = -CUDART_INF_F, ssq_acc = 0.f;
+  int best_i = 0;
+  float* red = cs.mred;  // [2][8 warps][16 rows][8 cols]
+
+  const int nrows = in.b - in.a;
+  const int ng = gemv_ngroups(nrows, glog);
+  for (int grp = 0; grp < ng; ++grp) {
+    const int g0 = gemv_group_row(in.a, nrows, ng, grp);
+    const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < K; k0 += KC) {
+      const int kw = min(KC, K - k0);
+      const int pitch = kw * 2 + 16;
+      const int nsteps = kw >> 4;
+      ring_wait_full(rg, chunk, p);
+      const uint32_t abase = ring_s + (chunk % kSlots) * kSlotBytes + lrow * pitch + lk * 2;
+      int s = warp;
+      for (; s + kConsumerWarps < nsteps; s += 2 * kConsumerWarps) {
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        ldmatrix_x4(abase + s * 32, a0, a1, a2, a3);
+        ldmatrix_x4(abase + (s + kConsumerWarps) * 32, c0, c1, c2, c3);
+        uint32_t b0 = 0, b1 = 0, e0 = 0, e1 = 0;
+        if (bslot >= 0) {
+          const uint16_t* bp = bcol + k0 + s * 16;
+          b0 = *reinterpret_cast<const uint32_t*>(bp);
+          b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
+          e0 = *reinterpret_cast<const uint32_t*>(bp + kConsumerWarps * 16);
+          e1 = *reinterpret_cast<const uint32_t*>(bp + kConsumerWarps * 16 + 8);
+        }
+        mma_bf16_16816(acc0, a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(acc1, c0, c1, c2, c3, e0, e1);
+      }
+      if (s < nsteps) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(abase + s * 32, a0, a1, a2, a3);
+        uint32_t b0 = 0, b1 = 0;
+        if (bslot >= 0) {
+          const uint16_t* bp = bcol + k0 + s * 16;
+          b0 = *reinterpret_cast<const uint32_t*>(bp);
+          b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
+        }
+        mma_bf16_16816(acc0, a0, a1, a2, a3, b0, b1);
+      }
+      ring_release(rg, chunk, lane);
+      ++chunk;
+    }
+    // cross-warp reduction: red[buf][warp][row][col]; fragment c0/c1 = (row g, cols 2t, 2t+1), c2/c3 = row g+8
+    float* rb = red + (grp & 1) * (kConsumerWarps * 128) + warp * 128;
+    rb[g * 8 + 2 * t] = acc0[0] + acc1[0];
+    rb[g * 8 + 2 * t + 1] = acc0[1] + acc1[1];
+    rb[(g + 8) * 8 + 2 * t] = acc0[2] + acc1[2];
+    rb[(g + 8) * 8 + 2 * t + 1] = acc0[3] + acc1[3];
+    consumer_sync();
+    const float* rr = red + (grp & 1) * (kConsumerWarps * 128);
+    auto rowval = [&](int i, int n) -> float {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) v += rr[w * 128 + i * 8 + n] + rr[w * 128 + i * 8 + 4 + n];
+      return v;
+    };
+    if (swiglu) {
+      if (ctid < nl * N) {
+        const int j = ctid / N, n = ctid % N;
+        const float gv = rowval(j, n), uv = rowval(nl + j, n);
+        op.out[(size_t)n * op.out_stride + g0 + j] = gv / (1.0f + expf(-gv)) * uv;
+      }
+    } else if (ctid < 16 * N) {
+      const int i = ctid / N, n = ctid % N;
+      if (i < nl) {
+        const float val = rowval(i, n);
+        if (op.out_kind == OUT_STORE) {
+          op.out[(size_t)n * op.out_stride + g0 + i] = val;
+        } else if (op.out_kind == OUT_RESID) {
+          const float xn = xres[n * nrows + (g0 - in.a) + i] + val;
+          __stcg(p.x + (size_t)n * p.d + g0 + i, xn);
+          ssq_acc += xn * xn;
+        } else {
+          if (p.logits) p.logits[(size_t)n * p.V + g0 + i] = val;
+          if (val > best_v) { best_v = val; best_i = g0 + i; }
+        }
+      }
+    }
+    // the other buffer is rewritten two groups later, after the next group's barrier
+  }
+  if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
+    // reduce the per-thread (row, n) state over the 16 rows of each n
+    consumer_sync();
+    if (ctid < 16 * N) {
+      cs.sq[ctid] = (op.out_kind == OUT_RESID) ? ssq_acc : best_v;
+      cs.best_idx[ctid] = best_i;
+    }
+    consumer_sync();
+    if (ctid < N) {
+      if (op.out_kind == OUT_RESID) {
+        float s2 = 0.f;
+        for (int i = 0; i < 16; ++i) s2 += cs.sq[i * N + ctid];
+        if (op.ssq_out >= 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], s2);
+      } else {
+        float bv = -CUDART_INF_F;
+        int bi = 0x7fffffff;
+        for (int i = 0; i < 16; ++i) {
+          const float v = cs.sq[i * N + ctid];
+          const int ix = cs.best_idx[i * N + ctid];
+          if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
+        }
+        p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(bv, __int_as_float(bi));
+      }
+    }
   }
 }
 
@@ -368,7 +549,7 @@ __device__ __forceinline__ void load_f32_smem(const float* src, float (&dst)[CPL
 template <int RG, int NR, bool STAGED>
 __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
                              uint32_t& chunk, CSmem& cs, float* act, int ctid) {
-  constexpr int CPL = kSlotBytes / 2 / RG / kConsumerThreads;  // 4 or 8 inputs per thread
+  constexpr int CPL = kChunkBytes / 2 / RG / kConsumerThreads;  // 4 or 8 inputs per thread
   constexpr int KC = CPL * kConsumerThreads;
   constexpr int V = RG * NR;
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -411,7 +592,6 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
     for (int grp = 0; grp < ng; ++grp) {
       const int g0 = gemv_group_row(in.a, nrows, ng, grp);
       const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
-      const int nphys = swiglu ? 2 * nl : nl;
       float acc[RG][NR];
 #pragma unroll
       for (int i = 0; i < RG; ++i)
@@ -610,25 +790,6 @@ __device__ __forceinline__ void attn_range(const KParams& p, const OpDesc& op, i
   t1 = min(t0 + tc, pos0);
 }
 
-__device__ bool attn_produce(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
-                             int lane) {
-  const int hkv = op.n_kv_heads, hd = op.head_dim;
-  const int b = in.a / hkv, g = in.a % hkv;
-  int t0, t1;
-  attn_range(p, op, b, in.b, t0, t1);
-  const int P = kSlotBytes / (4 * hd);
-  const uint32_t ring_base = smem_u32(rg.base);
-  for (int t = t0; t < t1; t += P) {
-    const int np = min(P, t1 - t);
-    const uint32_t bytes = (uint32_t)(np * hd * 2);
-    if (!ring_acquire(rg, chunk, 2 * bytes, p, lane)) return false;
-    const uint32_t dst = ring_base + (chunk % kSlots) * kSlotBytes;
-    if (lane == 0) bulk_g2s(dst, p.kcache + kv_index(p, op, b, g, t), bytes, &rg.full[chunk % kSlots]);
-    if (lane == 1) bulk_g2s(dst + kSlotBytes / 2, p.vcache + kv_index(p, op, b, g, t), bytes, &rg.full[chunk % kSlots]);
-    ++chunk;
-  }
-  return true;
-}
 
 template <int E>
 __device__ __forceinline__ void load_head_slice(const uint16_t* row, int lane, float (&out)[E]) {
@@ -704,7 +865,7 @@ __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in
   int t0, t1;
   attn_range(p, op, b, c, t0, t1);
   const int pos0 = p.positions[b];
-  const int P = kSlotBytes / (4 * hd);
+  const int P = kChunkBytes / (4 * hd);
   const float qscale = rsqrtf((float)hd) * kLog2e;
 
   float q[J][E], o[J][E], m[J], l[J];
@@ -732,7 +893,7 @@ __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in
     const int np = min(P, t1 - t);
     ring_wait_full(rg, chunk, p);
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(rg.slot_ptr(chunk));
-    const uint16_t* Vs = Ks + kSlotBytes / 4;
+    const uint16_t* Vs = Ks + kChunkBytes / 4;
     for (int tb = 0; tb < np; tb += 32)
       attn_block<E, J>(Ks + (size_t)tb * hd, Vs + (size_t)tb * hd, min(32, np - tb), hd, lane, npair_w, prow, -1,
                        q, m, l, o);
@@ -1019,6 +1180,124 @@ __device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& i
 }
 
 // ------------------------------------------------------------------------------------------------
+// Producer: the chunks of an SM's queue, in the order its consumers read them. A cursor walks them and the
+// producer loads each chunk into the ring. Optionally (MK_PREFETCH_AHEAD > 0) a second cursor runs that
+// many chunks further and asks L2 to fetch those bytes early (cp.async.bulk.prefetch.L2); measured on the
+// hybrid stack this doubled HBM reads (prefetched lines were evicted before use), so it is off.
+// ------------------------------------------------------------------------------------------------
+#ifndef MK_PREFETCH_AHEAD
+#define MK_PREFETCH_AHEAD 0
+#endif
+constexpr int kPrefetchAhead = MK_PREFETCH_AHEAD;
+
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+struct ChunkCursor {
+  int qi, q1;
+  int kind;  // 0: load the next instruction, 1: GEMV chunks, 2: attention KV chunks
+  // the instruction's fields, cached in registers when it is loaded
+  int K, kc, pad, passes, ng, n, a, glog, swiglu;
+  const OpDesc* op;
+  // GEMV walk: pass, row group, first input of the next slice; this lane's row pointer in the group
+  int pass, grp, k0, nphys;
+  const uint16_t* row;
+  // attention walk: next position, end, positions per chunk, bytes per position, this lane's base
+  int t, t1, P, pos_bytes;
+  const uint16_t* kv;
+};
+
+__device__ __forceinline__ void cursor_group(ChunkCursor& c, int lane) {
+  const int g0 = gemv_group_row(c.a, c.n, c.ng, c.grp);
+  const int nl = gemv_group_row(c.a, c.n, c.ng, c.grp + 1) - g0;
+  c.nphys = c.swiglu ? 2 * nl : nl;
+  c.row = (lane < c.nphys) ? gemv_row_src(*c.op, g0, lane, nl, c.swiglu != 0) : nullptr;
+}
+
+// This lane's copy of the next chunk (bytes = 0: none) and the chunk's total bytes; false at the end.
+__device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, int lane, const void*& src,
+                                            uint32_t& bytes, uint32_t& dst, uint32_t& total) {
+  for (;;) {
+    if (c.kind == 0) {
+      if (c.qi >= c.q1) return false;
+      const Instr in = p.instrs[c.qi];
+      const OpDesc& op = p.ops[in.op];
+      c.op = &op;
+      const int type = op.type;
+      if (type == OP_GEMV) {
+        c.swiglu = op.out_kind == OUT_SWIGLU;
+        c.glog = c.swiglu ? op.rg / 2 : op.rg;
+        c.a = in.a;
+        c.n = in.b - in.a;
+        c.ng = gemv_ngroups(c.n, c.glog);
+        c.K = op.K;
+        c.kc = op.kc;
+        c.pad = op.mma ? 16 : 0;  // the tensor-core path pads rows for ldmatrix
+        c.passes = op.passes;
+        c.pass = c.grp = c.k0 = 0;
+        if (c.ng == 0) {
+          ++c.qi;
+          continue;
+        }
+        cursor_group(c, lane);
+        c.kind = 1;
+      } else if (type == OP_ATTN) {
+        const int hkv = op.n_kv_heads, hd = op.head_dim;
+        const int b = in.a / hkv, g = in.a % hkv;
+        attn_range(p, op, b, in.b, c.t, c.t1);
+        c.P = kChunkBytes / (4 * hd);
+        c.pos_bytes = hd * 2;
+        c.kv = (lane == 0) ? p.kcache + kv_index(p, op, b, g, 0) : p.vcache + kv_index(p, op, b, g, 0);
+        c.kind = 2;
+      } else {
+        ++c.qi;
+        continue;
+      }
+    }
+    if (c.kind == 1) {
+      const int kw = min(c.kc, c.K - c.k0);
+      total = (uint32_t)(c.nphys * kw * 2);
+      if (lane < c.nphys) {
+        src = c.row + c.k0;
+        bytes = (uint32_t)(kw * 2);
+        dst = (uint32_t)(lane * (kw * 2 + c.pad));
+      } else {
+        bytes = 0;
+      }
+      c.k0 += c.kc;
+      if (c.k0 >= c.K) {
+        c.k0 = 0;
+        if (++c.grp >= c.ng) {
+          c.grp = 0;
+          if (++c.pass >= c.passes) {
+            c.kind = 0;
+            ++c.qi;
+            return true;
+          }
+        }
+        cursor_group(c, lane);
+      }
+      return true;
+    }
+    // attention: K then V of up to P positions
+    if (c.t >= c.t1) {
+      c.kind = 0;
+      ++c.qi;
+      continue;
+    }
+    const int np = min(c.P, c.t1 - c.t);
+    const uint32_t nb = (uint32_t)(np * c.pos_bytes);
+    total = 2 * nb;
+    bytes = (lane < 2) ? nb : 0;
+    src = reinterpret_cast<const uint8_t*>(c.kv) + (size_t)c.t * c.pos_bytes;
+    dst = (lane == 1) ? kChunkBytes / 2 : 0;
+    c.t += c.P;
+    return true;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
 // final op: greedy argmax over the LM-head partials, sequence bookkeeping, counter reset
 // ------------------------------------------------------------------------------------------------
 __device__ void final_consume(const KParams& p, int ctid) {
@@ -1059,15 +1338,32 @@ __device__ void final_consume(const KParams& p, int ctid) {
 __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
   const int lane = threadIdx.x & 31;
   uint32_t chunk = 0;
-  for (int qi = q0; qi < q1; ++qi) {
-    const Instr in = p.instrs[qi];
-    const OpDesc& op = p.ops[in.op];
-    bool ok = true;
-    if (p.trace && lane == 0) p.trace[(size_t)qi * kTraceWords + 3] = global_timer();
-    if (op.type == OP_GEMV) ok = gemv_produce(p, op, in, rg, chunk, lane);
-    else if (op.type == OP_ATTN) ok = attn_produce(p, op, in, rg, chunk, lane);
-    if (p.trace && lane == 0) p.trace[(size_t)qi * kTraceWords + 4] = global_timer();
-    if (!ok) break;
+  const uint32_t ring_base = smem_u32(rg.base);
+  ChunkCursor mc, pc;
+  mc.qi = pc.qi = q0;
+  mc.q1 = pc.q1 = q1;
+  mc.kind = pc.kind = 0;
+  const void* src = nullptr;
+  uint32_t bytes = 0, dst = 0, total = 0;
+  if (kPrefetchAhead > 0) {
+    for (int i = 0; i < kPrefetchAhead; ++i) {
+      if (!cursor_next(p, pc, lane, src, bytes, dst, total)) break;
+      if (bytes) prefetch_l2(src, bytes);
+    }
+  }
+  int last_qi = -1;
+  while (cursor_next(p, mc, lane, src, bytes, dst, total)) {
+    if (p.trace && lane == 0 && mc.qi != last_qi) {
+      p.trace[(size_t)mc.qi * kTraceWords + 3] = global_timer();
+      last_qi = mc.qi;
+    }
+    if (!ring_acquire(rg, chunk, total, p, lane)) break;
+    if (bytes) bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + dst, src, bytes, &rg.full[chunk % kSlots]);
+    ++chunk;
+    const void* psrc = nullptr;
+    uint32_t pbytes = 0, pdst = 0, ptotal = 0;
+    if (kPrefetchAhead > 0 && cursor_next(p, pc, lane, psrc, pbytes, pdst, ptotal) && pbytes)
+      prefetch_l2(psrc, pbytes);
   }
   // every issued copy must land before the CTA may exit
   if (lane == 0) {
@@ -1111,7 +1407,9 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
     switch (op.type) {
       case OP_EMBED: embed_consume(p, op, in, ctid); break;
       case OP_GEMV:
-        if (op.staged) {
+        if (op.mma) {
+          gemv_mma_consume(p, op, in, rg, chunk, cs, actf, ctid);
+        } else if (op.staged) {
           if (nr == 1) gemv_dispatch<16, 1, true>(p, op, in, rg, chunk, cs, actf, ctid);
           else gemv_dispatch<16, 2, true>(p, op, in, rg, chunk, cs, actf, ctid);
         } else {
