@@ -70,6 +70,19 @@ struct mk_handle {
   float* state = nullptr;
   float* pend = nullptr;
   int pend_rec = 0;
+  // MLA: latent cache and the per-step query / latent-output buffers
+  uint16_t* latent = nullptr;
+  float* mla_cq = nullptr;    // [N][q_lora] normalised c_q
+  float* mla_qf = nullptr;    // [N][H * (nope + rope)] projected queries
+  float* mla_qt = nullptr;    // [N][H * (kv_lora + rope)] absorbed, rotated, scaled queries
+  float* mla_olat = nullptr;  // [N][H * kv_lora] attention output in latent space
+  int mla_qf_stride = 0, mla_qt_stride = 0, mla_olat_stride = 0;
+  // MoE routing of the current layer and the expert SwiGLU outputs
+  int32_t* route_idx = nullptr;
+  float* route_w = nullptr;
+  int32_t* union_list = nullptr;
+  float* hexp = nullptr;
+  size_t hexp_floats = 0;
   uint32_t* counters = nullptr;
   uint32_t* arrive = nullptr;
   int32_t* status = nullptr;
@@ -168,18 +181,58 @@ mk_status check_desc(mk_handle* h, const mk_model_desc& d, const mk_weights& w) 
         return fail(h, MK_ERR_UNSUPPORTED, "lin_dk %d (32, 64 or 128)", d.lin_dk);
       if (d.lin_dv % 8) return fail(h, MK_ERR_UNSUPPORTED, "lin_dv %d must be a multiple of 8", d.lin_dv);
     } else if (m == MK_MIXER_MLA) {
-      return fail(h, MK_ERR_UNSUPPORTED, "layer %d: MLA is not built in this version", i);
+      NEED(w_dq); NEED(q_norm); NEED(w_uq); NEED(w_dkv); NEED(kv_norm); NEED(w_uk); NEED(w_uv); NEED(wo);
+      // the latent attention op gives each lane 16 latent dims and 2 rope dims of a 512 + 64 latent, each
+      // warp one head of an 8-head group; the absorbed-query op gives each lane nope / 32 query dims
+      if (d.kv_lora != 512 || d.qk_rope != 64)
+        return fail(h, MK_ERR_UNSUPPORTED, "MLA latent %d + rope %d (512 + 64)", d.kv_lora, d.qk_rope);
+      if (d.qk_nope < 32 || d.qk_nope > 128 || d.qk_nope % 32)
+        return fail(h, MK_ERR_UNSUPPORTED, "qk_nope %d (32, 64, 96 or 128)", d.qk_nope);
+      if (d.mla_heads < 8 || d.mla_heads % 8) return fail(h, MK_ERR_UNSUPPORTED, "mla_heads %d (multiple of 8)", d.mla_heads);
+      if (d.v_head < 16 || d.v_head % 16) return fail(h, MK_ERR_UNSUPPORTED, "v_head %d (multiple of 16)", d.v_head);
+      if (d.q_lora < 16 || d.q_lora % 16) return fail(h, MK_ERR_UNSUPPORTED, "q_lora %d (multiple of 16)", d.q_lora);
     } else {
       return fail(h, MK_ERR_INVALID_ARG, "layer %d: mixer %d", i, m);
     }
     if (d.ffn_kind == MK_FFN_DENSE) {
       NEED(w_gate); NEED(w_up); NEED(w_down);
       if (d.ffn_dim < 8 || d.ffn_dim % 8) return fail(h, MK_ERR_INVALID_ARG, "ffn_dim %d", d.ffn_dim);
+    } else if (d.ffn_kind == MK_FFN_MOE) {
+      NEED(w_router); NEED(e_gate); NEED(e_up); NEED(e_down);
+      if (L.router_bias && !aligned16(L.router_bias)) return fail(h, MK_ERR_INVALID_ARG, "layer %d: router_bias alignment", i);
+      if (d.n_experts < 1 || d.n_experts > kMaxExperts)
+        return fail(h, MK_ERR_UNSUPPORTED, "n_experts %d (1..%d)", d.n_experts, kMaxExperts);
+      if (d.top_k < 1 || d.top_k > kMaxTopK || d.top_k > d.n_experts)
+        return fail(h, MK_ERR_UNSUPPORTED, "top_k %d (1..min(%d, n_experts))", d.top_k, kMaxTopK);
+      if (d.n_shared < 0 || d.n_shared > 8) return fail(h, MK_ERR_UNSUPPORTED, "n_shared %d (0..8)", d.n_shared);
+      if (d.n_shared) { NEED(s_gate); NEED(s_up); NEED(s_down); }
+      if (d.expert_format == MK_FMT_NVFP4) {
+        // NVFP4 rows are copied as 16-byte multiples of codes (2 per byte) and of e4m3 scales (1 per 16)
+        if (d.expert_dim < 256 || d.expert_dim % 256 || d.d_model % 256)
+          return fail(h, MK_ERR_UNSUPPORTED, "NVFP4 experts need expert_dim and d_model multiples of 256");
+        NEED(e_gate_scales); NEED(e_up_scales); NEED(e_down_scales);
+        NEED(e_gate_gscale); NEED(e_up_gscale); NEED(e_down_gscale);
+        if (d.n_shared) {
+          NEED(s_gate_scales); NEED(s_up_scales); NEED(s_down_scales);
+          NEED(s_gate_gscale); NEED(s_up_gscale); NEED(s_down_gscale);
+        }
+      } else if (d.expert_format == MK_FMT_BF16) {
+        if (d.expert_dim < 8 || d.expert_dim % 8) return fail(h, MK_ERR_INVALID_ARG, "expert_dim %d", d.expert_dim);
+      } else {
+        return fail(h, MK_ERR_INVALID_ARG, "expert_format %d", d.expert_format);
+      }
     } else {
-      return fail(h, MK_ERR_UNSUPPORTED, "MoE is not built in this version");
+      return fail(h, MK_ERR_INVALID_ARG, "ffn_kind %d", d.ffn_kind);
     }
 #undef NEED
   }
+  bool has_gqa = false, has_mla = false;
+  for (int i = 0; i < d.n_layers; ++i) {
+    has_gqa = has_gqa || d.mixer[i] == MK_MIXER_GQA;
+    has_mla = has_mla || d.mixer[i] == MK_MIXER_MLA;
+  }
+  if (has_gqa && has_mla && d.head_dim != d.qk_rope)
+    return fail(h, MK_ERR_UNSUPPORTED, "GQA and MLA layers in one model need head_dim == qk_rope (one RoPE table)");
   return MK_OK;
 }
 
@@ -203,17 +256,47 @@ void derive_layout(mk_handle* h) {
     } else if (is_delta(m)) {
       proj = std::max(proj, delta_proj_cols(D, m));
       attn = std::max(attn, D.lin_heads * D.lin_dv);
+    } else if (m == MK_MIXER_MLA) {
+      proj = std::max(proj, D.q_lora + D.kv_lora + D.qk_rope);
+      attn = std::max(attn, D.mla_heads * D.v_head);
     }
   }
   h->proj_stride = round_up(proj, 8);
   h->attn_stride = round_up(attn, 8);
-  h->hbuf_stride = round_up(std::max(D.ffn_dim, 8), 8);
-  h->max_ops = 16 * D.n_layers + 16;
+  // dense SwiGLU hidden rows, or the MoE router logits
+  const int hb = D.ffn_kind == MK_FFN_MOE ? D.n_experts : D.ffn_dim;
+  h->hbuf_stride = round_up(std::max(hb, 8), 8);
+  h->max_ops = 32 * D.n_layers + 16;
   if (h->n_gqa) {
     h->attn_part_stride = D.head_dim + 4;
     h->rot_dim = D.head_dim;
   }
+  if (h->n_mla) {
+    h->attn_part_stride = std::max(h->attn_part_stride, D.kv_lora + 4);
+    h->rot_dim = D.qk_rope;
+    h->mla_qf_stride = D.mla_heads * (D.qk_nope + D.qk_rope);
+    h->mla_qt_stride = D.mla_heads * (D.kv_lora + D.qk_rope);
+    h->mla_olat_stride = D.mla_heads * D.kv_lora;
+  }
   if (h->n_delta) h->pend_rec = round_up(2 * D.lin_dk + D.lin_dv + 1, 4);
+  if (D.ffn_kind == MK_FFN_MOE) {
+    // the shared experts plus the union of the experts the rows of one step select
+    const int64_t uni = std::min<int64_t>(D.n_experts, (int64_t)h->nmax * D.top_k);
+    h->hexp_floats = (size_t)(D.n_shared + uni) * h->nmax * D.expert_dim;
+  }
+}
+
+// Attention partial records of one step (GQA and MLA share the buffer): (sequence, kv head or head group,
+// context chunk) triples times rows times heads per group. The chunk count of an op is at most n_sm / the
+// other factors, so the triples are at most max(n_sm, sequences x groups).
+size_t attn_part_records(const mk_handle* h, int B, int R) {
+  const mk_model_desc& D = h->desc;
+  size_t recs = 0;
+  if (h->n_gqa)
+    recs = (size_t)std::max(h->n_sm, B * D.n_kv_heads) * R * (D.n_q_heads / D.n_kv_heads);
+  if (h->n_mla)
+    recs = std::max(recs, (size_t)std::max(h->n_sm, B * (D.mla_heads / 8)) * R * 8);
+  return 2 * recs;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -308,6 +391,207 @@ OpDesc gemv_desc(int K, std::initializer_list<std::pair<const void*, int>> mats)
   return d;
 }
 
+// Multi-head latent attention, absorbed form, of layer i (the ops are described in mk_kernel.cu):
+//   GEMV [w_dq; w_dkv] on RMSNorm(x) -> proj;  MLA_PREP: c_q norm -> mla_cq, latent (norm + rope) -> cache;
+//   GEMV w_uq on c_q -> mla_qf;  MLA_QABS -> mla_qt;  MLA_ATTN over context chunks -> partials;
+//   ATTN_COMBINE -> mla_olat;  MLA_UV -> attn_out;  GEMV wo, residual add.
+void mla_layer(mk_handle* h, Builder& bld, int i, int B, int R) {
+  const mk_model_desc& D = h->desc;
+  const mk_layer_weights& L = h->w.layers[i];
+  const int N = B * R, d = D.d_model;
+  const int H = D.mla_heads, nope = D.qk_nope, rp = D.qk_rope, kl = D.kv_lora, ql = D.q_lora;
+  constexpr int G = kConsumerWarps;  // heads per attention group (one per warp)
+  const int ngr = H / G;
+
+  OpDesc a = gemv_desc(d, {{L.w_dq, ql}, {L.w_dkv, kl + rp}});
+  a.layer = i;
+  a.in_kind = IN_NORM;
+  a.gain = reinterpret_cast<const uint16_t*>(L.attn_norm);
+  a.ssq_in = 2 * i;
+  a.out_kind = OUT_STORE;
+  a.out = h->proj;
+  a.out_stride = h->proj_stride;
+  gemv_op(bld, a, N);
+
+  OpDesc pr = blank(OP_MLA_PREP);
+  pr.layer = i;
+  pr.slot = h->slot[i];
+  pr.q_lora = ql;
+  pr.kv_lora = kl;
+  pr.rope = rp;
+  pr.q_norm = reinterpret_cast<const uint16_t*>(L.q_norm);
+  pr.kv_norm = reinterpret_cast<const uint16_t*>(L.kv_norm);
+  pr.in = h->proj;
+  pr.in_stride = h->proj_stride;
+  pr.aux = h->mla_cq;
+  pr.aux_stride = ql;
+  const int op_pr = bld.add(pr);
+  // one warp per (row, q or kv half); the op indexes its work by SM, so SM s takes items 8s .. 8s + 7
+  const int n_pr = std::min(h->n_sm, (2 * N + kConsumerWarps - 1) / kConsumerWarps);
+  for (int s = 0; s < n_pr; ++s) bld.place(op_pr, s, 0, 0, 0);
+
+  OpDesc uq = gemv_desc(ql, {{L.w_uq, h->mla_qf_stride}});
+  uq.layer = i;
+  uq.in_kind = IN_BUF;
+  uq.in = h->mla_cq;
+  uq.in_stride = ql;
+  uq.out_kind = OUT_STORE;
+  uq.out = h->mla_qf;
+  uq.out_stride = h->mla_qf_stride;
+  gemv_op(bld, uq, N);
+
+  OpDesc qa = blank(OP_MLA_QABS);
+  qa.layer = i;
+  qa.nope = nope;
+  qa.rope = rp;
+  qa.kv_lora = kl;
+  qa.w_uk = reinterpret_cast<const uint16_t*>(L.w_uk);
+  qa.in = h->mla_qf;
+  qa.in_stride = h->mla_qf_stride;
+  qa.out = h->mla_qt;
+  qa.out_stride = h->mla_qt_stride;
+  const int op_qa = bld.add(qa);
+  int k = 0;
+  for (int hh = 0; hh < H; ++hh)
+    for (int cb = 0; cb < kl / 128; ++cb, ++k) bld.place(op_qa, k % h->n_sm, hh, cb, 0);
+
+  OpDesc at = blank(OP_MLA_ATTN);
+  at.layer = i;
+  at.slot = h->slot[i];
+  at.kv_lora = kl;
+  at.rope = rp;
+  at.n_heads = H;
+  at.n_kv_heads = ngr;
+  at.groups = G;
+  at.head_dim = kl;
+  at.in = h->mla_qt;
+  at.in_stride = h->mla_qt_stride;
+  const int rows_per = std::min(R, 2);  // (row, head) pairs per warp
+  const int nsplit = (R + rows_per - 1) / rows_per;
+  at.nchunk = std::max(1, h->n_sm / (B * ngr * nsplit));
+  const int op_at = bld.add(at);
+  k = 0;
+  for (int b = 0; b < B; ++b)
+    for (int g = 0; g < ngr; ++g)
+      for (int c = 0; c < at.nchunk; ++c)
+        for (int sp = 0; sp < nsplit; ++sp, ++k) {
+          const int rlo = sp * rows_per, rhi = std::min(R, rlo + rows_per);
+          bld.place(op_at, k % h->n_sm, b * ngr + g, c, rlo | (rhi << 8));
+        }
+
+  OpDesc cb = at;
+  cb.type = OP_ATTN_COMBINE;
+  cb.n_instr = 0;
+  cb.n_deps = 0;
+  cb.out = h->mla_olat;
+  cb.out_stride = h->mla_olat_stride;
+  const int op_cb = bld.add(cb);
+  k = 0;
+  for (int b = 0; b < B; ++b)
+    for (int r = 0; r < R; ++r)
+      for (int hh = 0; hh < H; ++hh, ++k) bld.place(op_cb, k % h->n_sm, b, r, hh);
+
+  OpDesc uv = blank(OP_MLA_UV);
+  uv.layer = i;
+  uv.kv_lora = kl;
+  uv.v_head = D.v_head;
+  uv.w_uv = reinterpret_cast<const uint16_t*>(L.w_uv);
+  uv.in = h->mla_olat;
+  uv.in_stride = h->mla_olat_stride;
+  uv.out = h->attn_out;
+  uv.out_stride = h->attn_stride;
+  const int op_uv = bld.add(uv);
+  k = 0;
+  for (int hh = 0; hh < H; ++hh)
+    for (int jb = 0; jb < (D.v_head + 63) / 64; ++jb, ++k) bld.place(op_uv, k % h->n_sm, hh, jb, 0);
+
+  OpDesc o = gemv_desc(H * D.v_head, {{L.wo, d}});
+  o.layer = i;
+  o.in_kind = IN_BUF;
+  o.in = h->attn_out;
+  o.in_stride = h->attn_stride;
+  o.out_kind = OUT_RESID;
+  o.ssq_out = 2 * i + 1;
+  gemv_op(bld, o, N);
+}
+
+// MoE feed-forward of layer i: router GEMV on RMSNorm(x) -> hbuf; ROUTE (one instruction); MOE_UP over
+// the F hidden rows and MOE_DOWN over the d output rows, each one instruction per SM covering its row
+// range of every selected expert, so an SM's work does not depend on which experts the rows picked.
+void moe_layer(mk_handle* h, Builder& bld, int i, int N) {
+  const mk_model_desc& D = h->desc;
+  const mk_layer_weights& L = h->w.layers[i];
+  const int d = D.d_model, E = D.n_experts, F = D.expert_dim;
+  const bool fp4 = D.expert_format == MK_FMT_NVFP4;
+
+  OpDesc z = gemv_desc(d, {{L.w_router, E}});
+  z.layer = i;
+  z.in_kind = IN_NORM;
+  z.gain = reinterpret_cast<const uint16_t*>(L.ffn_norm);
+  z.ssq_in = 2 * i + 1;
+  z.out_kind = OUT_STORE;
+  z.out = h->hbuf;
+  z.out_stride = h->hbuf_stride;
+  gemv_op(bld, z, N);
+
+  OpDesc ro = blank(OP_ROUTE);
+  ro.layer = i;
+  ro.n_experts = E;
+  ro.top_k = D.top_k;
+  ro.route_scale = D.route_scale;
+  ro.router_bias = L.router_bias;
+  ro.in = h->hbuf;
+  ro.in_stride = h->hbuf_stride;
+  const int op_ro = bld.add(ro);
+  bld.place(op_ro, 0, 0, 0, 0);
+
+  OpDesc ex = blank(OP_MOE_UP);
+  ex.layer = i;
+  ex.n_experts = E;
+  ex.n_shared = D.n_shared;
+  ex.top_k = D.top_k;
+  ex.fp4 = fp4 ? 1 : 0;
+  ex.route_op = op_ro;
+  ex.F = F;
+  // the kernel's expert GEMV: 16 weight rows per group and 4 (bf16) or 8 (NVFP4) inputs per thread for up
+  // to 4 activation rows; 8 rows, 8 inputs per thread and ceil(N / 8) passes otherwise
+  ex.rg = N <= 4 ? 16 : 8;
+  ex.kc = (fp4 || N > 4 ? 8 : 4) * kConsumerThreads;
+  ex.passes = N <= 8 ? 1 : (N + 7) / 8;
+
+  OpDesc up = ex;
+  up.ew[0] = L.e_gate;
+  up.ew[1] = L.e_up;
+  up.sw[0] = L.s_gate;
+  up.sw[1] = L.s_up;
+  up.esc[0] = L.e_gate_scales;
+  up.esc[1] = L.e_up_scales;
+  up.ssc[0] = L.s_gate_scales;
+  up.ssc[1] = L.s_up_scales;
+  up.egs[0] = L.e_gate_gscale;
+  up.egs[1] = L.e_up_gscale;
+  up.sgs[0] = L.s_gate_gscale;
+  up.sgs[1] = L.s_up_gscale;
+  up.gain = reinterpret_cast<const uint16_t*>(L.ffn_norm);
+  up.ssq_in = 2 * i + 1;
+  const int op_up = bld.add(up);
+  for (int s = 0; s < h->n_sm; ++s)
+    bld.place(op_up, s, (int)((int64_t)F * s / h->n_sm), (int)((int64_t)F * (s + 1) / h->n_sm), 0);
+
+  OpDesc dn = ex;
+  dn.type = OP_MOE_DOWN;
+  dn.ew[0] = L.e_down;
+  dn.sw[0] = L.s_down;
+  dn.esc[0] = L.e_down_scales;
+  dn.ssc[0] = L.s_down_scales;
+  dn.egs[0] = L.e_down_gscale;
+  dn.sgs[0] = L.s_down_gscale;
+  dn.ssq_out = 2 * i + 2;
+  const int op_dn = bld.add(dn);
+  for (int s = 0; s < h->n_sm; ++s)
+    bld.place(op_dn, s, (int)((int64_t)d * s / h->n_sm), (int)((int64_t)d * (s + 1) / h->n_sm), 0);
+}
+
 // Host-side program of one (batch, rows, head) shape: the op list, the flattened per-SM queues and their
 // offsets. Reads the handle's shape, weights, slots and activation buffer pointers; touches no device.
 struct HostProgram {
@@ -398,7 +682,7 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
       o.out_kind = OUT_RESID;
       o.ssq_out = 2 * i + 1;
       gemv_op(bld, o, N);
-    } else {  // gated delta net / KDA
+    } else if (is_delta(m)) {  // gated delta net / KDA
       const int H = D.lin_heads, dk = D.lin_dk, dv = D.lin_dv;
       const bool kda = m == MK_MIXER_KDA;
       OpDesc pj = gemv_desc(d, {{L.wq, H * dk}, {L.wk, H * dk}, {L.wv, H * dv}, {L.wa, kda ? H * dk : H}, {L.wb, H}});
@@ -442,6 +726,12 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
       o.out_kind = OUT_RESID;
       o.ssq_out = 2 * i + 1;
       gemv_op(bld, o, N);
+    } else {
+      mla_layer(h, bld, i, B, R);
+    }
+    if (D.ffn_kind == MK_FFN_MOE) {
+      moe_layer(h, bld, i, N);
+      continue;
     }
     // dense SwiGLU
     OpDesc up = gemv_desc(d, {{L.w_gate, D.ffn_dim}, {L.w_up, D.ffn_dim}});
@@ -585,6 +875,11 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.state = h->state;
   p.pend = h->pend;
   p.pend_rec = h->pend_rec;
+  p.latent = h->latent;
+  p.route_idx = h->route_idx;
+  p.route_w = h->route_w;
+  p.union_list = h->union_list;
+  p.hexp = h->hexp;
   p.seq = h->seq;
   p.rope = h->rope;
   p.rot_dim = h->rot_dim;
@@ -677,13 +972,25 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
   ALLOC(stage_argmax, kMaxN);
   ALLOC(stage_logits, (size_t)h->nmax * D.vocab);
   if (h->n_gqa) {
-    const int hkv = D.n_kv_heads, hd = D.head_dim, G = D.n_q_heads / D.n_kv_heads;
+    const int hkv = D.n_kv_heads, hd = D.head_dim;
     const size_t cache = (size_t)h->n_gqa * Bm * hkv * D.max_ctx * hd;
     ALLOC(kcache, cache);
     ALLOC(vcache, cache);
-    const size_t recs = (size_t)std::max(h->n_sm, Bm * hkv) * Rm * G * 2;
-    ALLOC(attn_part, recs * h->attn_part_stride);
     ALLOC(arrive, (size_t)h->n_gqa * Bm * hkv);
+  }
+  if (h->n_gqa || h->n_mla) ALLOC(attn_part, attn_part_records(h, Bm, Rm) * h->attn_part_stride);
+  if (h->n_mla) {
+    ALLOC(latent, (size_t)h->n_mla * Bm * D.max_ctx * (D.kv_lora + D.qk_rope));
+    ALLOC(mla_cq, (size_t)kMaxN * D.q_lora);
+    ALLOC(mla_qf, (size_t)kMaxN * h->mla_qf_stride);
+    ALLOC(mla_qt, (size_t)kMaxN * h->mla_qt_stride);
+    ALLOC(mla_olat, (size_t)kMaxN * h->mla_olat_stride);
+  }
+  if (D.ffn_kind == MK_FFN_MOE) {
+    ALLOC(route_idx, (size_t)kMaxN * kMaxTopK);
+    ALLOC(route_w, (size_t)kMaxN * kMaxTopK);
+    ALLOC(union_list, (size_t)kMaxExperts + 1);
+    ALLOC(hexp, h->hexp_floats);
   }
   if (h->n_delta) {
     const int H = D.lin_heads, dk = D.lin_dk, dv = D.lin_dv;
@@ -909,6 +1216,12 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   }
   const mk_model_desc& D = tmp.desc;
   if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows) return MK_ERR_INVALID_ARG;
+  bool has_mla = false;
+  for (int i = 0; i < D.n_layers; ++i) has_mla = has_mla || D.mixer[i] == MK_MIXER_MLA;
+  if (has_mla || D.ffn_kind == MK_FFN_MOE) {
+    fprintf(stderr, "mk_decode_step_static: MLA and MoE models are not accepted by this call\n");
+    return MK_ERR_UNSUPPORTED;
+  }
   cudaError_t e = cudaGetDevice(&tmp.device);
   if (e != cudaSuccess) return MK_ERR_CUDA;
   int coop = 0, smem_optin = 0;
@@ -943,11 +1256,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   const size_t o_ssq = carve(off, sizeof(float) * (size_t)(2 * D.n_layers + 1) * tmp.n_sm * kMaxN);
   const size_t o_amax = carve(off, sizeof(float2) * (size_t)tmp.n_sm * kMaxN);
   size_t o_apart = 0, o_rope = 0;
-  if (tmp.n_gqa) {
-    const int G = D.n_q_heads / D.n_kv_heads;
-    const size_t recs = (size_t)std::max(tmp.n_sm, batch * hkv) * rows * G * 2;
-    o_apart = carve(off, sizeof(float) * recs * tmp.attn_part_stride);
-  }
+  if (tmp.n_gqa) o_apart = carve(off, sizeof(float) * attn_part_records(&tmp, batch, rows) * tmp.attn_part_stride);
   if (tmp.rot_dim) o_rope = carve(off, sizeof(float2) * (size_t)D.max_ctx * (tmp.rot_dim / 2));
   tmp.counters = reinterpret_cast<uint32_t*>(base + o_counters);
   tmp.arrive = tmp.n_gqa ? reinterpret_cast<uint32_t*>(base + o_arrive) : nullptr;

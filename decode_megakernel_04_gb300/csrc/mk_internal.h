@@ -45,7 +45,9 @@ enum OpType : int32_t {
   OP_MOE_UP = 8,      // MoE: gate/up GEMV of shared + routed experts, SwiGLU
   OP_MOE_DOWN = 9,    // MoE: down GEMV of shared + routed experts, weighted sum, residual add
   OP_FINAL = 10,      // greedy argmax, sequence bookkeeping, counter reset
-  OP_ATTN_COMBINE = 11,  // GQA: merge the context-chunk partials of one (sequence, row, q head)
+  OP_ATTN_COMBINE = 11,  // GQA / MLA: merge the context-chunk partials of one (sequence, row, head)
+  OP_MLA_QABS = 12,   // MLA: absorbed query q~_h = W_UK[h] q_nope_h, rotated q_rope (scaled for the softmax)
+  OP_MLA_UV = 13,     // MLA: o_h = W_UV[h] o_lat_h
 };
 
 enum InKind : int32_t { IN_NORM = 0, IN_BUF = 1 };
@@ -90,6 +92,26 @@ struct OpDesc {
   int32_t dk, dv;
   int32_t per_channel_decay; // KDA
   int32_t col_group;         // value columns per instruction
+  // ---- MoE (OP_ROUTE, OP_MOE_UP, OP_MOE_DOWN) ----
+  int32_t n_experts, n_shared, top_k, fp4;
+  int32_t route_op;          // index of the op whose routing the expert ops read
+  int32_t F;                 // expert hidden size
+  float route_scale;
+  const float* router_bias;  // [E] or NULL
+  const void* ew[2];         // routed experts: gate, up (MOE_UP) or down (MOE_DOWN); bf16 or e2m1 codes
+  const void* sw[2];         // shared experts, same layout
+  const uint8_t* esc[2];     // e4m3 block scales (NVFP4)
+  const uint8_t* ssc[2];
+  const float* egs[2];       // fp32 per-expert tensor scales (NVFP4)
+  const float* sgs[2];
+  // ---- MLA ----
+  int32_t q_lora, kv_lora, nope, rope, v_head;
+  const uint16_t* w_uk;      // [H, kv_lora, nope]
+  const uint16_t* w_uv;      // [H, v_head, kv_lora]
+  const uint16_t* q_norm;
+  const uint16_t* kv_norm;
+  float* aux;                // op-specific second output (MLA: the normalised c_q)
+  int32_t aux_stride;
 };
 
 struct Instr {
@@ -143,11 +165,12 @@ struct KParams {
   int32_t pend_rec;         // floats per pending record (k_hat, v, alpha, beta)
   // MLA: latent cache [slot][max_batch][max_ctx][kv_lora + rope] bf16
   uint16_t* latent;
-  // MoE routing: per layer-slot [N][top_k] expert ids / weights, per expert row lists
+  // MoE routing of the current layer: [N][top_k] expert ids and weights; the union of the experts the
+  // step selected, ascending: union_list[0] = count, union_list[1..] = experts
   int32_t* route_idx;
   float* route_w;
-  int32_t* expert_rows;     // [E][kMaxN] row ids routed to an expert (this step)
-  int32_t* expert_cnt;      // [E] + union list
+  int32_t* union_list;
+  float* hexp;              // [n_shared + union][N][F] expert SwiGLU outputs
   SeqState* seq;
   const float2* rope;       // [max_ctx][rot_dim / 2] (cos, sin)
   int32_t rot_dim;

@@ -14,6 +14,7 @@
 // abort flag that every other wait also polls, drains its in-flight copies and returns.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 #include <stdint.h>
 
@@ -149,6 +150,7 @@ struct CSmem {
   int32_t last;
   int32_t pad[2];
   float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
+  float e2m1[16];                        // e2m1 code -> value (NVFP4 experts)
 };
 
 struct Ring {
@@ -988,7 +990,7 @@ __device__ void attn_combine_consume(const KParams& p, const OpDesc& op, const I
     mine[hd + 1] = l;
   }
   consumer_sync();
-  if (ctid < hd) {
+  for (int i = ctid; i < hd; i += kConsumerThreads) {
     float M = -CUDART_INF_F;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stage[w * (hd + 2) + hd]);
@@ -999,9 +1001,9 @@ __device__ void attn_combine_consume(const KParams& p, const OpDesc& op, const I
       if (mw == -CUDART_INF_F) continue;
       const float s = exp2f(mw - M);
       L += s * stage[w * (hd + 2) + hd + 1];
-      acc += s * stage[w * (hd + 2) + ctid];
+      acc += s * stage[w * (hd + 2) + i];
     }
-    __stcg(op.out + (size_t)(b * R + r) * op.out_stride + (size_t)hq * hd + ctid, acc / L);
+    __stcg(op.out + (size_t)(b * R + r) * op.out_stride + (size_t)hq * hd + i, acc / L);
   }
 }
 
@@ -1180,6 +1182,531 @@ __device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& i
 }
 
 // ------------------------------------------------------------------------------------------------
+// MoE routing (one instruction): for each row, s = sigmoid(z) over the experts; top_k experts are picked
+// by top_k sequential argmax passes over s + bias, the lowest index winning a tie (the pages' router takes
+// its top-k as sequential argmax passes: Kimi K3's TPU megakernel, "How it maps onto a TPU v7"); the
+// weights are route_scale * s_sel / sum(s_sel). Also the union of the picked experts, ascending.
+// ------------------------------------------------------------------------------------------------
+__device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int E = op.n_experts, K = op.top_k, N = p.N;
+  int* flags = reinterpret_cast<int*>(stage);
+  for (int e = ctid; e < E; e += kConsumerThreads) flags[e] = 0;
+  consumer_sync();
+  for (int n = warp; n < N; n += kConsumerWarps) {
+    float sc[kMaxExperts / 32], bs[kMaxExperts / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      const int e = lane + 32 * j;
+      sc[j] = 0.f;
+      bs[j] = -CUDART_INF_F;
+      if (e < E) {
+        sc[j] = sigmoidf_(__ldcg(op.in + (size_t)n * op.in_stride + e));
+        bs[j] = sc[j] + (op.router_bias ? __ldg(op.router_bias + e) : 0.f);
+      }
+    }
+    float ssum = 0.f;
+    float ssel[kMaxTopK];
+    for (int k = 0; k < K; ++k) {
+      float bv = -CUDART_INF_F;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        const int e = lane + 32 * j;
+        if (bs[j] > bv) { bv = bs[j]; bi = e; }  // ascending e within a lane: first occurrence wins
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      float s_w = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        if (lane + 32 * j == bi) {
+          s_w = sc[j];
+          bs[j] = -CUDART_INF_F;  // taken
+        }
+      }
+      s_w = __shfl_sync(0xffffffffu, s_w, bi & 31);
+      ssel[k] = s_w;
+      ssum += s_w;
+      if (lane == 0) {
+        __stcg(p.route_idx + n * kMaxTopK + k, bi);
+        flags[bi] = 1;
+      }
+    }
+    if (lane == 0)
+      for (int k = 0; k < K; ++k) __stcg(p.route_w + n * kMaxTopK + k, op.route_scale * ssel[k] / ssum);
+  }
+  consumer_sync();
+  if (ctid == 0) {
+    int cnt = 0;
+    for (int e = 0; e < E; ++e)
+      if (flags[e]) __stcg(p.union_list + 1 + cnt++, e);
+    __stcg(p.union_list, cnt);
+  }
+}
+
+// e2m1 code -> value: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0 is the
+// subnormal m * 0.5 (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6). Filled into shared memory at kernel start.
+__device__ __forceinline__ float e2m1_value(int code) {
+  const int e = (code >> 1) & 3, m = code & 1;
+  const float mag = (e == 0) ? 0.5f * m : ldexpf(1.0f + 0.5f * m, e - 1);
+  return (code & 8) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  __nv_fp8_e4m3 v;
+  v.__x = b;
+  return static_cast<float>(v);
+}
+
+// Weight row r of matrix m (0: gate / down, 1: up) of selected expert slot j; for NVFP4 also its scales.
+struct ExpertRow {
+  const uint8_t* w;
+  const uint8_t* s;
+};
+__device__ __forceinline__ ExpertRow expert_row(const KParams& p, const OpDesc& op, int j, int m, int r, int K) {
+  const int S = op.n_shared;
+  const bool shared = j < S;
+  const int e = shared ? j : __ldcg(p.union_list + 1 + (j - S));
+  const int rows = (op.type == OP_MOE_UP) ? op.F : p.d;
+  const size_t row = (size_t)e * rows + r;
+  ExpertRow out;
+  const void* base = shared ? op.sw[m] : op.ew[m];
+  if (op.fp4) {
+    out.w = static_cast<const uint8_t*>(base) + row * (K / 2);
+    out.s = (shared ? op.ssc[m] : op.esc[m]) + row * (K / 16);
+  } else {
+    out.w = static_cast<const uint8_t*>(base) + row * K * 2;
+    out.s = nullptr;
+  }
+  return out;
+}
+
+__device__ __forceinline__ float expert_gscale(const KParams& p, const OpDesc& op, int j, int m) {
+  if (!op.fp4) return 1.f;
+  const int S = op.n_shared;
+  if (j < S) return __ldg(op.sgs[m] + j);
+  return __ldg(op.egs[m] + __ldcg(p.union_list + 1 + (j - S)));
+}
+
+// ------------------------------------------------------------------------------------------------
+// MoE expert GEMVs. One instruction per SM covers output rows [a, b) of EVERY selected expert (the shared
+// expert(s), then the step's union of routed experts), so the work per SM does not depend on routing.
+//   OP_MOE_UP:   hexp[j][n][f] = silu(g) * u,  g / u = rows f of expert j's gate / up times RMSNorm(x)_n
+//   OP_MOE_DOWN: x[n][r] += sum_j w[j][n] * (down_j[r] . hexp[j][n]),  w = 1 for shared experts, the
+//                router weight for routed ones (0 when row n did not pick expert j)
+// Weights stream through the ring like a dense GEMV (bf16 rows, or NVFP4 rows = codes then block
+// scales); inputs come from L2 per chunk. NVFP4 decodes as e2m1 * e4m3 (exact in fp32) and the fp32
+// tensor scale multiplies the dot product.
+// ------------------------------------------------------------------------------------------------
+template <int RG, int NR, int CPL, bool FP4>
+__device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+                            CSmem& cs, float* act, int ctid) {
+  constexpr int KC = CPL * kConsumerThreads;
+  constexpr int V = RG * NR;
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const bool up = op.type == OP_MOE_UP;
+  const int N = p.N;
+  const int K = up ? p.d : op.F;
+  const int glog = up ? RG / 2 : RG;
+  const int nsel = op.n_shared + __ldcg(p.union_list);
+  const int nrows = in.b - in.a;
+  const int ng = gemv_ngroups(nrows, glog);
+  const int passes = op.passes;
+  // DOWN: each row's routing (expert ids, weights) and this SM's slice of x, in the staging area
+  int* ridx = reinterpret_cast<int*>(act);  // [N][top_k]
+  float* rw = act + N * op.top_k;           // [N][top_k]
+  float* xres = act + 2 * N * op.top_k;     // [N][nrows]
+  if (up) {
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      float s = 0.f;
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      s = warp_sum(s);
+      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)p.d + p.eps);
+    }
+  } else {
+    for (int i = ctid; i < N * op.top_k; i += kConsumerThreads) {
+      const int n = i / op.top_k, k = i % op.top_k;
+      ridx[i] = __ldcg(p.route_idx + n * kMaxTopK + k);
+      rw[i] = __ldcg(p.route_w + n * kMaxTopK + k);
+    }
+    for (int i = ctid; i < N * nrows; i += kConsumerThreads)
+      xres[i] = __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows);
+  }
+  consumer_sync();
+
+  for (int j = 0; j < nsel && ng > 0; ++j) {
+    const float gs0 = expert_gscale(p, op, j, 0);
+    const float gs1 = up ? expert_gscale(p, op, j, 1) : 1.f;
+    const float* hin = p.hexp + (size_t)j * N * op.F;  // DOWN input
+    const int ej = j < op.n_shared ? -1 : __ldcg(p.union_list + 1 + (j - op.n_shared));
+    for (int pass = 0; pass < passes; ++pass) {
+      const int nbase = pass * NR;
+      for (int grp = 0; grp < ng; ++grp) {
+        const int g0 = gemv_group_row(in.a, nrows, ng, grp);
+        const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
+        float acc[RG][NR];
+#pragma unroll
+        for (int i = 0; i < RG; ++i)
+#pragma unroll
+          for (int n = 0; n < NR; ++n) acc[i][n] = 0.f;
+        for (int k0 = 0; k0 < K; k0 += KC) {
+          const int kw = min(KC, K - k0);
+          const int col = ctid * CPL;
+          float a[NR][CPL];
+          if (col < kw) {
+            float gsc[CPL];
+            if (up) load_bf16_global<CPL>(op.gain + k0 + col, gsc);
+#pragma unroll
+            for (int n = 0; n < NR; ++n) {
+              const int row = nbase + n;
+              if (row < N) {
+                if (up) {
+                  load_f32<CPL>(p.x + (size_t)row * p.d + k0 + col, a[n]);
+                  const float s = cs.inv_rms[row];
+#pragma unroll
+                  for (int c = 0; c < CPL; ++c) a[n][c] *= s * gsc[c];
+                } else {
+                  load_f32<CPL>(hin + (size_t)row * op.F + k0 + col, a[n]);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
+              }
+            }
+          }
+          ring_wait_full(rg, chunk, p);
+          if (col < kw) {
+            const uint8_t* slot = rg.slot_ptr(chunk);
+            if (FP4) {
+              const int pitch = kw / 2 + kw / 16;
+#pragma unroll
+              for (int i = 0; i < RG; ++i) {
+                const uint8_t* rowp = slot + (size_t)i * pitch;
+                const uint32_t codes = *reinterpret_cast<const uint32_t*>(rowp + col / 2);
+                const float sc = e4m3_to_f32(rowp[kw / 2 + col / 16]);
+                float wf[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) wf[c] = cs.e2m1[(codes >> (4 * c)) & 15u] * sc;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                  for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[c], a[n][c], acc[i][n]);
+              }
+            } else {
+              const uint8_t* wbase = slot + col * 2;
+              float wf[RG][CPL];
+#pragma unroll
+              for (int i = 0; i < RG; ++i) load_bf16_row<CPL>(wbase + (size_t)i * kw * 2, wf[i]);
+#pragma unroll
+              for (int i = 0; i < RG; ++i)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                  for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[i][c], a[n][c], acc[i][n]);
+            }
+          }
+          ring_release(rg, chunk, lane);
+          ++chunk;
+        }
+        float v[V];
+#pragma unroll
+        for (int i = 0; i < RG; ++i)
+#pragma unroll
+          for (int n = 0; n < NR; ++n) v[i * NR + n] = acc[i][n];
+        block_reduce<V>(v, cs, warp, lane, ctid);
+        if (up) {
+          if (ctid < nl * NR) {
+            const int jj = ctid / NR, n = ctid % NR, row = nbase + n;
+            if (row < N) {
+              const float g = cs.val[jj * NR + n] * gs0;
+              const float u = cs.val[(nl + jj) * NR + n] * gs1;
+              __stcg(p.hexp + ((size_t)j * N + row) * op.F + g0 + jj, g / (1.0f + expf(-g)) * u);
+            }
+          }
+        } else if (ctid < V) {
+          const int i = ctid / NR, n = ctid % NR, row = nbase + n;
+          if (i < nl && row < N) {
+            float w = (ej < 0) ? 1.f : 0.f;  // shared experts weigh 1, routed ones their router weight
+            for (int k = 0; k < op.top_k; ++k)
+              if (ridx[row * op.top_k + k] == ej) w = rw[row * op.top_k + k];
+            xres[row * nrows + (g0 - in.a) + i] += w * (cs.val[ctid] * gs0);
+          }
+        }
+        consumer_sync();
+      }
+    }
+  }
+  if (!up) {
+    // write the SM's slice of x back and the RMS partial of the new x
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      float s = 0.f;
+      for (int i = lane; i < nrows; i += 32) {
+        const float xn = xres[n * nrows + i];
+        __stcg(p.x + (size_t)n * p.d + in.a + i, xn);
+        s += xn * xn;
+      }
+      s = warp_sum(s);
+      if (lane == 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + blockIdx.x) * kMaxN + n], s);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Multi-head latent attention, absorbed form. The cache holds one (kv_lora + rope)-wide bf16 latent per
+// position (576 = 512 + 64 in the pages' model: Kimi K3's TPU megakernel, "Why one user at a time is a
+// bandwidth problem").
+//   MLA_PREP : c_q = RMSNorm(proj[0:q_lora]) -> aux;  c_kv = RMSNorm(proj[q_lora : q_lora+kv_lora]),
+//              k_r = RoPE(proj[q_lora+kv_lora :]) -> latent cache at positions p_b + r
+//   MLA_QABS : q~_h = W_UK[h] q_nope_h (kv_lora), q_r = RoPE(q_rope_h), both times log2(e)/sqrt(nope+rope)
+//   MLA_ATTN : per (sequence, 8-head group, context chunk, rows): online softmax of q~.c + q_r.k_r over
+//              the chunk, partial (o_lat, m, l) records; the GQA combine op merges them
+//   MLA_UV   : o_h = W_UV[h] o_lat_h
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ size_t lat_index(const KParams& p, const OpDesc& op, int b, int t) {
+  return (((size_t)op.slot * p.max_batch + b) * p.max_ctx + t) * (op.kv_lora + op.rope);
+}
+
+__device__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int total = p.N * 2;
+  const int ql = op.q_lora, kl = op.kv_lora, rp = op.rope, half = rp / 2;
+  for (int it = blockIdx.x * kConsumerWarps + warp; it < total; it += p.n_sm * kConsumerWarps) {
+    const int n = it >> 1, part = it & 1;
+    const float* row = op.in + (size_t)n * op.in_stride;
+    if (part == 0) {
+      float s = 0.f;
+      for (int i = lane; i < ql; i += 32) {
+        const float v = __ldcg(row + i);
+        s += v * v;
+      }
+      const float inv = rsqrtf(warp_sum(s) / (float)ql + p.eps);
+      for (int i = lane; i < ql; i += 32)
+        __stcg(op.aux + (size_t)n * op.aux_stride + i, __ldcg(row + i) * inv * bf2f(op.q_norm[i]));
+    } else {
+      const int b = n / p.R, r = n % p.R;
+      const int pos = p.positions[b] + r;
+      uint16_t* lat = p.latent + lat_index(p, op, b, pos);
+      float s = 0.f;
+      for (int i = lane; i < kl; i += 32) {
+        const float v = __ldcg(row + ql + i);
+        s += v * v;
+      }
+      const float inv = rsqrtf(warp_sum(s) / (float)kl + p.eps);
+      for (int i = lane; i < kl; i += 32) lat[i] = f2bf(__ldcg(row + ql + i) * inv * bf2f(op.kv_norm[i]));
+      const float2* cs = p.rope + (size_t)pos * (p.rot_dim / 2);
+      for (int i = lane; i < half; i += 32) {
+        const float x1 = __ldcg(row + ql + kl + i), x2 = __ldcg(row + ql + kl + i + half);
+        const float2 t = cs[i];
+        lat[kl + i] = f2bf(x1 * t.x - x2 * t.y);
+        lat[kl + i + half] = f2bf(x2 * t.x + x1 * t.y);
+      }
+    }
+  }
+}
+
+// instruction (a = head h, b = 128-column block of the latent): qt[n][h][c] for c in the block; block 0
+// also writes the rotated rope query qt[n][h][kv_lora ..]
+__device__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int h = in.a, cb = in.b;
+  const int nope = op.nope, rp = op.rope, kl = op.kv_lora, half = rp / 2;
+  const int qw = nope + rp;  // per-head width of the projected query
+  const float qs = rsqrtf((float)(nope + rp)) * kLog2e;
+  const int ldq = op.in_stride, ldt = op.out_stride;
+  const int N = p.N;
+  const int per_warp = 128 / kConsumerWarps;  // latent columns per warp
+  const int E = nope / 32;                     // nope inputs per lane (4 for nope = 128)
+  for (int cc = 0; cc < per_warp; ++cc) {
+    const int c = cb * 128 + warp * per_warp + cc;
+    if (c >= kl) break;
+    const uint16_t* wrow = op.w_uk + ((size_t)h * kl + c) * nope + lane * E;
+    float w[4];
+    for (int e = 0; e < E; ++e) w[e] = bf2f(wrow[e]);
+    for (int n = 0; n < N; ++n) {
+      const float* q = op.in + (size_t)n * ldq + (size_t)h * qw + lane * E;
+      float d = 0.f;
+      for (int e = 0; e < E; ++e) d = fmaf(w[e], __ldcg(q + e), d);
+      d = warp_sum(d);
+      if (lane == 0) __stcg(op.out + (size_t)n * ldt + (size_t)h * (kl + rp) + c, d * qs);
+    }
+  }
+  if (cb == 0) {
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      const int b = n / p.R, r = n % p.R;
+      const int pos = p.positions[b] + r;
+      const float* q = op.in + (size_t)n * ldq + (size_t)h * qw + nope;
+      const float2* cs = p.rope + (size_t)pos * (p.rot_dim / 2);
+      float* dst = op.out + (size_t)n * ldt + (size_t)h * (kl + rp) + kl;
+      for (int i = lane; i < half; i += 32) {
+        const float x1 = __ldcg(q + i), x2 = __ldcg(q + i + half);
+        const float2 t = cs[i];
+        __stcg(dst + i, (x1 * t.x - x2 * t.y) * qs);
+        __stcg(dst + i + half, (x2 * t.x + x1 * t.y) * qs);
+      }
+    }
+  }
+}
+
+// Latent attention block: up to 32 positions (rows of the latent chunk in shared memory, 576 bf16 each)
+// folded into the online softmax of the warp's J (row, head) pairs. Lane L owns latent dims
+// [16L, 16L+16) and rope dims [2L, 2L+2).
+template <int J>
+__device__ __forceinline__ void mla_block(const uint16_t* lat, int nb, int ldl, int kl, int lane, int npair_w,
+                                          const int (&prow)[J], int causal, const float (&q)[J][16],
+                                          const float (&qr)[J][2], float (&m)[J], float (&l)[J], float (&o)[J][16]) {
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (j >= npair_w) break;
+    float part[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      float acc = 0.f;
+      if (jj < nb) {
+        const uint16_t* row = lat + (size_t)jj * ldl;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(row + lane * 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(row + lane * 16 + 8);
+        const uint32_t rr = *reinterpret_cast<const uint32_t*>(row + kl + lane * 2);
+        const uint32_t ws[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc = fmaf(q[j][2 * e], bf_lo(ws[e]), acc);
+          acc = fmaf(q[j][2 * e + 1], bf_hi(ws[e]), acc);
+        }
+        acc = fmaf(qr[j][0], bf_lo(rr), acc);
+        acc = fmaf(qr[j][1], bf_hi(rr), acc);
+      }
+      part[jj] = acc;
+    }
+    MultiReduce<32, 16>::run(part, lane);
+    bool valid = lane < nb;
+    if (causal >= 0) valid = valid && (lane <= prow[j]);
+    const float s = valid ? part[0] : -CUDART_INF_F;
+    const float m_new = fmaxf(m[j], warp_max(s));
+    if (m_new == -CUDART_INF_F) continue;
+    const float corr = exp2f(m[j] - m_new);
+    const float pj = valid ? exp2f(s - m_new) : 0.f;
+    l[j] = l[j] * corr + warp_sum(pj);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[j][e] *= corr;
+    for (int jj = 0; jj < nb; ++jj) {
+      const float pp = __shfl_sync(0xffffffffu, pj, jj);
+      const uint16_t* row = lat + (size_t)jj * ldl;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(row + lane * 16);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(row + lane * 16 + 8);
+      const uint32_t ws[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        o[j][2 * e] = fmaf(pp, bf_lo(ws[e]), o[j][2 * e]);
+        o[j][2 * e + 1] = fmaf(pp, bf_hi(ws[e]), o[j][2 * e + 1]);
+      }
+    }
+    m[j] = m_new;
+  }
+}
+
+// instruction (a = b * ngroups + head group, b = chunk, c = first row | last row << 8); warp w owns head
+// group*8 + w for the rows of the instruction (J rows per warp)
+template <int J>
+__device__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                                 uint32_t& chunk, uint16_t* stage, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int ngr = op.n_kv_heads, G = op.groups;  // head groups, heads per group
+  const int b = in.a / ngr, hg = in.a % ngr, c = in.b;
+  const int rlo = in.c & 0xff, rhi = in.c >> 8;
+  const int kl = op.kv_lora, ldl = op.kv_lora + op.rope;
+  const int R = p.R;
+  const int h = hg * G + warp;
+  int t0, t1;
+  attn_range(p, op, b, c, t0, t1);
+  const int pos0 = p.positions[b];
+  const int P = kChunkBytes / (ldl * 2);
+  float q[J][16], qr[J][2], o[J][16], m[J], l[J];
+  int prow[J];
+  const int npair_w = (warp < G) ? (rhi - rlo) : 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    m[j] = -CUDART_INF_F;
+    l[j] = 0.f;
+    prow[j] = rlo + j;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) { o[j][e] = 0.f; q[j][e] = 0.f; }
+    qr[j][0] = qr[j][1] = 0.f;
+    if (j < npair_w) {
+      const float* qp = op.in + (size_t)(b * R + rlo + j) * op.in_stride + (size_t)h * ldl;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) q[j][e] = __ldcg(qp + lane * 16 + e);
+      qr[j][0] = __ldcg(qp + kl + lane * 2);
+      qr[j][1] = __ldcg(qp + kl + lane * 2 + 1);
+    }
+  }
+  for (int t = t0; t < t1; t += P) {
+    const int np = min(P, t1 - t);
+    ring_wait_full(rg, chunk, p);
+    const uint16_t* lat = reinterpret_cast<const uint16_t*>(rg.slot_ptr(chunk));
+    mla_block<J>(lat, np, ldl, kl, lane, npair_w, prow, -1, q, qr, m, l, o);
+    ring_release(rg, chunk, lane);
+    ++chunk;
+  }
+  if (c == op.nchunk - 1) {
+    for (int i = ctid; i < R * ldl; i += kConsumerThreads) {
+      const int r = i / ldl, e = i % ldl;
+      stage[i] = __ldcg(p.latent + lat_index(p, op, b, pos0 + r) + e);
+    }
+    consumer_sync();
+    mla_block<J>(stage, R, ldl, kl, lane, npair_w, prow, 0, q, qr, m, l, o);
+    consumer_sync();
+  }
+  // partial records as in GQA: [((b * ngroups + hg) * nchunk + c) * R + r][head in group][o, m, l]
+  const int stride = p.attn_part_stride;
+  const size_t base_rec = ((size_t)(b * ngr + hg) * op.nchunk + c) * R;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (j < npair_w) {
+      float* rec = p.attn_part + ((base_rec + rlo + j) * G + warp) * stride;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) __stcg(rec + lane * 16 + e, o[j][e]);
+      if (lane == 0) {
+        __stcg(rec + kl, m[j]);
+        __stcg(rec + kl + 1, l[j]);
+      }
+    }
+  }
+}
+
+// instruction (a = head h, b = 64-row block of v_head): out[n][h * v_head + j] = W_UV[h][j] . o_lat[n][h]
+__device__ void mla_uv_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int h = in.a, jb = in.b;
+  const int kl = op.kv_lora, vh = op.v_head;
+  const int per_warp = 64 / kConsumerWarps;
+  const int N = p.N;
+  for (int jj = 0; jj < per_warp; ++jj) {
+    const int j = jb * 64 + warp * per_warp + jj;
+    if (j >= vh) break;
+    const uint16_t* wrow = op.w_uv + ((size_t)h * vh + j) * kl + lane * 16;
+    const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(wrow));
+    const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(wrow + 8));
+    const uint32_t ws[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    for (int n = 0; n < N; ++n) {
+      const float* ol = op.in + (size_t)n * op.in_stride + (size_t)h * kl + lane * 16;
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        d = fmaf(bf_lo(ws[e]), __ldcg(ol + 2 * e), d);
+        d = fmaf(bf_hi(ws[e]), __ldcg(ol + 2 * e + 1), d);
+      }
+      d = warp_sum(d);
+      if (lane == 0) __stcg(op.out + (size_t)n * op.out_stride + (size_t)h * vh + j, d);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
 // Producer: the chunks of an SM's queue, in the order its consumers read them. A cursor walks them and the
 // producer loads each chunk into the ring. Optionally (MK_PREFETCH_AHEAD > 0) a second cursor runs that
 // many chunks further and asks L2 to fetch those bytes early (cp.async.bulk.prefetch.L2); measured on the
@@ -1203,10 +1730,31 @@ struct ChunkCursor {
   // GEMV walk: pass, row group, first input of the next slice; this lane's row pointer in the group
   int pass, grp, k0, nphys;
   const uint16_t* row;
-  // attention walk: next position, end, positions per chunk, bytes per position, this lane's base
-  int t, t1, P, pos_bytes;
+  // attention walk: next position, end, positions per chunk, bytes per position, this lane's base,
+  // number of copies per chunk (2: K and V of GQA; 1: the MLA latent)
+  int t, t1, P, pos_bytes, ncopy;
   const uint16_t* kv;
+  // MoE walk: selected expert slot, count, format, this lane's weight row (codes) and scale row
+  int j, nsel, fp4, up;
+  const uint8_t* mw;
+  const uint8_t* ms;
 };
+
+__device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& c, int lane) {
+  const int g0 = gemv_group_row(c.a, c.n, c.ng, c.grp);
+  const int nl = gemv_group_row(c.a, c.n, c.ng, c.grp + 1) - g0;
+  c.nphys = c.up ? 2 * nl : nl;
+  const int pr = c.fp4 ? (lane & 15) : lane;  // NVFP4: lanes 16..31 copy the scale rows
+  c.mw = nullptr;
+  c.ms = nullptr;
+  if (pr < c.nphys) {
+    const int m = (c.up && pr >= nl) ? 1 : 0;
+    const int r = g0 + (m ? pr - nl : pr);
+    const ExpertRow er = expert_row(p, *c.op, c.j, m, r, c.K);
+    c.mw = er.w;
+    c.ms = er.s;
+  }
+}
 
 __device__ __forceinline__ void cursor_group(ChunkCursor& c, int lane) {
   const int g0 = gemv_group_row(c.a, c.n, c.ng, c.grp);
@@ -1248,8 +1796,42 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         attn_range(p, op, b, in.b, c.t, c.t1);
         c.P = kChunkBytes / (4 * hd);
         c.pos_bytes = hd * 2;
+        c.ncopy = 2;
         c.kv = (lane == 0) ? p.kcache + kv_index(p, op, b, g, 0) : p.vcache + kv_index(p, op, b, g, 0);
         c.kind = 2;
+      } else if (type == OP_MLA_ATTN) {
+        const int b = in.a / op.n_kv_heads;
+        const int ldl = op.kv_lora + op.rope;
+        attn_range(p, op, b, in.b, c.t, c.t1);
+        c.P = kChunkBytes / (2 * ldl);
+        c.pos_bytes = ldl * 2;
+        c.ncopy = 1;
+        c.kv = p.latent + lat_index(p, op, b, 0);
+        c.kind = 2;
+      } else if (type == OP_MOE_UP || type == OP_MOE_DOWN) {
+        // the expert list is known once the router op has finished
+        int ok = 1;
+        if (lane == 0)
+          ok = wait_counter(&p.counters[op.route_op], (uint32_t)p.ops[op.route_op].n_instr, p) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        c.up = type == OP_MOE_UP;
+        c.fp4 = op.fp4;
+        c.glog = c.up ? op.rg / 2 : op.rg;
+        c.a = in.a;
+        c.n = in.b - in.a;
+        c.ng = gemv_ngroups(c.n, c.glog);
+        c.K = c.up ? p.d : op.F;
+        c.kc = op.kc;
+        c.passes = op.passes;
+        c.nsel = op.n_shared + __ldcg(p.union_list);
+        c.j = c.pass = c.grp = c.k0 = 0;
+        if (c.ng == 0 || c.nsel == 0) {
+          ++c.qi;
+          continue;
+        }
+        cursor_moe_group(p, c, lane);
+        c.kind = 4;
       } else {
         ++c.qi;
         continue;
@@ -1280,7 +1862,50 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       }
       return true;
     }
-    // attention: K then V of up to P positions
+    if (c.kind == 4) {
+      const int kw = min(c.kc, c.K - c.k0);
+      bytes = 0;
+      if (c.fp4) {
+        const int pitch = kw / 2 + kw / 16;  // row layout in the slot: codes, then block scales
+        total = (uint32_t)(c.nphys * pitch);
+        if (c.mw) {
+          if (lane < 16) {
+            src = c.mw + c.k0 / 2;
+            bytes = (uint32_t)(kw / 2);
+            dst = (uint32_t)(lane * pitch);
+          } else {
+            src = c.ms + c.k0 / 16;
+            bytes = (uint32_t)(kw / 16);
+            dst = (uint32_t)((lane - 16) * pitch + kw / 2);
+          }
+        }
+      } else {
+        total = (uint32_t)(c.nphys * kw * 2);
+        if (c.mw) {
+          src = c.mw + (size_t)c.k0 * 2;
+          bytes = (uint32_t)(kw * 2);
+          dst = (uint32_t)(lane * kw * 2);
+        }
+      }
+      c.k0 += c.kc;
+      if (c.k0 >= c.K) {
+        c.k0 = 0;
+        if (++c.grp >= c.ng) {
+          c.grp = 0;
+          if (++c.pass >= c.passes) {
+            c.pass = 0;
+            if (++c.j >= c.nsel) {
+              c.kind = 0;
+              ++c.qi;
+              return true;
+            }
+          }
+        }
+        cursor_moe_group(p, c, lane);
+      }
+      return true;
+    }
+    // attention: K then V (GQA) or the latent (MLA) of up to P positions
     if (c.t >= c.t1) {
       c.kind = 0;
       ++c.qi;
@@ -1288,8 +1913,8 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
     }
     const int np = min(c.P, c.t1 - c.t);
     const uint32_t nb = (uint32_t)(np * c.pos_bytes);
-    total = 2 * nb;
-    bytes = (lane < 2) ? nb : 0;
+    total = c.ncopy * nb;
+    bytes = (lane < c.ncopy) ? nb : 0;
     src = reinterpret_cast<const uint8_t*>(c.kv) + (size_t)c.t * c.pos_bytes;
     dst = (lane == 1) ? kChunkBytes / 2 : 0;
     c.t += c.P;
@@ -1439,10 +2064,33 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
         break;
       }
       case OP_ATTN_COMBINE:
-        if (op.head_dim == 256) attn_combine_consume<8>(p, op, in, actf, ctid);
+        if (op.head_dim == 512) attn_combine_consume<16>(p, op, in, actf, ctid);
+        else if (op.head_dim == 256) attn_combine_consume<8>(p, op, in, actf, ctid);
         else if (op.head_dim == 128) attn_combine_consume<4>(p, op, in, actf, ctid);
         else attn_combine_consume<2>(p, op, in, actf, ctid);
         break;
+      case OP_ROUTE: route_consume(p, op, actf, ctid); break;
+      case OP_MOE_UP:
+      case OP_MOE_DOWN:
+        if (op.fp4) {
+          if (nr == 1) moe_consume<16, 1, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 2) moe_consume<16, 2, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 4) moe_consume<16, 4, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else moe_consume<8, 8, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+        } else {
+          if (nr == 1) moe_consume<16, 1, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 2) moe_consume<16, 2, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 4) moe_consume<16, 4, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else moe_consume<8, 8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
+        }
+        break;
+      case OP_MLA_PREP: mla_prep_consume(p, op, ctid); break;
+      case OP_MLA_QABS: mla_qabs_consume(p, op, in, ctid); break;
+      case OP_MLA_ATTN:
+        if (((in.c >> 8) - (in.c & 0xff)) <= 1) mla_attn_consume<1>(p, op, in, rg, chunk, act, ctid);
+        else mla_attn_consume<2>(p, op, in, rg, chunk, act, ctid);
+        break;
+      case OP_MLA_UV: mla_uv_consume(p, op, in, ctid); break;
       case OP_DELTA:
         if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
         else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
@@ -1498,6 +2146,8 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     if (s_state == 0 && blockIdx.x == 0 && tid == 0) atomicCAS(p.status, 0, kStatusDevice);
     return;
   }
+  if (tid < 16) cs.e2m1[tid] = e2m1_value(tid);
+  __syncthreads();
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
   if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1);
   else run_consumer(p, rg, cs, act, q0, q1, tid);

@@ -222,7 +222,8 @@ void mk_destroy(mk_handle* h);
  * mk_get_status would). Errors: MK_ERR_INVALID_ARG (as mk_create / mk_decode_step, or a missing
  * persistent buffer), MK_ERR_UNSUPPORTED when the step needs more working memory than
  * MK_STATIC_SCRATCH_BYTES (a message on stderr gives both sizes), MK_ERR_CUDA, MK_ERR_DEVICE,
- * MK_ERR_TIMEOUT. No MoE or MLA model is accepted (as mk_create). */
+ * MK_ERR_TIMEOUT. MLA and MoE models are refused with MK_ERR_UNSUPPORTED: their latent cache and routing
+ * buffers are not among the persistent buffers below. */
 #define MK_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 typedef struct mk_state_buffers {

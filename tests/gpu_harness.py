@@ -22,11 +22,32 @@ class Report:
         self.steps = 0
         self.token_mismatch = 0
         self.near_ties = 0
+        self.route_ties = 0
+        self.prefill_tie = False
+        self.compared = 0
         self.errors = []
+
+
+ROUTE_TIE = 1e-4   # router scores closer than this at the top-k boundary may be picked either way in fp32
+
+
+def routing_near_tie(orc) -> bool:
+    """True when, in the oracle's last call, some row's k-th and (k+1)-th biased router scores of some MoE
+    layer lie within ROUTE_TIE: the fp32 kernel may then pick the other expert, which changes that row's
+    output by far more than the logit tolerance, so such a step is not compared."""
+    k = getattr(orc.cfg, "top_k", 0)
+    for idx, biased in orc.routing.values():
+        if biased.shape[-1] <= k:
+            continue
+        s = -np.sort(-biased, axis=-1)
+        if np.any(s[..., k - 1] - s[..., k] < ROUTE_TIE):
+            return True
+    return False
 
 
 def compare_logits(gpu: np.ndarray, ref: np.ndarray, tol: float, rep: Report, what: str):
     err = float(np.max(np.abs(gpu.astype(np.float64) - ref)))
+    rep.compared += 1
     rep.max_err = max(rep.max_err, err)
     if not np.isfinite(err) or err > tol:
         rep.errors.append(f"{what}: max |diff| {err:.4g} > {tol}")
@@ -61,6 +82,10 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
     ctx = make_tokens(seed, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
     mk.prefill(ctx)
     orc.prefill(ctx.cpu().numpy())
+    if routing_near_tie(orc):
+        # the context itself hit a routing near-tie: the two caches may legitimately differ from here on
+        rep.route_ties += 1
+        rep.prefill_tie = True
     pos = np.full(B, T, dtype=np.int64)
     tok = make_tokens(seed, "start", (B, 1), cfg.vocab).numpy().astype(np.int64)
     V = cfg.vocab
@@ -73,7 +98,10 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy()
-        compare_logits(g, ref, tol, rep, f"decode step {s}")
+        if rep.prefill_tie or routing_near_tie(orc):
+            rep.route_ties += 1
+        else:
+            compare_logits(g, ref, tol, rep, f"decode step {s}")
         if check_argmax:
             # the kernel's own argmax must be the argmax of the logits it wrote
             assert np.array_equal(am.cpu().numpy(), g.argmax(-1)), "in-kernel argmax differs from logits argmax"
@@ -91,7 +119,10 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy().reshape(B, R_verify, V)
-        compare_logits(g, ref, tol, rep, f"verify block {vi}")
+        if rep.prefill_tie or routing_near_tie(orc):
+            rep.route_ties += 1
+        else:
+            compare_logits(g, ref, tol, rep, f"verify block {vi}")
         if check_argmax:
             assert np.array_equal(am.cpu().numpy().reshape(B, R_verify), g.argmax(-1))
         # accept `acc` rows: the next anchor is the oracle's greedy token after the last accepted row
@@ -105,6 +136,9 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
                 logits, None)
         ref = orc.step(tok, pos)[:, 0]
         assert mk.status() == 0
-        compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
+        if rep.prefill_tie or routing_near_tie(orc):
+            rep.route_ties += 1
+        else:
+            compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
     mk.close()
     return rep

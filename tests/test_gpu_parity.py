@@ -107,3 +107,63 @@ def test_host_entry_point_matches_device_entry_point():
     np.testing.assert_array_equal(la.cpu().numpy(), lb)
     a.close()
     b.close()
+
+
+TOL_NVFP4 = 5e-2
+
+
+def _check_moe(rep):
+    _check(rep)
+    assert rep.compared >= 2, f"only {rep.compared} steps compared ({rep.route_ties} routing near-ties)"
+
+
+def test_kda_decode_and_verify():
+    """KDA (per-channel decay) recurrent layers at full width (64 heads x 128 / 128, d 7168) with a dense
+    FFN: batch 2, ragged context, decode and verify blocks (pending-row replay of the delta rule)."""
+    import dataclasses
+    from gpu_harness import run_case
+    cfg = dataclasses.replace(config("moe_kda_mla"), n_layers=2, mixers=("kda", "kda"), ffn="dense",
+                              ffn_dim=2048, vocab=32768)
+    rep = run_case(cfg, B=2, T=29, decode_steps=2, verify_accepts=(3, 6), tol=TOL_BF16)
+    _check(rep)
+
+
+def test_kda_mla_moe_full_width_two_layers():
+    """One KDA and one MLA layer at the full widths of the MoE / KDA / MLA model (d 7168; MLA 64 heads,
+    latent 512 + rope 64, q_lora 1536; experts d x 2048 bf16, 1 shared), with 16 routed experts top-4 so
+    the oracle stays small; batch 2: prefill (16 rows per call: two expert passes), decode, verify."""
+    import dataclasses
+    from gpu_harness import run_case
+    cfg = dataclasses.replace(config("moe_kda_mla"), n_layers=2, mixers=("kda", "mla"), n_experts=16, top_k=4,
+                              vocab=32768)
+    rep = run_case(cfg, B=2, T=37, decode_steps=2, verify_accepts=(3, 6), tol=TOL_BF16)
+    _check_moe(rep)
+
+
+def test_mla_moe_batch8_decode():
+    """MLA + MoE at batch 8 (8-row expert GEMV groups, one head group per warp, many context chunks)."""
+    import dataclasses
+    from gpu_harness import run_case
+    cfg = dataclasses.replace(config("moe_kda_mla"), n_layers=1, mixers=("mla",), d_model=2048, n_experts=64,
+                              top_k=8, expert_dim=512, vocab=8192)
+    rep = run_case(cfg, B=8, T=45, decode_steps=2, tol=TOL_BF16)
+    _check_moe(rep)
+
+
+def test_nvfp4_moe_256_experts():
+    """NVFP4 experts (e2m1 codes, e4m3 block scales, fp32 tensor scales), 256 experts top-8 + 1 shared,
+    router bias, with GQA 8/2 x 128; narrow (d 512, experts 512) so the dequantised oracle stays small."""
+    from gpu_harness import run_case
+    cfg = config("moe_nvfp4_gqa", n_layers=2, d_model=512, expert_dim=512, vocab=8192, n_q_heads=8,
+                 n_kv_heads=2, head_dim=128)
+    rep = run_case(cfg, B=2, T=33, decode_steps=2, verify_accepts=(3, 6), tol=TOL_NVFP4)
+    _check_moe(rep)
+
+
+def test_nvfp4_moe_full_width_one_layer():
+    """One layer of the NVFP4 MoE model at full width (d 6144, GQA 48/8 x 128, experts 6144 x 2048), 32
+    experts top-8, batch 1 decode."""
+    from gpu_harness import run_case
+    cfg = config("moe_nvfp4_gqa", n_layers=1, n_experts=32, vocab=16384)
+    rep = run_case(cfg, B=1, T=12, decode_steps=3, tol=TOL_NVFP4)
+    _check_moe(rep)
