@@ -83,6 +83,7 @@ struct mk_handle {
   int32_t* union_list = nullptr;
   float* hexp = nullptr;
   size_t hexp_floats = 0;
+  int32_t* route_log = nullptr;  // caller's device buffer (mk_set_routing_log) or NULL
   uint32_t* counters = nullptr;
   uint32_t* arrive = nullptr;
   int32_t* status = nullptr;
@@ -880,6 +881,7 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.route_w = h->route_w;
   p.union_list = h->union_list;
   p.hexp = h->hexp;
+  p.route_log = h->route_log;
   p.seq = h->seq;
   p.rope = h->rope;
   p.rot_dim = h->rot_dim;
@@ -1105,6 +1107,15 @@ mk_status mk_get_status(mk_handle* h, void* stream) {
     h->err = code == MK_ERR_TIMEOUT ? "device watchdog timeout" : "device input check failed (token or position)";
     return (mk_status)code;
   }
+  return MK_OK;
+}
+
+mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (device_log && h->desc.ffn_kind != MK_FFN_MOE) return fail(h, MK_ERR_INVALID_ARG, "the model has no MoE layers");
+  if (device_log && (reinterpret_cast<uintptr_t>(device_log) & 3u))
+    return fail(h, MK_ERR_INVALID_ARG, "routing log must be 4-byte aligned");
+  h->route_log = device_log;
   return MK_OK;
 }
 

@@ -171,6 +171,7 @@ struct KParams {
   float* route_w;
   int32_t* union_list;
   float* hexp;              // [n_shared + union][N][F] expert SwiGLU outputs
+  int32_t* route_log;       // optional [n_layers][max_batch][max_ctx][top_k] expert ids by position
   SeqState* seq;
   const float2* rope;       // [max_ctx][rot_dim / 2] (cos, sin)
   int32_t rot_dim;

@@ -1235,6 +1235,10 @@ __device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, 
       if (lane == 0) {
         __stcg(p.route_idx + n * kMaxTopK + k, bi);
         flags[bi] = 1;
+        if (p.route_log) {
+          const int b = n / p.R, pos = p.positions[b] + n % p.R;
+          p.route_log[(((size_t)op.layer * p.max_batch + b) * p.max_ctx + pos) * K + k] = bi;
+        }
       }
     }
     if (lane == 0)

@@ -183,6 +183,15 @@ mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const in
  * of the interrupted step is undefined: run mk_prefill_kv again). */
 mk_status mk_get_status(mk_handle* h, void* stream);
 
+/* Routing log of MoE models (for checking and analysis; the decode path does not need it). With a
+ * non-NULL `device_log` — device int32 [n_layers][max_batch][max_ctx][top_k], owned by the caller and kept
+ * alive while set — every later step and prefill writes, for each MoE layer l and each row r of sequence b
+ * at position t = positions[b] + r, the ids of the experts that row selected, in pick order, to
+ * device_log[((l * max_batch + b) * max_ctx + t) * top_k + k]. Entries of dense layers and of positions
+ * no call has reached are left as they were. NULL turns the log off (the default). Takes effect at the
+ * next launch. Errors: MK_ERR_INVALID_ARG (no MoE layer in the model, misaligned pointer). */
+mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log);
+
 /* Human-readable description of the last error on this handle ("" if none). Owned by the handle. */
 const char* mk_last_error(const mk_handle* h);
 

@@ -23,26 +23,41 @@ class Report:
         self.token_mismatch = 0
         self.near_ties = 0
         self.route_ties = 0
-        self.prefill_tie = False
+        self.routed_rows = 0
+        self.diverged = False
         self.compared = 0
         self.errors = []
 
 
-ROUTE_TIE = 1e-4   # router scores closer than this at the top-k boundary may be picked either way in fp32
+ROUTE_TIE = 1e-4   # router scores this close at the top-k boundary may be picked either way in fp32
 
 
-def routing_near_tie(orc) -> bool:
-    """True when, in the oracle's last call, some row's k-th and (k+1)-th biased router scores of some MoE
-    layer lie within ROUTE_TIE: the fp32 kernel may then pick the other expert, which changes that row's
-    output by far more than the logit tolerance, so such a step is not compared."""
-    k = getattr(orc.cfg, "top_k", 0)
-    for idx, biased in orc.routing.values():
-        if biased.shape[-1] <= k:
-            continue
-        s = -np.sort(-biased, axis=-1)
-        if np.any(s[..., k - 1] - s[..., k] < ROUTE_TIE):
-            return True
-    return False
+def check_routing(orc, log, pos0, R: int, rep, what: str):
+    """Compares the experts the kernel selected (its routing log, by position) with the oracle's last call,
+    as sets per (layer, sequence, row). A difference is accepted only where the oracle's k-th and (k+1)-th
+    biased scores lie within ROUTE_TIE (a near-tie that fp32 may break the other way); from then on the
+    two runs hold different states, so later logits are not compared (rep.diverged)."""
+    if log is None or rep.diverged:
+        return
+    k = orc.cfg.top_k
+    lg = log.cpu().numpy()
+    for layer, (idx, biased) in orc.routing.items():
+        B = idx.shape[0]
+        for b in range(B):
+            for r in range(R):
+                got = np.sort(lg[layer, b, int(pos0[b]) + r])
+                want = np.sort(idx[b, r])
+                rep.routed_rows += 1
+                if np.array_equal(got, want):
+                    continue
+                s = -np.sort(-biased[b, r])
+                gap = s[k - 1] - s[k] if s.shape[0] > k else np.inf
+                if gap < ROUTE_TIE:
+                    rep.route_ties += 1
+                    rep.diverged = True
+                else:
+                    rep.errors.append(f"{what}: layer {layer} seq {b} row {r}: experts {got.tolist()} vs oracle "
+                                      f"{want.tolist()} (boundary gap {gap:.3g})")
 
 
 def compare_logits(gpu: np.ndarray, ref: np.ndarray, tol: float, rep: Report, what: str):
@@ -80,12 +95,13 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
     orc = Oracle(cfg, w, B, max_ctx)
     rep = Report()
     ctx = make_tokens(seed, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
+    log = None
+    if cfg.ffn == "moe":
+        log = torch.full((cfg.n_layers, B, max_ctx, cfg.top_k), -1, dtype=torch.int32, device=dev)
+        mk.set_routing_log(log)
     mk.prefill(ctx)
     orc.prefill(ctx.cpu().numpy())
-    if routing_near_tie(orc):
-        # the context itself hit a routing near-tie: the two caches may legitimately differ from here on
-        rep.route_ties += 1
-        rep.prefill_tie = True
+    check_routing(orc, log, np.zeros(B, dtype=np.int64), T, rep, "prefill")
     pos = np.full(B, T, dtype=np.int64)
     tok = make_tokens(seed, "start", (B, 1), cfg.vocab).numpy().astype(np.int64)
     V = cfg.vocab
@@ -98,9 +114,8 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy()
-        if rep.prefill_tie or routing_near_tie(orc):
-            rep.route_ties += 1
-        else:
+        check_routing(orc, log, pos, 1, rep, f"decode step {s}")
+        if not rep.diverged:
             compare_logits(g, ref, tol, rep, f"decode step {s}")
         if check_argmax:
             # the kernel's own argmax must be the argmax of the logits it wrote
@@ -119,9 +134,8 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy().reshape(B, R_verify, V)
-        if rep.prefill_tie or routing_near_tie(orc):
-            rep.route_ties += 1
-        else:
+        check_routing(orc, log, pos, R_verify, rep, f"verify block {vi}")
+        if not rep.diverged:
             compare_logits(g, ref, tol, rep, f"verify block {vi}")
         if check_argmax:
             assert np.array_equal(am.cpu().numpy().reshape(B, R_verify), g.argmax(-1))
@@ -136,9 +150,8 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
                 logits, None)
         ref = orc.step(tok, pos)[:, 0]
         assert mk.status() == 0
-        if rep.prefill_tie or routing_near_tie(orc):
-            rep.route_ties += 1
-        else:
+        check_routing(orc, log, pos, 1, rep, "decode after verify")
+        if not rep.diverged:
             compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
     mk.close()
     return rep

@@ -114,6 +114,7 @@ TOL_NVFP4 = 5e-2
 
 def _check_moe(rep):
     _check(rep)
+    assert rep.routed_rows > 0
     assert rep.compared >= 2, f"only {rep.compared} steps compared ({rep.route_ties} routing near-ties)"
 
 
