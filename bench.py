@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--sweep", default="2,4,8", help="extra batch sizes timed after the headline ('' = none)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (diagnostic runs only)")
+    ap.add_argument("--context", type=int, default=0, help="override the context length (diagnostic runs only)")
     ap.add_argument("--accept", type=int, default=6, help="accepted length per verify step (verify workloads)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -166,7 +167,8 @@ def oracle_sample(cfg, weights_cpu_fn, batch: int, rows: int, n_steps: int = 2):
     after a 16-token prefill, and scale the per-layer time to the full depth. Returns (tok/s, seconds per
     step estimate, description)."""
     from oracle import Oracle, ops
-    k = 4 if cfg.n_layers >= 4 else cfg.n_layers
+    # MoE layers hold tens of GB of experts: one layer is enough of a sample there
+    k = 1 if cfg.ffn == "moe" else (4 if cfg.n_layers >= 4 else cfg.n_layers)
     sub = cfg.with_layers(k)
     w = weights_cpu_fn(sub)
     orc = Oracle(sub, w, batch, 64)
@@ -235,8 +237,9 @@ def workload_config(wl, cfg, B, args):
         "moe_nvfp4_gqa": "GQA MoE 256e top-8, NVFP4 experts, d_model 6144",
     }[cfg.name]
     mode = f"{wl.rows}-row verify, accepted length {args.accept}" if wl.rows > 1 else "greedy decode"
-    return {"workload": f"{desc}, {cfg.n_layers} layers, {mode}, batch {B}, {wl.context}-token context",
-            "batch": B, "rows": wl.rows, "context": wl.context, "layers": cfg.n_layers,
+    T = args.context or wl.context
+    return {"workload": f"{desc}, {cfg.n_layers} layers, {mode}, batch {B}, {T}-token context",
+            "batch": B, "rows": wl.rows, "context": T, "layers": cfg.n_layers,
             "l2": "inputs larger than L2 (every step streams the whole weight set, far above 129 MB)"}
 
 
@@ -256,7 +259,7 @@ def run_mk(args, wl, cfg):
     w = make_weights(cfg, seed=0, device=dev)
     R = wl.rows
     adv = args.accept if R > 1 else 1
-    T = wl.context
+    T = args.context or wl.context
     W, K = args.warmup, args.steps
     hbm, peak_kind = peaks()
     uuid = None
@@ -266,7 +269,7 @@ def run_mk(args, wl, cfg):
         pass
 
     def measure(B, K_, with_e2e):
-        max_ctx = T + (W + K_ + 2) * adv * (2 if with_e2e else 1) + 2 * R + 16
+        max_ctx = T + (W + K_ + 2) * adv * (2 if with_e2e else 1) + 5 * adv + 2 * R + 16
         mk = Megakernel(cfg, w, max_batch=B, max_rows=8, max_ctx=max_ctx, device=local)
         ctx = make_tokens(rank, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
         mk.prefill(ctx, stream=sh)
@@ -317,20 +320,41 @@ def run_mk(args, wl, cfg):
             e2e = {"value": ws * B * adv / dt, "unit": "tokens/s",
                    "h2d_bytes_per_step": int(4 * (B * R + B)), "d2h_bytes_per_step": int(4 * B * R),
                    "ms_per_step": dt * 1e3}
+        expert_reads = None
+        if cfg.ffn == "moe":
+            # routed experts read per step: the union of the experts the step's rows selected, per layer,
+            # from the routing log of a few more steps of the same token stream (outside the timed region)
+            log = torch.full((cfg.n_layers, B, max_ctx, cfg.top_k), -1, dtype=torch.int32, device=dev)
+            mk.set_routing_log(log)
+            unions = []
+            base = T + steps * adv * (2 if with_e2e else 1)   # past every position used above
+            for s in range(4):
+                p_s = base + s * adv
+                mk.step(toks[(W + s) % (steps + 1)], torch.full((B,), p_s, dtype=torch.int32, device=dev), logits, None, stream=sh)
+                if mk.status(sh) != 0:
+                    raise RuntimeError("device status in the routing-log steps")
+                lg = log.cpu().numpy()
+                u = 0
+                for layer in range(cfg.n_layers):
+                    rows = [lg[layer, b, p_s + r] for b in range(B) for r in range(R)]
+                    u += len(np.unique(np.concatenate(rows)))
+                unions.append(u)
+            mk.set_routing_log(None)
+            expert_reads = float(np.mean(unions))
         mk.close()
         del ctx, toks, pos, logits
-        return ms, clk.summary(), e2e
+        return ms, clk.summary(), e2e, expert_reads
 
     B = args.batch
-    ms, clocks, e2e = measure(B, K, not args.no_e2e)
-    acct = roofline.step_bytes(cfg, B, R, [T + W * adv + K * adv // 2] * B)
+    ms, clocks, e2e, ereads = measure(B, K, not args.no_e2e)
+    acct = roofline.step_bytes(cfg, B, R, [T + W * adv + K * adv // 2] * B, expert_reads=ereads)
     achieved = acct["total"] / (ms * 1e-3) / 1e9
     sweep = {}
     for sb in [int(x) for x in args.sweep.split(",") if x.strip()]:
         if sb == B or sb * R > 64:
             continue
-        sms, sclk, _ = measure(sb, max(5, K // 2), False)
-        sacct = roofline.step_bytes(cfg, sb, R, [T + W * adv + K * adv // 4] * sb)
+        sms, sclk, _, sereads = measure(sb, max(5, K // 2), False)
+        sacct = roofline.step_bytes(cfg, sb, R, [T + W * adv + K * adv // 4] * sb, expert_reads=sereads)
         sweep[str(sb)] = {"tokens_per_s": ws * sb * adv / (sms * 1e-3), "ms_per_step": sms,
                           "hbm_gbs": sacct["total"] / (sms * 1e-3) / 1e9,
                           "frac": sacct["total"] / (sms * 1e-3) / 1e9 / hbm}
@@ -350,7 +374,7 @@ def run_mk(args, wl, cfg):
     line = {
         "metric": METRIC, "value": ws * B * adv / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if cfg.expert_fmt == "bf16" else "bf16+nvfp4", "data": "synthetic",
         "config": workload_config(wl, cfg, B, args),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
