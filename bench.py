@@ -240,6 +240,7 @@ def workload_config(wl, cfg, B, args):
     T = args.context or wl.context
     return {"workload": f"{desc}, {cfg.n_layers} layers, {mode}, batch {B}, {T}-token context",
             "batch": B, "rows": wl.rows, "context": T, "layers": cfg.n_layers,
+            "prefill": f"one {T}-token random-token prefill, forked to all {B} sequences",
             "l2": "inputs larger than L2 (every step streams the whole weight set, far above 129 MB)"}
 
 
@@ -271,8 +272,12 @@ def run_mk(args, wl, cfg):
     def measure(B, K_, with_e2e):
         max_ctx = T + (W + K_ + 2) * adv * (2 if with_e2e else 1) + 5 * adv + 2 * R + 16
         mk = Megakernel(cfg, w, max_batch=B, max_rows=8, max_ctx=max_ctx, device=local)
-        ctx = make_tokens(rank, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
+        # one prefill of sequence 0, forked to the others (the decode steps then diverge: every row draws
+        # its own tokens); the caches and states of every sequence are separate copies in HBM
+        ctx = make_tokens(rank, "ctx", (1, T), cfg.vocab, device=dev).contiguous()
         mk.prefill(ctx, stream=sh)
+        for b in range(1, B):
+            mk.fork(0, b, stream=sh)
         torch.cuda.synchronize()
         steps = W + K_
         toks = torch.empty((steps + 1, B, R), dtype=torch.int32, device=dev)

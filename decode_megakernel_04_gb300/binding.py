@@ -59,7 +59,8 @@ class StateBuffers(C.Structure):
 
 
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
-           "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log"]
+           "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log",
+           "mk_fork_sequence"]
 
 _lib = None
 
@@ -88,10 +89,11 @@ def load(path: str | None = None) -> C.CDLL:
     lib.mk_destroy.argtypes = [_P]
     lib.mk_destroy.restype = None
     lib.mk_set_routing_log.argtypes = [_P, _P]
+    lib.mk_fork_sequence.argtypes = [_P, C.c_int, C.c_int, _P]
     lib.mk_decode_step_static.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.POINTER(StateBuffers),
                                           _P, _P, C.c_int, C.c_int, _P, _P, _P]
     for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
-              "mk_decode_step_static", "mk_set_routing_log"):
+              "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence"):
         getattr(lib, f).restype = C.c_int
     if path is None:
         _lib = lib
@@ -190,6 +192,10 @@ class Megakernel:
             self.h, tokens_np.ctypes.data, positions_np.ctypes.data, B, R,
             None if logits_np is None else logits_np.ctypes.data, argmax_np.ctypes.data, stream)
         self._check(rc)
+
+    def fork(self, src: int, dst: int, stream=None):
+        """Make sequence ``dst`` a copy of sequence ``src`` (caches, states, pending rows, counts)."""
+        self._check(self.lib.mk_fork_sequence(self.h, src, dst, stream))
 
     def set_routing_log(self, log=None):
         """Route the expert ids of every MoE row into ``log`` (device int32 [n_layers, max_batch, max_ctx,

@@ -16,9 +16,17 @@
 #include "mk_internal.h"
 
 namespace mk {
+// the two builds of the megakernel: without (dense) and with (full) the MLA and MoE ops
+namespace dense {
 size_t kernel_smem_bytes();
 cudaError_t kernel_configure();
 cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream);
+}  // namespace dense
+namespace full {
+size_t kernel_smem_bytes();
+cudaError_t kernel_configure();
+cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream);
+}  // namespace full
 cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream);
 cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t stream);
 }  // namespace mk
@@ -26,6 +34,12 @@ cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t str
 using namespace mk;
 
 namespace {
+
+size_t kernel_smem_bytes() { return std::max(dense::kernel_smem_bytes(), full::kernel_smem_bytes()); }
+cudaError_t kernel_configure(bool full_ops) { return full_ops ? full::kernel_configure() : dense::kernel_configure(); }
+cudaError_t kernel_launch(bool full_ops, const KParams& p, int n_sm, cudaStream_t stream) {
+  return full_ops ? full::kernel_launch(p, n_sm, stream) : dense::kernel_launch(p, n_sm, stream);
+}
 
 struct Program {
   int B = 0, R = 0;
@@ -54,6 +68,7 @@ struct mk_handle {
   // per-layer slot among layers of the same kind
   std::vector<int> slot;
   int n_gqa = 0, n_delta = 0, n_mla = 0;
+  bool full_ops = false;  // the model has MLA or MoE layers: launch the full build of the kernel
 
   int nmax = 0;
   int proj_stride = 0, attn_stride = 0, hbuf_stride = 0;
@@ -248,6 +263,7 @@ void derive_layout(mk_handle* h) {
     else h->slot[i] = h->n_delta++;
   }
   h->nmax = D.max_batch * D.max_rows;
+  h->full_ops = h->n_mla > 0 || D.ffn_kind == MK_FFN_MOE;
   int proj = 8, attn = 8;
   for (int i = 0; i < D.n_layers; ++i) {
     const int m = D.mixer[i];
@@ -896,7 +912,7 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
     h->last_prog = prog;
   }
   h->n_ops_last = prog->n_ops;
-  cudaError_t e = kernel_launch(p, h->n_sm, stream);
+  cudaError_t e = kernel_launch(h->full_ops, p, h->n_sm, stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
   return MK_OK;
 }
@@ -946,14 +962,14 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     delete h;
     return MK_ERR_UNSUPPORTED;
   }
-  if ((e = kernel_configure()) != cudaSuccess) {
+  derive_layout(h);
+  if ((e = kernel_configure(h->full_ops)) != cudaSuccess) {
     fprintf(stderr, "mk_create: %s\n", cudaGetErrorString(e));
     delete h;
     return MK_ERR_CUDA;
   }
 
   const mk_model_desc& D = h->desc;
-  derive_layout(h);
   const int Bm = D.max_batch, Rm = D.max_rows;
 
 #define ALLOC(ptr, count) \
@@ -1110,6 +1126,37 @@ mk_status mk_get_status(mk_handle* h, void* stream) {
   return MK_OK;
 }
 
+mk_status mk_fork_sequence(mk_handle* h, int src, int dst, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  const int Bm = D.max_batch;
+  if (src < 0 || src >= Bm || dst < 0 || dst >= Bm) return fail(h, MK_ERR_INVALID_ARG, "sequence %d -> %d", src, dst);
+  if (src == dst) return MK_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSetDevice(h->device);
+  auto copy = [&](void* base, size_t per_seq_bytes, size_t group) {
+    // sequence b's block of `per_seq_bytes` inside group `group` of max_batch such blocks
+    if (e != cudaSuccess) return;
+    char* g = static_cast<char*>(base) + group * Bm * per_seq_bytes;
+    e = cudaMemcpyAsync(g + dst * per_seq_bytes, g + src * per_seq_bytes, per_seq_bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  for (int sl = 0; sl < h->n_gqa; ++sl) {
+    const size_t per = sizeof(uint16_t) * D.n_kv_heads * D.max_ctx * D.head_dim;
+    copy(h->kcache, per, sl);
+    copy(h->vcache, per, sl);
+  }
+  for (int sl = 0; sl < h->n_mla; ++sl)
+    copy(h->latent, sizeof(uint16_t) * D.max_ctx * (D.kv_lora + D.qk_rope), sl);
+  for (int sl = 0; sl < h->n_delta; ++sl) {
+    copy(h->state, sizeof(float) * D.lin_heads * D.lin_dv * D.lin_dk, sl);
+    for (int par = 0; par < 2; ++par)
+      copy(h->pend, sizeof(float) * D.max_rows * D.lin_heads * h->pend_rec, 2 * sl + par);
+  }
+  copy(h->seq, sizeof(SeqState), 0);
+  if (e != cudaSuccess) return cuda_fail(h, e, "fork copy");
+  return MK_OK;
+}
+
 mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log) {
   if (!h) return MK_ERR_INVALID_ARG;
   if (device_log && h->desc.ffn_kind != MK_FFN_MOE) return fail(h, MK_ERR_INVALID_ARG, "the model has no MoE layers");
@@ -1240,8 +1287,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   cudaDeviceGetAttribute(&tmp.n_sm, cudaDevAttrMultiProcessorCount, tmp.device);
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, tmp.device);
   if (!coop || smem_optin < (int)kernel_smem_bytes()) return MK_ERR_UNSUPPORTED;
-  if (kernel_configure() != cudaSuccess) return MK_ERR_CUDA;
   derive_layout(&tmp);
+  if (kernel_configure(tmp.full_ops) != cudaSuccess) return MK_ERR_CUDA;
   if (!state->seq || (tmp.n_gqa && (!state->kcache || !state->vcache)) ||
       (tmp.n_delta && (!state->state || !state->pending))) {
     fprintf(stderr, "mk_decode_step_static: a persistent buffer this model needs is NULL\n");

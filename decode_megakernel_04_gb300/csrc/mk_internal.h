@@ -159,7 +159,7 @@ struct KParams {
   // GQA caches: [slot][max_batch][Hkv][max_ctx][hd] bf16
   uint16_t* kcache;
   uint16_t* vcache;
-  // delta rule: state [slot][max_batch][H][dv][dk] fp32; pending [2][slot][max_batch][max_rows][H][rec]
+  // delta rule: state [slot][max_batch][H][dv][dk] fp32; pending [slot][2][max_batch][max_rows][H][rec]
   float* state;
   float* pend;
   int32_t pend_rec;         // floats per pending record (k_hat, v, alpha, beta)

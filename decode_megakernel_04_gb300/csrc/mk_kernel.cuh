@@ -20,8 +20,17 @@
 
 #include "mk_internal.h"
 
-namespace mk {
+// This file is compiled twice (mk_kernel_dense.cu, mk_kernel_full.cu): MK_VARIANT_FULL = 0 leaves out the
+// MLA and MoE handlers, so models without them get a kernel whose register allocation those handlers do
+// not perturb; MK_VARIANT_NS names the namespace of each copy.
+#ifndef MK_VARIANT_FULL
+#error "define MK_VARIANT_FULL and MK_VARIANT_NS before including mk_kernel.cuh"
+#endif
 
+namespace mk {
+namespace MK_VARIANT_NS {
+
+constexpr bool kFull = MK_VARIANT_FULL != 0;
 constexpr int kStatusTimeout = 5;
 constexpr int kStatusDevice = 6;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -1803,7 +1812,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         c.ncopy = 2;
         c.kv = (lane == 0) ? p.kcache + kv_index(p, op, b, g, 0) : p.vcache + kv_index(p, op, b, g, 0);
         c.kind = 2;
-      } else if (type == OP_MLA_ATTN) {
+      } else if (kFull && type == OP_MLA_ATTN) {
         const int b = in.a / op.n_kv_heads;
         const int ldl = op.kv_lora + op.rope;
         attn_range(p, op, b, in.b, c.t, c.t1);
@@ -1812,7 +1821,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         c.ncopy = 1;
         c.kv = p.latent + lat_index(p, op, b, 0);
         c.kind = 2;
-      } else if (type == OP_MOE_UP || type == OP_MOE_DOWN) {
+      } else if (kFull && (type == OP_MOE_UP || type == OP_MOE_DOWN)) {
         // the expert list is known once the router op has finished
         int ok = 1;
         if (lane == 0)
@@ -1866,7 +1875,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       }
       return true;
     }
-    if (c.kind == 4) {
+    if (kFull && c.kind == 4) {
       const int kw = min(c.kc, c.K - c.k0);
       bytes = 0;
       if (c.fp4) {
@@ -2013,6 +2022,36 @@ __device__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& i
   gemv_consume<RG, NR, STAGED>(p, op, in, rg, chunk, cs, act, ctid);
 }
 
+// The MLA and MoE ops (full variant only).
+__device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+                                            uint32_t& chunk, CSmem& cs, uint16_t* act, float* actf, int nr, int ctid) {
+  switch (op.type) {
+      case OP_ROUTE: route_consume(p, op, actf, ctid); break;
+      case OP_MOE_UP:
+      case OP_MOE_DOWN:
+        if (op.fp4) {
+          if (nr == 1) moe_consume<16, 1, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 2) moe_consume<16, 2, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 4) moe_consume<16, 4, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          else moe_consume<8, 8, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+        } else {
+          if (nr == 1) moe_consume<16, 1, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 2) moe_consume<16, 2, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else if (nr == 4) moe_consume<16, 4, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          else moe_consume<8, 8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
+        }
+        break;
+      case OP_MLA_PREP: mla_prep_consume(p, op, ctid); break;
+      case OP_MLA_QABS: mla_qabs_consume(p, op, in, ctid); break;
+      case OP_MLA_ATTN:
+        if (((in.c >> 8) - (in.c & 0xff)) <= 1) mla_attn_consume<1>(p, op, in, rg, chunk, act, ctid);
+        else mla_attn_consume<2>(p, op, in, rg, chunk, act, ctid);
+        break;
+      case OP_MLA_UV: mla_uv_consume(p, op, in, ctid); break;
+    default: break;
+  }
+}
+
 __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16_t* act, int q0, int q1, int ctid) {
   uint32_t chunk = 0;
   float* actf = reinterpret_cast<float*>(act);
@@ -2068,33 +2107,20 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
         break;
       }
       case OP_ATTN_COMBINE:
-        if (op.head_dim == 512) attn_combine_consume<16>(p, op, in, actf, ctid);
+        if (kFull && op.head_dim == 512) attn_combine_consume<16>(p, op, in, actf, ctid);
         else if (op.head_dim == 256) attn_combine_consume<8>(p, op, in, actf, ctid);
         else if (op.head_dim == 128) attn_combine_consume<4>(p, op, in, actf, ctid);
         else attn_combine_consume<2>(p, op, in, actf, ctid);
         break;
-      case OP_ROUTE: route_consume(p, op, actf, ctid); break;
+      case OP_ROUTE:
       case OP_MOE_UP:
       case OP_MOE_DOWN:
-        if (op.fp4) {
-          if (nr == 1) moe_consume<16, 1, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 2) moe_consume<16, 2, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 4) moe_consume<16, 4, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else moe_consume<8, 8, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-        } else {
-          if (nr == 1) moe_consume<16, 1, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 2) moe_consume<16, 2, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 4) moe_consume<16, 4, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else moe_consume<8, 8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
-        }
-        break;
-      case OP_MLA_PREP: mla_prep_consume(p, op, ctid); break;
-      case OP_MLA_QABS: mla_qabs_consume(p, op, in, ctid); break;
+      case OP_MLA_PREP:
+      case OP_MLA_QABS:
       case OP_MLA_ATTN:
-        if (((in.c >> 8) - (in.c & 0xff)) <= 1) mla_attn_consume<1>(p, op, in, rg, chunk, act, ctid);
-        else mla_attn_consume<2>(p, op, in, rg, chunk, act, ctid);
+      case OP_MLA_UV:
+        if constexpr (kFull) run_full_op(p, op, in, rg, chunk, cs, act, actf, nr, ctid);
         break;
-      case OP_MLA_UV: mla_uv_consume(p, op, in, ctid); break;
       case OP_DELTA:
         if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
         else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
@@ -2150,13 +2176,18 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     if (s_state == 0 && blockIdx.x == 0 && tid == 0) atomicCAS(p.status, 0, kStatusDevice);
     return;
   }
-  if (tid < 16) cs.e2m1[tid] = e2m1_value(tid);
-  __syncthreads();
+  if (kFull) {
+    if (tid < 16) cs.e2m1[tid] = e2m1_value(tid);
+    __syncthreads();
+  }
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
   if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1);
   else run_consumer(p, rg, cs, act, q0, q1, tid);
 }
 
+}  // namespace MK_VARIANT_NS
+
+#if !MK_VARIANT_FULL
 // ------------------------------------------------------------------------------------------------
 // helper kernels (set-up, not on the decode path)
 // ------------------------------------------------------------------------------------------------
@@ -2175,11 +2206,13 @@ __global__ void fill_i32_kernel(int32_t* dst, int n, int32_t value) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = value;
 }
+#endif
 
 }  // namespace mk
 
 // ---- host-side launch wrappers (used by mk_host.cu) ---------------------------------------------
 namespace mk {
+namespace MK_VARIANT_NS {
 
 size_t kernel_smem_bytes() { return kSmemBytes; }
 
@@ -2193,6 +2226,9 @@ cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream) {
                                      kSmemBytes, stream);
 }
 
+}  // namespace MK_VARIANT_NS
+
+#if !MK_VARIANT_FULL
 cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream) {
   const int n = max_ctx * (rot_dim / 2);
   rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(tab, max_ctx, rot_dim, theta);
@@ -2203,5 +2239,6 @@ cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t str
   fill_i32_kernel<<<(n + 255) / 256, 256, 0, stream>>>(dst, n, value);
   return cudaGetLastError();
 }
+#endif
 
 }  // namespace mk

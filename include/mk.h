@@ -183,6 +183,14 @@ mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const in
  * of the interrupted step is undefined: run mk_prefill_kv again). */
 mk_status mk_get_status(mk_handle* h, void* stream);
 
+/* Makes sequence `dst` a copy of sequence `src` (both in 0..max_batch-1): its KV / latent caches,
+ * recurrent states, pending verify rows and committed / pending counts, so that dst continues exactly as
+ * src would. For parallel sampling or beam search from one shared prefix (one prefill, then forks), and
+ * for setting up a batch of long contexts quickly. Device-to-device copies of whole per-sequence blocks,
+ * asynchronous on `stream`; must not overlap a step that uses either sequence. src == dst does nothing.
+ * The pages have no counterpart for this call. Errors: MK_ERR_INVALID_ARG, MK_ERR_CUDA. */
+mk_status mk_fork_sequence(mk_handle* h, int src, int dst, void* stream);
+
 /* Routing log of MoE models (for checking and analysis; the decode path does not need it). With a
  * non-NULL `device_log` — device int32 [n_layers][max_batch][max_ctx][top_k], owned by the caller and kept
  * alive while set — every later step and prefill writes, for each MoE layer l and each row r of sequence b

@@ -168,3 +168,35 @@ def test_nvfp4_moe_full_width_one_layer():
     cfg = config("moe_nvfp4_gqa", n_layers=1, n_experts=32, vocab=16384)
     rep = run_case(cfg, B=1, T=12, decode_steps=3, tol=TOL_NVFP4)
     _check_moe(rep)
+
+
+def test_fork_sequence():
+    """One prefill of sequence 0 forked to sequences 1 and 2 equals three separate prefills of the same
+    context: decode and verify steps with different tokens per sequence match the oracle (GQA + GDN)."""
+    from decode_megakernel_04_gb300 import Megakernel
+    from gpu_harness import Report, compare_logits
+    from oracle import Oracle
+    cfg = config("hybrid_gdn_gqa", n_layers=4, vocab=8192)
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=1, device=dev)
+    B, T, R = 3, 21, 8
+    mk = Megakernel(cfg, w, max_batch=B, max_rows=R, max_ctx=64)
+    orc = Oracle(cfg, w, B, 64)
+    ctx = make_tokens(1, "ctx", (1, T), cfg.vocab, device=dev).contiguous()
+    mk.prefill(ctx)
+    mk.fork(0, 1)
+    mk.fork(0, 2)
+    orc.prefill(np.repeat(ctx.cpu().numpy(), B, axis=0))
+    rep = Report()
+    pos = np.full(B, T, dtype=np.int64)
+    for s, rows in enumerate((1, R, 1)):
+        tok = make_tokens(1, f"fork{s}", (B, rows), cfg.vocab).numpy().astype(np.int64)
+        logits = torch.empty((B * rows, cfg.vocab), device=dev)
+        mk.step(torch.from_numpy(tok.astype(np.int32)).to(dev).contiguous(),
+                torch.from_numpy(pos.astype(np.int32)).to(dev), logits)
+        assert mk.status() == 0
+        ref = orc.step(tok, pos)
+        compare_logits(logits.cpu().numpy().reshape(B, rows, -1), ref, TOL_BF16, rep, f"step {s}")
+        pos = pos + (rows if rows == 1 else 5)
+    mk.close()
+    _check(rep)
