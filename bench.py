@@ -35,7 +35,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per launch from one ncu capture, keyed by (workload, batch) and valid only for the kernel
 # sources they were taken with (the hash below); null once the sources change.
-KNOWN_TRAFFIC: dict = {}
+KNOWN_TRAFFIC: dict = {
+    # 4-layer full-width capture (profiles/megakernel_hybrid_gdn_gqa_4L_ctx512_b1_full.md) scaled to 64 layers
+    ("hybrid_gdn_gqa_decode", 1): (42.83e9, "b39980a8e12caa51"),
+}
 
 
 def sources_hash() -> str:
