@@ -591,6 +591,9 @@ void moe_layer(mk_handle* h, Builder& bld, int i, int N) {
   up.sgs[1] = L.s_up_gscale;
   up.gain = reinterpret_cast<const uint16_t*>(L.ffn_norm);
   up.ssq_in = 2 * i + 1;
+  // up to 2 rows: the normalised inputs are staged in shared memory once per instruction
+  const int64_t act_floats = kActBytes / 4;
+  up.staged = (N <= 2 && (int64_t)N * d <= act_floats) ? 1 : 0;
   const int op_up = bld.add(up);
   for (int s = 0; s < h->n_sm; ++s)
     bld.place(op_up, s, (int)((int64_t)F * s / h->n_sm), (int)((int64_t)F * (s + 1) / h->n_sm), 0);
@@ -604,6 +607,11 @@ void moe_layer(mk_handle* h, Builder& bld, int i, int N) {
   dn.egs[0] = L.e_down_gscale;
   dn.sgs[0] = L.s_down_gscale;
   dn.ssq_out = 2 * i + 2;
+  {  // routing of the rows, the SM's slice of x and two expert input buffers
+    const int64_t rt = (N * D.top_k + 3) & ~3;
+    const int64_t xr = ((int64_t)N * ((d + h->n_sm - 1) / h->n_sm) + 3) & ~3;
+    dn.staged = (N <= 2 && 2 * rt + xr + 2LL * N * F <= act_floats) ? 1 : 0;
+  }
   const int op_dn = bld.add(dn);
   for (int s = 0; s < h->n_sm; ++s)
     bld.place(op_dn, s, (int)((int64_t)d * s / h->n_sm), (int)((int64_t)d * (s + 1) / h->n_sm), 0);

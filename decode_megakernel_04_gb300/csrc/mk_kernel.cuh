@@ -555,6 +555,14 @@ __device__ __forceinline__ void load_f32_smem(const float* src, float (&dst)[CPL
   }
 }
 
+// 16-byte asynchronous global -> shared copy through L2 (cp.async.cg) and its group fences
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory"); }
+
 // STAGED: activations from shared memory (fp32, N*K*4 <= kActBytes); otherwise each chunk loads
 // its activation slice from global memory (L2).
 template <int RG, int NR, bool STAGED>
@@ -1254,11 +1262,15 @@ __device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, 
       for (int k = 0; k < K; ++k) __stcg(p.route_w + n * kMaxTopK + k, op.route_scale * ssel[k] / ssum);
   }
   consumer_sync();
-  if (ctid == 0) {
+  if (warp == 0) {  // compact the picked experts in ascending order, 32 at a time
     int cnt = 0;
-    for (int e = 0; e < E; ++e)
-      if (flags[e]) __stcg(p.union_list + 1 + cnt++, e);
-    __stcg(p.union_list, cnt);
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const bool f = e0 + lane < E && flags[e0 + lane] != 0;
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      if (f) __stcg(p.union_list + 1 + cnt + __popc(m & ((1u << lane) - 1u)), e0 + lane);
+      cnt += __popc(m);
+    }
+    if (lane == 0) __stcg(p.union_list, cnt);
   }
 }
 
@@ -1316,7 +1328,10 @@ __device__ __forceinline__ float expert_gscale(const KParams& p, const OpDesc& o
 // scales); inputs come from L2 per chunk. NVFP4 decodes as e2m1 * e4m3 (exact in fp32) and the fp32
 // tensor scale multiplies the dot product.
 // ------------------------------------------------------------------------------------------------
-template <int RG, int NR, int CPL, bool FP4>
+// STG (up to 2 activation rows): the inputs sit in shared memory instead of being read from L2 per chunk —
+// for MOE_UP the normalised x rows, staged once; for MOE_DOWN expert j's SwiGLU rows, copied with cp.async
+// into one of two buffers while expert j - 1 computes.
+template <int RG, int NR, int CPL, bool FP4, bool STG>
 __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
                             CSmem& cs, float* act, int ctid) {
   constexpr int KC = CPL * kConsumerThreads;
@@ -1331,15 +1346,32 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
   const int ng = gemv_ngroups(nrows, glog);
   const int passes = op.passes;
   // DOWN: each row's routing (expert ids, weights) and this SM's slice of x, in the staging area
+  const int rt = (N * op.top_k + 3) & ~3;
   int* ridx = reinterpret_cast<int*>(act);  // [N][top_k]
-  float* rw = act + N * op.top_k;           // [N][top_k]
-  float* xres = act + 2 * N * op.top_k;     // [N][nrows]
+  float* rw = act + rt;                     // [N][top_k]
+  float* xres = act + 2 * rt;               // [N][nrows]
+  // staged inputs: UP [N][K] at act; DOWN two [N][F] buffers after xres
+  float* hst = act + 2 * rt + ((N * nrows + 3) & ~3);
   if (up) {
     for (int n = warp; n < N; n += kConsumerWarps) {
       float s = 0.f;
       for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
       s = warp_sum(s);
       if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)p.d + p.eps);
+    }
+    if constexpr (STG) {
+      consumer_sync();
+      for (int i = ctid * 4; i < N * K; i += kConsumerThreads * 4) {
+        const int n = i / K, k = i % K;
+        float4 v = __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)n * p.d + k));
+        const uint2 g = __ldg(reinterpret_cast<const uint2*>(op.gain + k));
+        const float sc = cs.inv_rms[n];
+        v.x *= sc * bf_lo(g.x);
+        v.y *= sc * bf_hi(g.x);
+        v.z *= sc * bf_lo(g.y);
+        v.w *= sc * bf_hi(g.y);
+        *reinterpret_cast<float4*>(act + i) = v;
+      }
     }
   } else {
     for (int i = ctid; i < N * op.top_k; i += kConsumerThreads) {
@@ -1350,12 +1382,30 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
     for (int i = ctid; i < N * nrows; i += kConsumerThreads)
       xres[i] = __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows);
   }
+  auto stage_down = [&](int jn) {
+    const float* src = p.hexp + (size_t)jn * N * op.F;
+    float* dst = hst + (jn & 1) * N * op.F;
+    for (int i = ctid * 4; i < N * op.F; i += kConsumerThreads * 4) cp_async16(dst + i, src + i);
+    cp_async_commit();
+  };
+  if (STG && !up && ng > 0 && nsel > 0) stage_down(0);
   consumer_sync();
 
   for (int j = 0; j < nsel && ng > 0; ++j) {
     const float gs0 = expert_gscale(p, op, j, 0);
     const float gs1 = up ? expert_gscale(p, op, j, 1) : 1.f;
     const float* hin = p.hexp + (size_t)j * N * op.F;  // DOWN input
+    if (STG && !up) {
+      // expert j's rows were requested one expert ago; request j + 1's, wait for j's, publish
+      if (j + 1 < nsel) {
+        stage_down(j + 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      consumer_sync();
+      hin = hst + (j & 1) * N * op.F;
+    }
     const int ej = j < op.n_shared ? -1 : __ldcg(p.union_list + 1 + (j - op.n_shared));
     for (int pass = 0; pass < passes; ++pass) {
       const int nbase = pass * NR;
@@ -1373,12 +1423,14 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
           float a[NR][CPL];
           if (col < kw) {
             float gsc[CPL];
-            if (up) load_bf16_global<CPL>(op.gain + k0 + col, gsc);
+            if (!STG && up) load_bf16_global<CPL>(op.gain + k0 + col, gsc);
 #pragma unroll
             for (int n = 0; n < NR; ++n) {
               const int row = nbase + n;
               if (row < N) {
-                if (up) {
+                if (STG) {
+                  load_f32_smem<CPL>((up ? act : hin) + (size_t)row * K + k0 + col, a[n]);
+                } else if (up) {
                   load_f32<CPL>(p.x + (size_t)row * p.d + k0 + col, a[n]);
                   const float s = cs.inv_rms[row];
 #pragma unroll
@@ -1523,7 +1575,9 @@ __device__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
 }
 
 // instruction (a = head h, b = 128-column block of the latent): qt[n][h][c] for c in the block; block 0
-// also writes the rotated rope query qt[n][h][kv_lora ..]
+// also writes the rotated rope query qt[n][h][kv_lora ..]. Warp w owns 16 latent columns: their W_UK rows
+// (lane L holds inputs [L*E, L*E + E) of each) are loaded together up front, then each query row costs 16
+// dot products folded across the warp by one multi-value reduction.
 __device__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int h = in.a, cb = in.b;
@@ -1532,21 +1586,30 @@ __device__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr
   const float qs = rsqrtf((float)(nope + rp)) * kLog2e;
   const int ldq = op.in_stride, ldt = op.out_stride;
   const int N = p.N;
-  const int per_warp = 128 / kConsumerWarps;  // latent columns per warp
-  const int E = nope / 32;                     // nope inputs per lane (4 for nope = 128)
-  for (int cc = 0; cc < per_warp; ++cc) {
-    const int c = cb * 128 + warp * per_warp + cc;
-    if (c >= kl) break;
-    const uint16_t* wrow = op.w_uk + ((size_t)h * kl + c) * nope + lane * E;
-    float w[4];
-    for (int e = 0; e < E; ++e) w[e] = bf2f(wrow[e]);
-    for (int n = 0; n < N; ++n) {
-      const float* q = op.in + (size_t)n * ldq + (size_t)h * qw + lane * E;
+  const int E = nope / 32;  // nope inputs per lane (1 .. 4)
+  const int c0 = cb * 128 + warp * 16;
+  float w[16][4];
+#pragma unroll
+  for (int cc = 0; cc < 16; ++cc) {
+    const uint16_t* wrow = op.w_uk + ((size_t)h * kl + c0 + cc) * nope + lane * E;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[cc][e] = (e < E) ? bf2f(__ldg(wrow + e)) : 0.f;
+  }
+  for (int n = 0; n < N; ++n) {
+    const float* q = op.in + (size_t)n * ldq + (size_t)h * qw + lane * E;
+    float qv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qv[e] = (e < E) ? __ldcg(q + e) : 0.f;
+    float v[16];
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc) {
       float d = 0.f;
-      for (int e = 0; e < E; ++e) d = fmaf(w[e], __ldcg(q + e), d);
-      d = warp_sum(d);
-      if (lane == 0) __stcg(op.out + (size_t)n * ldt + (size_t)h * (kl + rp) + c, d * qs);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d = fmaf(w[cc][e], qv[e], d);
+      v[cc] = d;
     }
+    MultiReduce<16, 16>::run(v, lane);  // lane 2i: column i
+    if ((lane & 1) == 0) __stcg(op.out + (size_t)n * ldt + (size_t)h * (kl + rp) + c0 + (lane >> 1), v[0] * qs);
   }
   if (cb == 0) {
     for (int n = warp; n < N; n += kConsumerWarps) {
@@ -1691,31 +1754,46 @@ __device__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr
   }
 }
 
-// instruction (a = head h, b = 64-row block of v_head): out[n][h * v_head + j] = W_UV[h][j] . o_lat[n][h]
+// instruction (a = head h, b = 64-row block of v_head): out[n][h * v_head + j] = W_UV[h][j] . o_lat[n][h].
+// Warp w owns 8 rows j (v_head is a multiple of 16, so a warp's rows are all valid or all past the end);
+// lane L holds latent dims [16L, 16L + 16) of each row, loaded together up front.
 __device__ void mla_uv_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int h = in.a, jb = in.b;
   const int kl = op.kv_lora, vh = op.v_head;
-  const int per_warp = 64 / kConsumerWarps;
   const int N = p.N;
-  for (int jj = 0; jj < per_warp; ++jj) {
-    const int j = jb * 64 + warp * per_warp + jj;
-    if (j >= vh) break;
-    const uint16_t* wrow = op.w_uv + ((size_t)h * vh + j) * kl + lane * 16;
+  const int j0 = jb * 64 + warp * 8;
+  if (j0 >= vh) return;
+  uint32_t ws[8][8];
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    const uint16_t* wrow = op.w_uv + ((size_t)h * vh + j0 + jj) * kl + lane * 16;
     const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(wrow));
     const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(wrow + 8));
-    const uint32_t ws[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    for (int n = 0; n < N; ++n) {
-      const float* ol = op.in + (size_t)n * op.in_stride + (size_t)h * kl + lane * 16;
+    ws[jj][0] = a0.x; ws[jj][1] = a0.y; ws[jj][2] = a0.z; ws[jj][3] = a0.w;
+    ws[jj][4] = a1.x; ws[jj][5] = a1.y; ws[jj][6] = a1.z; ws[jj][7] = a1.w;
+  }
+  for (int n = 0; n < N; ++n) {
+    const float* ol = op.in + (size_t)n * op.in_stride + (size_t)h * kl + lane * 16;
+    float o[16];
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(ol + e));
+      o[e] = t.x; o[e + 1] = t.y; o[e + 2] = t.z; o[e + 3] = t.w;
+    }
+    float v[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
       float d = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        d = fmaf(bf_lo(ws[e]), __ldcg(ol + 2 * e), d);
-        d = fmaf(bf_hi(ws[e]), __ldcg(ol + 2 * e + 1), d);
+        d = fmaf(bf_lo(ws[jj][e]), o[2 * e], d);
+        d = fmaf(bf_hi(ws[jj][e]), o[2 * e + 1], d);
       }
-      d = warp_sum(d);
-      if (lane == 0) __stcg(op.out + (size_t)n * op.out_stride + (size_t)h * vh + j, d);
+      v[jj] = d;
     }
+    MultiReduce<8, 16>::run(v, lane);  // lane 4i: row i
+    if ((lane & 3) == 0) __stcg(op.out + (size_t)n * op.out_stride + (size_t)h * vh + j0 + (lane >> 2), v[0]);
   }
 }
 
@@ -2030,15 +2108,23 @@ __device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, 
       case OP_MOE_UP:
       case OP_MOE_DOWN:
         if (op.fp4) {
-          if (nr == 1) moe_consume<16, 1, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 2) moe_consume<16, 2, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 4) moe_consume<16, 4, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else moe_consume<8, 8, 8, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          if (op.staged) {
+            if (nr == 1) moe_consume<16, 1, 8, true, true>(p, op, in, rg, chunk, cs, actf, ctid);
+            else moe_consume<16, 2, 8, true, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          } else if (nr == 4) {
+            moe_consume<16, 4, 8, true, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          } else {
+            moe_consume<8, 8, 8, true, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          }
         } else {
-          if (nr == 1) moe_consume<16, 1, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 2) moe_consume<16, 2, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 4) moe_consume<16, 4, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else moe_consume<8, 8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          if (op.staged) {
+            if (nr == 1) moe_consume<16, 1, 4, false, true>(p, op, in, rg, chunk, cs, actf, ctid);
+            else moe_consume<16, 2, 4, false, true>(p, op, in, rg, chunk, cs, actf, ctid);
+          } else if (nr == 4) {
+            moe_consume<16, 4, 4, false, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          } else {
+            moe_consume<8, 8, 8, false, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          }
         }
         break;
       case OP_MLA_PREP: mla_prep_consume(p, op, ctid); break;
