@@ -159,7 +159,8 @@ struct CSmem {
   int32_t last;
   int32_t pad[2];
   float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
-  float e2m1[16];                        // e2m1 code -> value (NVFP4 experts)
+  int32_t uni_c[kMaxExperts + 4];        // MoE: the step's expert union, consumers' copy (count, ids)
+  int32_t uni_p[kMaxExperts + 4];        // the producer warp's copy
 };
 
 struct Ring {
@@ -1274,14 +1275,6 @@ __device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, 
   }
 }
 
-// e2m1 code -> value: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0 is the
-// subnormal m * 0.5 (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6). Filled into shared memory at kernel start.
-__device__ __forceinline__ float e2m1_value(int code) {
-  const int e = (code >> 1) & 3, m = code & 1;
-  const float mag = (e == 0) ? 0.5f * m : ldexpf(1.0f + 0.5f * m, e - 1);
-  return (code & 8) ? -mag : mag;
-}
-
 __device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
   __nv_fp8_e4m3 v;
   v.__x = b;
@@ -1293,10 +1286,11 @@ struct ExpertRow {
   const uint8_t* w;
   const uint8_t* s;
 };
-__device__ __forceinline__ ExpertRow expert_row(const KParams& p, const OpDesc& op, int j, int m, int r, int K) {
+__device__ __forceinline__ ExpertRow expert_row(const KParams& p, const OpDesc& op, int j, int m, int r, int K,
+                                               const int32_t* uni) {
   const int S = op.n_shared;
   const bool shared = j < S;
-  const int e = shared ? j : __ldcg(p.union_list + 1 + (j - S));
+  const int e = shared ? j : uni[1 + (j - S)];
   const int rows = (op.type == OP_MOE_UP) ? op.F : p.d;
   const size_t row = (size_t)e * rows + r;
   ExpertRow out;
@@ -1311,11 +1305,26 @@ __device__ __forceinline__ ExpertRow expert_row(const KParams& p, const OpDesc& 
   return out;
 }
 
-__device__ __forceinline__ float expert_gscale(const KParams& p, const OpDesc& op, int j, int m) {
+__device__ __forceinline__ float expert_gscale(const OpDesc& op, int j, int m, const int32_t* uni) {
   if (!op.fp4) return 1.f;
   const int S = op.n_shared;
   if (j < S) return __ldg(op.sgs[m] + j);
-  return __ldg(op.egs[m] + __ldcg(p.union_list + 1 + (j - S)));
+  return __ldg(op.egs[m] + uni[1 + (j - S)]);
+}
+
+// Eight e2m1 codes (one 32-bit word, element i in bits 4i..4i+3) times the block scale, without a table:
+// one byte permute looks up twice the magnitudes {0, 1, 2, 3, 4, 6, 8, 12} of four codes at once, the
+// 2^23 bias trick turns a byte into its float value, and the code's sign bit picks +-scale/2.
+__device__ __forceinline__ void e2m1x8_decode(uint32_t codes, float scale, float (&w)[8]) {
+  const float hs = 0.5f * scale;
+  const uint32_t m03 = __byte_perm(0x03020100u, 0x0C080604u, codes & 0x7777u);
+  const uint32_t m47 = __byte_perm(0x03020100u, 0x0C080604u, (codes >> 16) & 0x7777u);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t mag = ((c < 4 ? m03 : m47) >> (8 * (c & 3))) & 0xffu;
+    const float v = __uint_as_float(0x4B000000u | mag) - 8388608.0f;
+    w[c] = v * (((codes >> (4 * c + 3)) & 1u) ? -hs : hs);
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1341,7 +1350,10 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
   const int N = p.N;
   const int K = up ? p.d : op.F;
   const int glog = up ? RG / 2 : RG;
-  const int nsel = op.n_shared + __ldcg(p.union_list);
+  const int ucount = __ldcg(p.union_list);
+  const int nsel = op.n_shared + ucount;
+  for (int i = ctid; i <= ucount; i += kConsumerThreads) cs.uni_c[i] = __ldcg(p.union_list + i);
+  const int32_t* uni = cs.uni_c;  // read after the consumer_sync below
   const int nrows = in.b - in.a;
   const int ng = gemv_ngroups(nrows, glog);
   const int passes = op.passes;
@@ -1392,8 +1404,8 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
   consumer_sync();
 
   for (int j = 0; j < nsel && ng > 0; ++j) {
-    const float gs0 = expert_gscale(p, op, j, 0);
-    const float gs1 = up ? expert_gscale(p, op, j, 1) : 1.f;
+    const float gs0 = expert_gscale(op, j, 0, uni);
+    const float gs1 = up ? expert_gscale(op, j, 1, uni) : 1.f;
     const float* hin = p.hexp + (size_t)j * N * op.F;  // DOWN input
     if (STG && !up) {
       // expert j's rows were requested one expert ago; request j + 1's, wait for j's, publish
@@ -1406,7 +1418,7 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
       consumer_sync();
       hin = hst + (j & 1) * N * op.F;
     }
-    const int ej = j < op.n_shared ? -1 : __ldcg(p.union_list + 1 + (j - op.n_shared));
+    const int ej = j < op.n_shared ? -1 : uni[1 + (j - op.n_shared)];
     for (int pass = 0; pass < passes; ++pass) {
       const int nbase = pass * NR;
       for (int grp = 0; grp < ng; ++grp) {
@@ -1447,7 +1459,7 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
           ring_wait_full(rg, chunk, p);
           if (col < kw) {
             const uint8_t* slot = rg.slot_ptr(chunk);
-            if (FP4) {
+            if constexpr (FP4) {
               const int pitch = kw / 2 + kw / 16;
 #pragma unroll
               for (int i = 0; i < RG; ++i) {
@@ -1455,8 +1467,7 @@ __device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in,
                 const uint32_t codes = *reinterpret_cast<const uint32_t*>(rowp + col / 2);
                 const float sc = e4m3_to_f32(rowp[kw / 2 + col / 16]);
                 float wf[CPL];
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) wf[c] = cs.e2m1[(codes >> (4 * c)) & 15u] * sc;
+                e2m1x8_decode(codes, sc, wf);
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
 #pragma unroll
@@ -1825,8 +1836,10 @@ struct ChunkCursor {
   // number of copies per chunk (2: K and V of GQA; 1: the MLA latent)
   int t, t1, P, pos_bytes, ncopy;
   const uint16_t* kv;
-  // MoE walk: selected expert slot, count, format, this lane's weight row (codes) and scale row
+  // MoE walk: selected expert slot, count, format, this lane's weight row (codes) and scale row; the
+  // step's expert union, copied into shared memory when the walk reaches an expert op
   int j, nsel, fp4, up;
+  int32_t* uni;
   const uint8_t* mw;
   const uint8_t* ms;
 };
@@ -1841,7 +1854,7 @@ __device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& 
   if (pr < c.nphys) {
     const int m = (c.up && pr >= nl) ? 1 : 0;
     const int r = g0 + (m ? pr - nl : pr);
-    const ExpertRow er = expert_row(p, *c.op, c.j, m, r, c.K);
+    const ExpertRow er = expert_row(p, *c.op, c.j, m, r, c.K, c.uni);
     c.mw = er.w;
     c.ms = er.s;
   }
@@ -1915,7 +1928,10 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         c.K = c.up ? p.d : op.F;
         c.kc = op.kc;
         c.passes = op.passes;
-        c.nsel = op.n_shared + __ldcg(p.union_list);
+        const int ucount = __ldcg(p.union_list);
+        for (int i = lane; i <= ucount; i += 32) c.uni[i] = __ldcg(p.union_list + i);
+        __syncwarp();
+        c.nsel = op.n_shared + ucount;
         c.j = c.pass = c.grp = c.k0 = 0;
         if (c.ng == 0 || c.nsel == 0) {
           ++c.qi;
@@ -2051,7 +2067,7 @@ __device__ void final_consume(const KParams& p, int ctid) {
 // ------------------------------------------------------------------------------------------------
 // the two roles
 // ------------------------------------------------------------------------------------------------
-__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
+__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, int32_t* uni) {
   const int lane = threadIdx.x & 31;
   uint32_t chunk = 0;
   const uint32_t ring_base = smem_u32(rg.base);
@@ -2059,6 +2075,7 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1) {
   mc.qi = pc.qi = q0;
   mc.q1 = pc.q1 = q1;
   mc.kind = pc.kind = 0;
+  mc.uni = pc.uni = uni;
   const void* src = nullptr;
   uint32_t bytes = 0, dst = 0, total = 0;
   if (kPrefetchAhead > 0) {
@@ -2262,12 +2279,8 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     if (s_state == 0 && blockIdx.x == 0 && tid == 0) atomicCAS(p.status, 0, kStatusDevice);
     return;
   }
-  if (kFull) {
-    if (tid < 16) cs.e2m1[tid] = e2m1_value(tid);
-    __syncthreads();
-  }
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
-  if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1);
+  if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1, cs.uni_p);
   else run_consumer(p, rg, cs, act, q0, q1, tid);
 }
 
