@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <math_constants.h>
+#include <float.h>
 #include <stdint.h>
 
 #include "mk_internal.h"
@@ -1217,10 +1218,12 @@ __device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, 
     for (int j = 0; j < kMaxExperts / 32; ++j) {
       const int e = lane + 32 * j;
       sc[j] = 0.f;
-      bs[j] = -CUDART_INF_F;
+      bs[j] = -CUDART_INF_F;  // past the last expert, or already picked: never selected
       if (e < E) {
         sc[j] = sigmoidf_(__ldcg(op.in + (size_t)n * op.in_stride + e));
-        bs[j] = sc[j] + (op.router_bias ? __ldg(op.router_bias + e) : 0.f);
+        const float b = sc[j] + (op.router_bias ? __ldg(op.router_bias + e) : 0.f);
+        // a selectable expert always beats -inf, so each pass picks a valid id even from NaN scores
+        bs[j] = (b == b) ? fmaxf(b, -FLT_MAX) : -FLT_MAX;
       }
     }
     float ssum = 0.f;
