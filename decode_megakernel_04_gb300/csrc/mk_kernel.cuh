@@ -743,7 +743,7 @@ __device__ __forceinline__ int token_of(const KParams& p, int n) {
   return p.tokens[(n / p.R) * p.tok_stride + (n % p.R)];
 }
 
-__device__ void embed_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+__device__ __noinline__ void embed_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   for (int n = warp; n < p.N; n += kConsumerWarps) {
     const int tok = token_of(p, n);
@@ -766,7 +766,7 @@ __device__ __forceinline__ size_t kv_index(const KParams& p, const OpDesc& op, i
   return ((((size_t)op.slot * p.max_batch + b) * op.n_kv_heads + g) * p.max_ctx + t) * op.head_dim;
 }
 
-__device__ void rope_append_consume(const KParams& p, const OpDesc& op, int ctid) {
+__device__ __noinline__ void rope_append_consume(const KParams& p, const OpDesc& op, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hq = op.n_heads, hkv = op.n_kv_heads, hd = op.head_dim, half = hd / 2;
   const int per_row = hq + 2 * hkv;
@@ -874,7 +874,7 @@ __device__ __forceinline__ void attn_block(const uint16_t* Ks, const uint16_t* V
 }
 
 template <int E, int J>
-__device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+__device__ __noinline__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
                              CSmem& cs, uint16_t* stage_u16, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hd = E * 32;
@@ -960,7 +960,7 @@ __device__ void attn_consume(const KParams& p, const OpDesc& op, const Instr& in
 // of independent loads per 4 chunks); the 8 warp results are merged through shared memory.
 // ------------------------------------------------------------------------------------------------
 template <int E>
-__device__ void attn_combine_consume(const KParams& p, const OpDesc& op, const Instr& in, float* stage, int ctid) {
+__device__ __noinline__ void attn_combine_consume(const KParams& p, const OpDesc& op, const Instr& in, float* stage, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hd = E * 32;
   const int hkv = op.n_kv_heads, G = op.groups, NC = op.nchunk;
@@ -1037,7 +1037,7 @@ __device__ void attn_combine_consume(const KParams& p, const OpDesc& op, const I
 // is staged in shared memory by one round of independent loads before the arithmetic starts.
 // ------------------------------------------------------------------------------------------------
 template <int CW>
-__device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, CSmem& cs,
+__device__ __noinline__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, CSmem& cs,
                                           float* stage, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int b = in.a, h = in.b, jg = in.c;
@@ -1206,7 +1206,7 @@ __device__ void delta_consume(const KParams& p, const OpDesc& op, const Instr& i
 // its top-k as sequential argmax passes: Kimi K3's TPU megakernel, "How it maps onto a TPU v7"); the
 // weights are route_scale * s_sel / sum(s_sel). Also the union of the picked experts, ascending.
 // ------------------------------------------------------------------------------------------------
-__device__ void route_consume(const KParams& p, const OpDesc& op, float* stage, int ctid) {
+__device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, float* stage, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int E = op.n_experts, K = op.top_k, N = p.N;
   int* flags = reinterpret_cast<int*>(stage);
@@ -1344,7 +1344,7 @@ __device__ __forceinline__ void e2m1x8_decode(uint32_t codes, float scale, float
 // for MOE_UP the normalised x rows, staged once; for MOE_DOWN expert j's SwiGLU rows, copied with cp.async
 // into one of two buffers while expert j - 1 computes.
 template <int RG, int NR, int CPL, bool FP4, bool STG>
-__device__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+__device__ __noinline__ void moe_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
                             CSmem& cs, float* act, int ctid) {
   constexpr int KC = CPL * kConsumerThreads;
   constexpr int V = RG * NR;
@@ -1550,7 +1550,7 @@ __device__ __forceinline__ size_t lat_index(const KParams& p, const OpDesc& op, 
   return (((size_t)op.slot * p.max_batch + b) * p.max_ctx + t) * (op.kv_lora + op.rope);
 }
 
-__device__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
+__device__ __noinline__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int total = p.N * 2;
   const int ql = op.q_lora, kl = op.kv_lora, rp = op.rope, half = rp / 2;
@@ -1592,7 +1592,7 @@ __device__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
 // also writes the rotated rope query qt[n][h][kv_lora ..]. Warp w owns 16 latent columns: their W_UK rows
 // (lane L holds inputs [L*E, L*E + E) of each) are loaded together up front, then each query row costs 16
 // dot products folded across the warp by one multi-value reduction.
-__device__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+__device__ __noinline__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int h = in.a, cb = in.b;
   const int nope = op.nope, rp = op.rope, kl = op.kv_lora, half = rp / 2;
@@ -1702,7 +1702,7 @@ __device__ __forceinline__ void mla_block(const uint16_t* lat, int nb, int ldl, 
 // instruction (a = b * ngroups + head group, b = chunk, c = first row | last row << 8); warp w owns head
 // group*8 + w for the rows of the instruction (J rows per warp)
 template <int J>
-__device__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+__device__ __noinline__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
                                  uint32_t& chunk, uint16_t* stage, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int ngr = op.n_kv_heads, G = op.groups;  // head groups, heads per group
@@ -1771,7 +1771,7 @@ __device__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr
 // instruction (a = head h, b = 64-row block of v_head): out[n][h * v_head + j] = W_UV[h][j] . o_lat[n][h].
 // Warp w owns 8 rows j (v_head is a multiple of 16, so a warp's rows are all valid or all past the end);
 // lane L holds latent dims [16L, 16L + 16) of each row, loaded together up front.
-__device__ void mla_uv_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+__device__ __noinline__ void mla_uv_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int h = in.a, jb = in.b;
   const int kl = op.kv_lora, vh = op.v_head;
@@ -2035,7 +2035,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
 // ------------------------------------------------------------------------------------------------
 // final op: greedy argmax over the LM-head partials, sequence bookkeeping, counter reset
 // ------------------------------------------------------------------------------------------------
-__device__ void final_consume(const KParams& p, int ctid) {
+__device__ __noinline__ void final_consume(const KParams& p, int ctid) {
   if (p.argmax) {
     const int warp = ctid >> 5, lane = ctid & 31;
     for (int n = warp; n < p.N; n += kConsumerWarps) {
@@ -2115,7 +2115,7 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
 }
 
 template <int RG, int NR, bool STAGED>
-__device__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
+__device__ __noinline__ void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
                                            uint32_t& chunk, CSmem& cs, float* act, int ctid) {
   gemv_consume<RG, NR, STAGED>(p, op, in, rg, chunk, cs, act, ctid);
 }
