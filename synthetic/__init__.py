@@ -13,4 +13,4 @@ from .workloads import (  # noqa: F401
     make_tokens,
     weight_names,
 )
-from .nvfp4 import quantize_nvfp4, E2M1_GRID  # noqa: F401
+from .nvfp4 import quantize_nvfp4, quantize_nvfp4_experts, E2M1_GRID  # noqa: F401

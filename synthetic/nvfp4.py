@@ -31,15 +31,9 @@ def _e2m1_code(v: torch.Tensor) -> torch.Tensor:
     return (code + 8 * sign.to(code.dtype)).to(torch.uint8)
 
 
-def quantize_nvfp4(w: torch.Tensor):
-    """Encode fp32 ``w`` [..., K] (K % 16 == 0). Returns (packed uint8 [..., K/2],
-    e4m3 scale bits uint8 [..., K/16], fp32 tensor scale [1])."""
-    assert w.shape[-1] % 16 == 0
-    w = w.float()
-    amax = w.abs().max()
-    g = (amax / (6.0 * 448.0)).reshape(1).float()
-    if float(amax) == 0.0:
-        g = torch.ones(1, dtype=torch.float32, device=w.device)
+def _encode(w: torch.Tensor, g: torch.Tensor):
+    """Block scales and codes of ``w`` [..., K] given its tensor scale ``g`` (broadcastable to w's
+    leading dims + one trailing block axis)."""
     blocks = w.reshape(*w.shape[:-1], w.shape[-1] // 16, 16)
     amax_b = blocks.abs().amax(dim=-1)
     s = (amax_b / (6.0 * g)).clamp(max=448.0).to(torch.float8_e4m3fn)
@@ -49,4 +43,30 @@ def quantize_nvfp4(w: torch.Tensor):
     scaled = torch.where(denom > 0, blocks / safe, torch.zeros_like(blocks))
     codes = _e2m1_code(scaled).reshape(*w.shape)
     packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
-    return packed.contiguous(), s.view(torch.uint8).contiguous(), g
+    return packed.contiguous(), s.view(torch.uint8).contiguous()
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """Encode fp32 ``w`` [..., K] (K % 16 == 0). Returns (packed uint8 [..., K/2],
+    e4m3 scale bits uint8 [..., K/16], fp32 tensor scale [1])."""
+    assert w.shape[-1] % 16 == 0
+    w = w.float()
+    amax = w.abs().max()
+    g = (amax / (6.0 * 448.0)).reshape(1).float()
+    if float(amax) == 0.0:
+        g = torch.ones(1, dtype=torch.float32, device=w.device)
+    packed, s = _encode(w, g)
+    return packed, s, g
+
+
+def quantize_nvfp4_experts(w: torch.Tensor):
+    """``quantize_nvfp4`` applied to each w[e] of a stack [E, rows, K] at once (one tensor scale per
+    expert); the same bytes as the per-expert calls. Returns (packed [E, rows, K/2], scales
+    [E, rows, K/16], tensor scales [E])."""
+    assert w.dim() == 3 and w.shape[-1] % 16 == 0
+    w = w.float()
+    amax = w.abs().amax(dim=(1, 2))
+    g = (amax / (6.0 * 448.0)).float()
+    g = torch.where(amax == 0.0, torch.ones_like(g), g)
+    packed, s = _encode(w, g.reshape(-1, 1, 1))
+    return packed, s, g

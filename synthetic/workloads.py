@@ -17,7 +17,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-from .nvfp4 import quantize_nvfp4
+from .nvfp4 import quantize_nvfp4_experts
 
 
 @dataclass(frozen=True)
@@ -204,16 +204,19 @@ def make_weights(cfg: ModelConfig, seed: int = 0, device="cpu") -> dict[str, tor
             else:
                 out[name] = torch.zeros(shape, dtype=torch.float32, device=device)
         elif leaf in _EXPERT and cfg.expert_fmt == "nvfp4":
+            # experts are drawn one by one (each from its own stream) and encoded 16 at a time
             qs, ss, gs = [], [], []
-            for e in range(shape[0]):
-                w = _bf16(shape[1:], seed, f"{name}.{e}", cfg.init_std, device)
-                q, s, g = quantize_nvfp4(w.float())
+            for e0 in range(0, shape[0], 16):
+                w = torch.stack([_bf16(shape[1:], seed, f"{name}.{e}", cfg.init_std, device).float()
+                                 for e in range(e0, min(shape[0], e0 + 16))])
+                q, s, g = quantize_nvfp4_experts(w)
                 qs.append(q)
                 ss.append(s)
                 gs.append(g)
-            out[name + ".q"] = torch.stack(qs)
-            out[name + ".s"] = torch.stack(ss)
-            out[name + ".g"] = torch.stack(gs).reshape(shape[0]).to(torch.float32)
+                del w
+            out[name + ".q"] = torch.cat(qs)
+            out[name + ".s"] = torch.cat(ss)
+            out[name + ".g"] = torch.cat(gs).to(torch.float32)
         elif leaf in _EXPERT:
             out[name] = torch.stack(
                 [_bf16(shape[1:], seed, f"{name}.{e}", cfg.init_std, device) for e in range(shape[0])])

@@ -205,3 +205,15 @@ def test_linear_is_float64_product():
     x = RNG.standard_normal((3, 300))
     w = RNG.standard_normal((5000, 300)).astype(np.float32)
     np.testing.assert_allclose(ops.linear(x, w, block=777), x @ w.astype(np.float64).T, rtol=1e-12)
+
+
+def test_nvfp4_expert_stack_matches_per_expert_encoding():
+    """The stacked encoder (one tensor scale per expert) gives the same bytes as encoding each expert alone,
+    including an all-zero expert."""
+    from synthetic import quantize_nvfp4_experts
+    w = torch.from_numpy(RNG.standard_normal((5, 7, 64)) * 0.02).float()
+    w[3] = 0.0
+    q, s, g = quantize_nvfp4_experts(w)
+    for e in range(5):
+        qe, se, ge = quantize_nvfp4(w[e])
+        assert torch.equal(q[e], qe) and torch.equal(s[e], se) and float(g[e]) == float(ge)
