@@ -19,11 +19,11 @@ constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 #ifndef MK_RING_SLOTS
 #define MK_RING_SLOTS 4
 #endif
-#ifndef MK_ACT_KB
-#define MK_ACT_KB 72
-#endif
 constexpr int kSlots = MK_RING_SLOTS;
-constexpr int kActBytes = MK_ACT_KB * 1024;  // shared-memory activation / staging area
+// shared-memory activation / staging area: 80.25 KB, what is left of the 227 KB a CTA may use after the
+// ring and the consumers' bookkeeping; it holds 4 activation rows of width 5120 as bf16 hi/lo pairs with
+// their 16-byte row padding (4 x 5128 x 4 bytes), so batch 4 of a d = 5120 model takes the tensor cores
+constexpr int kActBytes = 82176;
 constexpr int kSlotBytes = 33 * 1024;   // ring slot allocation (payload <= kChunkBytes + row padding)
 constexpr int kChunkBytes = 32768;      // weight bytes per chunk
 constexpr int kMaxN = 64;        // rows per step (batch * rows)

@@ -187,6 +187,8 @@ constexpr size_t kActOff = (kCSmemOff + sizeof(CSmem) + 127) / 128 * 128;
 // ring | barriers | consumer scratch | activation / staging area (GEMV input rows as bf16; the attention
 // block's own K/V rows; the delta rule's row inputs)
 constexpr size_t kSmemBytes = kActOff + kActBytes;
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+static_assert(kActBytes % 128 == 0, "staging area must keep 128-byte alignment");
 
 // consumer side of one ring chunk
 __device__ __forceinline__ bool ring_wait_full(const Ring& rg, uint32_t chunk, const KParams& p) {

@@ -200,3 +200,12 @@ def test_fork_sequence():
         pos = pos + (rows if rows == 1 else 5)
     mk.close()
     _check(rep)
+
+
+def test_hybrid_batch4_decode():
+    """Batch 4 at full width: 4 activation rows of width 5120 fill the shared-memory staging area of the
+    tensor-core GEMV exactly."""
+    from gpu_harness import run_case
+    cfg = config("hybrid_gdn_gqa", n_layers=4)
+    rep = run_case(cfg, B=4, T=20, decode_steps=2, tol=TOL_BF16)
+    _check(rep)
