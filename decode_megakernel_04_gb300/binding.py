@@ -53,6 +53,18 @@ class Info(C.Structure):
                 ("ring_slot_bytes", _I), ("n_ops_last", _I), ("device_bytes", C.c_int64)]
 
 
+PLAN_OP_FIELDS = ["type", "n_instr", "layer", "rows", "K", "k_begin", "ldw", "mma", "staged", "kc", "rg", "passes",
+                  "out_kind", "nchunk", "groups", "head_dim", "n_heads", "n_kv_heads", "col_group"]
+
+
+class PlanOp(C.Structure):
+    _fields_ = [(f, _I) for f in PLAN_OP_FIELDS]
+
+
+class PlanInstr(C.Structure):
+    _fields_ = [("op", _I), ("sm", _I), ("a", _I), ("b", _I), ("c", _I)]
+
+
 class StateBuffers(C.Structure):
     """Caller-owned persistent buffers of mk_decode_step_static (see include/mk.h)."""
     _fields_ = [("kcache", _P), ("vcache", _P), ("state", _P), ("pending", _P), ("seq", _P), ("epoch", C.c_uint32)]
@@ -60,7 +72,7 @@ class StateBuffers(C.Structure):
 
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
            "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log",
-           "mk_fork_sequence"]
+           "mk_fork_sequence", "mk_plan"]
 
 _lib = None
 
@@ -90,14 +102,37 @@ def load(path: str | None = None) -> C.CDLL:
     lib.mk_destroy.restype = None
     lib.mk_set_routing_log.argtypes = [_P, _P]
     lib.mk_fork_sequence.argtypes = [_P, C.c_int, C.c_int, _P]
+    lib.mk_plan.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, C.c_int,
+                            C.POINTER(PlanOp), C.c_int, C.POINTER(C.c_int), C.POINTER(PlanInstr), C.c_int,
+                            C.POINTER(C.c_int)]
     lib.mk_decode_step_static.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.POINTER(StateBuffers),
                                           _P, _P, C.c_int, C.c_int, _P, _P, _P]
     for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
-              "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence"):
+              "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence", "mk_plan"):
         getattr(lib, f).restype = C.c_int
     if path is None:
         _lib = lib
     return lib
+
+
+def plan(desc: ModelDesc, weights: Weights, n_sm: int, batch: int, rows: int, head: bool = True):
+    """mk_plan: the program of one step shape for an n_sm-SM device, compiled on the host. Returns
+    (ops, instrs) as lists of dicts (fields of mk_plan_op / mk_plan_instr)."""
+    lib = load()
+    n_ops, n_instr = C.c_int(0), C.c_int(0)
+    rc = lib.mk_plan(C.byref(desc), C.byref(weights), n_sm, batch, rows, int(head), None, 0, C.byref(n_ops), None, 0,
+                     C.byref(n_instr))
+    if rc != MK_OK:
+        raise MKError(rc, "mk_plan")
+    ops = (PlanOp * max(1, n_ops.value))()
+    ins = (PlanInstr * max(1, n_instr.value))()
+    rc = lib.mk_plan(C.byref(desc), C.byref(weights), n_sm, batch, rows, int(head), ops, n_ops.value, C.byref(n_ops),
+                     ins, n_instr.value, C.byref(n_instr))
+    if rc != MK_OK:
+        raise MKError(rc, "mk_plan")
+    as_dict = lambda r, names: {f: getattr(r, f) for f in names}
+    return ([as_dict(ops[i], PLAN_OP_FIELDS) for i in range(n_ops.value)],
+            [as_dict(ins[i], ("op", "sm", "a", "b", "c")) for i in range(n_instr.value)])
 
 
 class MKError(RuntimeError):

@@ -1134,6 +1134,60 @@ mk_status mk_get_status(mk_handle* h, void* stream) {
   return MK_OK;
 }
 
+mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm, int batch, int rows,
+                  int with_head, mk_plan_op* ops, int ops_cap, int* n_ops, mk_plan_instr* instrs, int instr_cap,
+                  int* n_instr) {
+  if (!desc || !weights || !n_ops || !n_instr || n_sm < 1 || n_sm > 4096) return MK_ERR_INVALID_ARG;
+  mk_handle tmp;  // shape only: no device memory, buffer pointers stay NULL
+  tmp.desc = *desc;
+  tmp.w = *weights;
+  tmp.n_sm = n_sm;
+  mk_status st = check_desc(&tmp, tmp.desc, tmp.w);
+  if (st != MK_OK) return st;
+  if (batch < 1 || batch > desc->max_batch || rows < 1 || rows > desc->max_rows) return MK_ERR_INVALID_ARG;
+  derive_layout(&tmp);
+  HostProgram hp;
+  if ((st = construct_program(&tmp, batch, rows, with_head != 0, hp)) != MK_OK) return st;
+  *n_ops = (int)hp.ops.size();
+  *n_instr = (int)hp.flat.size();
+  for (int i = 0; i < (int)hp.ops.size() && ops && i < ops_cap; ++i) {
+    const OpDesc& o = hp.ops[i];
+    mk_plan_op& r = ops[i];
+    r.type = o.type;
+    r.n_instr = o.n_instr;
+    r.layer = o.layer;
+    r.rows = o.rows;
+    r.K = o.K;
+    r.k_begin = o.k_begin;
+    r.ldw = o.ldw;
+    r.mma = o.mma;
+    r.staged = o.staged;
+    r.kc = o.kc;
+    r.rg = o.rg;
+    r.passes = o.passes;
+    r.out_kind = o.out_kind;
+    r.nchunk = o.nchunk;
+    r.groups = o.groups;
+    r.head_dim = o.head_dim;
+    r.n_heads = o.n_heads;
+    r.n_kv_heads = o.n_kv_heads;
+    r.col_group = o.col_group;
+  }
+  if (instrs) {
+    int k = 0;
+    for (int sm = 0; sm < n_sm; ++sm)
+      for (int q = hp.qoff[sm]; q < hp.qoff[sm + 1] && k < instr_cap; ++q, ++k) {
+        const Instr& in = hp.flat[q];
+        instrs[k].op = in.op;
+        instrs[k].sm = sm;
+        instrs[k].a = in.a;
+        instrs[k].b = in.b;
+        instrs[k].c = in.c;
+      }
+  }
+  return MK_OK;
+}
+
 mk_status mk_fork_sequence(mk_handle* h, int src, int dst, void* stream) {
   if (!h) return MK_ERR_INVALID_ARG;
   const mk_model_desc& D = h->desc;

@@ -191,6 +191,36 @@ mk_status mk_get_status(mk_handle* h, void* stream);
  * The pages have no counterpart for this call. Errors: MK_ERR_INVALID_ARG, MK_ERR_CUDA. */
 mk_status mk_fork_sequence(mk_handle* h, int src, int dst, void* stream);
 
+/* ---- Program inspection (host only, no GPU needed) -------------------------------------------------
+ * Compiles the program of one step shape exactly as mk_decode_step would for a device with `n_sm` SMs,
+ * without touching any device, and describes it: one mk_plan_op per op (in program order) and one
+ * mk_plan_instr per instruction (grouped by SM, each SM's instructions in the order it runs them). The
+ * weight pointers are checked for presence and 16-byte alignment but never dereferenced. For tests and
+ * tools that check the scheduler (row coverage, chunking, staging decisions) on a machine without a GPU.
+ * The pages have no counterpart. Fills *n_ops / *n_instr with the true counts; writes at most ops_cap /
+ * instr_cap records. Errors: MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED (as mk_create / mk_decode_step). */
+typedef struct mk_plan_op {
+  int32_t type;        /* op kind (embed 0, gemv 1, rope/append 2, attention 3, delta rule 4, MLA prep 5,
+                          MLA attention 6, route 7, expert up 8, expert down 9, final 10, attention combine
+                          11, MLA absorbed query 12, MLA W_UV 13) */
+  int32_t n_instr;     /* instructions of the op                                                     */
+  int32_t layer;       /* model layer, -1 for embed / LM head / final                                 */
+  int32_t rows;        /* GEMV: logical output rows                                                   */
+  int32_t K, k_begin, ldw;  /* GEMV: inputs of this op, first input column, full input width         */
+  int32_t mma, staged, kc, rg, passes;  /* GEMV / expert path: tensor cores, staged inputs, inputs per
+                          chunk, weight rows per group, activation passes                              */
+  int32_t out_kind;    /* GEMV epilogue: store 0, residual 1, SwiGLU 2, logits 3                        */
+  int32_t nchunk, groups, head_dim, n_heads, n_kv_heads, col_group;  /* attention / delta / MLA       */
+} mk_plan_op;
+
+typedef struct mk_plan_instr {
+  int32_t op, sm, a, b, c;  /* op index, SM, and the op-specific operands (GEMV: rows [a, b))          */
+} mk_plan_instr;
+
+mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm, int batch, int rows,
+                  int with_head, mk_plan_op* ops, int ops_cap, int* n_ops, mk_plan_instr* instrs,
+                  int instr_cap, int* n_instr);
+
 /* Routing log of MoE models (for checking and analysis; the decode path does not need it). With a
  * non-NULL `device_log` — device int32 [n_layers][max_batch][max_ctx][top_k], owned by the caller and kept
  * alive while set — every later step and prefill writes, for each MoE layer l and each row r of sequence b
