@@ -100,7 +100,6 @@ struct mk_handle {
   size_t hexp_floats = 0;
   int32_t* route_log = nullptr;  // caller's device buffer (mk_set_routing_log) or NULL
   uint32_t* counters = nullptr;
-  uint32_t* arrive = nullptr;
   int32_t* status = nullptr;
   int32_t* abort_flag = nullptr;
   SeqState* seq = nullptr;
@@ -867,7 +866,6 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.instrs = prog->d_instr;
   p.qoff = prog->d_qoff;
   p.counters = h->counters;
-  p.arrive = h->arrive;
   p.status = h->status;
   p.abort_flag = h->abort_flag;
   p.timeout_ns = 2000000000ull;
@@ -1002,7 +1000,6 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const size_t cache = (size_t)h->n_gqa * Bm * hkv * D.max_ctx * hd;
     ALLOC(kcache, cache);
     ALLOC(vcache, cache);
-    ALLOC(arrive, (size_t)h->n_gqa * Bm * hkv);
   }
   if (h->n_gqa || h->n_mla) ALLOC(attn_part, attn_part_records(h, Bm, Rm) * h->attn_part_stride);
   if (h->n_mla) {
@@ -1125,8 +1122,6 @@ mk_status mk_get_status(mk_handle* h, void* stream) {
     cudaMemset(h->status, 0, sizeof(int32_t));
     cudaMemset(h->abort_flag, 0, sizeof(int32_t));
     cudaMemset(h->counters, 0, sizeof(uint32_t) * h->max_ops);
-    if (h->arrive)
-      cudaMemset(h->arrive, 0, sizeof(uint32_t) * (size_t)h->n_gqa * h->desc.max_batch * h->desc.n_kv_heads);
     cudaDeviceSynchronize();
     h->err = code == MK_ERR_TIMEOUT ? "device watchdog timeout" : "device input check failed (token or position)";
     return (mk_status)code;
@@ -1362,11 +1357,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
 
   // carve the working memory of this step out of the static array
   const int N = batch * rows;
-  const int hkv = std::max(D.n_kv_heads, 1);
   size_t off = 0;
   const size_t o_counters = carve(off, sizeof(uint32_t) * tmp.max_ops);
-  const size_t arrive_bytes = sizeof(uint32_t) * (size_t)tmp.n_gqa * D.max_batch * hkv;
-  const size_t o_arrive = carve(off, arrive_bytes);
   const size_t o_status = carve(off, 16);
   const size_t o_abort = carve(off, 16);
   const size_t o_x = carve(off, sizeof(float) * (size_t)N * D.d_model);
@@ -1379,7 +1371,6 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   if (tmp.n_gqa) o_apart = carve(off, sizeof(float) * attn_part_records(&tmp, batch, rows) * tmp.attn_part_stride);
   if (tmp.rot_dim) o_rope = carve(off, sizeof(float2) * (size_t)D.max_ctx * (tmp.rot_dim / 2));
   tmp.counters = reinterpret_cast<uint32_t*>(base + o_counters);
-  tmp.arrive = tmp.n_gqa ? reinterpret_cast<uint32_t*>(base + o_arrive) : nullptr;
   tmp.status = reinterpret_cast<int32_t*>(base + o_status);
   tmp.abort_flag = reinterpret_cast<int32_t*>(base + o_abort);
   tmp.x = reinterpret_cast<float*>(base + o_x);
@@ -1432,8 +1423,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
                            s)) != cudaSuccess ||
       (e = cudaMemsetAsync(tmp.counters, 0, sizeof(uint32_t) * tmp.max_ops, s)) != cudaSuccess ||
       (e = cudaMemsetAsync(tmp.status, 0, 16, s)) != cudaSuccess ||
-      (e = cudaMemsetAsync(tmp.abort_flag, 0, 16, s)) != cudaSuccess ||
-      (tmp.arrive && (e = cudaMemsetAsync(tmp.arrive, 0, arrive_bytes, s)) != cudaSuccess)) {
+      (e = cudaMemsetAsync(tmp.abort_flag, 0, 16, s)) != cudaSuccess) {
     fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
     return MK_ERR_CUDA;
   }

@@ -131,7 +131,6 @@ struct KParams {
   const Instr* instrs;
   const int32_t* qoff;      // [n_sm + 1] per-SM queue offsets into instrs
   uint32_t* counters;       // [n_ops] completed instructions per op in this launch
-  uint32_t* arrive;         // attention chunk arrival counters
   int32_t* status;
   int32_t* abort_flag;
   unsigned long long timeout_ns;

@@ -2,7 +2,7 @@
 //
 // Each CTA runs 8 consumer warps and 1 producer warp. The producer walks the SM's instruction queue
 // ahead of the consumers and streams every weight tile (and every cached-KV block) that an instruction
-// will read into a 6 x 32 KB shared-memory ring with bulk async copies (cp.async.bulk, completion on an
+// will read into a 4-slot shared-memory ring (32 KB of weights per slot) with bulk async copies (cp.async.bulk, completion on an
 // mbarrier). Weights never depend on activations, so the producer runs across op and layer boundaries
 // while the consumers wait on inter-SM dependency counters: the next op's weights are already arriving
 // when its inputs become ready. This is the pages' central idea — a weight load is issued as early as
