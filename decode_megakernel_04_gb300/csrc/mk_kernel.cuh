@@ -187,7 +187,9 @@ constexpr size_t kActOff = (kCSmemOff + sizeof(CSmem) + 127) / 128 * 128;
 // ring | barriers | consumer scratch | activation / staging area (GEMV input rows as bf16; the attention
 // block's own K/V rows; the delta rule's row inputs)
 constexpr size_t kSmemBytes = kActOff + kActBytes;
-static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+// 227 KB per CTA, less the 1 KB of static shared memory the kernel also uses (the 1024-byte alignment of
+// the dynamic array and the launch-state word)
+static_assert(kSmemBytes + 1024 <= 232448, "dynamic shared memory above what a CTA may use");
 static_assert(kActBytes % 128 == 0, "staging area must keep 128-byte alignment");
 
 // consumer side of one ring chunk
