@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -112,7 +113,7 @@ struct mk_handle {
   float* stage_logits = nullptr;
   int max_ops = 0;
   int n_ops_last = 0;
-  std::vector<Program> programs;
+  std::deque<Program> programs;  // stable addresses: launches and the trace keep pointers into it
   // optional per-instruction timestamp trace of the last step (env MK_TRACE=<file>), written at destroy
   std::string trace_path;
   unsigned long long* trace = nullptr;
@@ -832,11 +833,14 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     *st = cuda_fail(h, e, "program allocation");
     return prog;
   }
-  cudaMemcpy(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * prog.n_ops, cudaMemcpyHostToDevice);
-  cudaMemcpy(prog.d_instr, flat.data(), sizeof(Instr) * prog.n_instr, cudaMemcpyHostToDevice);
-  e = cudaMemcpy(prog.d_qoff, qoff.data(), sizeof(int32_t) * (h->n_sm + 1), cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) *st = cuda_fail(h, e, "program upload");
-  h->bytes += (int64_t)(sizeof(OpDesc) * prog.n_ops + sizeof(Instr) * prog.n_instr);
+  if ((e = cudaMemcpy(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * prog.n_ops, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(prog.d_instr, flat.data(), sizeof(Instr) * prog.n_instr, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(prog.d_qoff, qoff.data(), sizeof(int32_t) * (h->n_sm + 1), cudaMemcpyHostToDevice)) !=
+          cudaSuccess) {
+    *st = cuda_fail(h, e, "program upload");
+    return prog;
+  }
+  h->bytes += (int64_t)(sizeof(OpDesc) * prog.n_ops + sizeof(Instr) * prog.n_instr + sizeof(int32_t) * (h->n_sm + 1));
   return prog;
 }
 

@@ -164,7 +164,9 @@ mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_to
  * The verify semantics follow the pages' speculative step: an anchor plus seven drafts are checked
  * as eight rows of one sequence and only the accepted prefix is kept (Kimi K3's TPU megakernel,
  * "What DSpark changes per step").
- * One kernel launch. Asynchronous. Host errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch,
+ * One kernel launch. Asynchronous, except that the first call with a given (batch, rows) shape (and the
+ * first prefill with a given batch) compiles that shape's program and uploads it with synchronous
+ * cudaMalloc / cudaMemcpy; later calls reuse it. Host errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch,
  * rows outside 1..max_rows, both outputs NULL). Device errors via mk_get_status: MK_ERR_DEVICE
  * (token outside [0, vocab), position outside the window, positions[b] + rows > max_ctx; the step is
  * then skipped and no state changes), MK_ERR_TIMEOUT. */
