@@ -387,6 +387,7 @@ def run_mk(args, wl, cfg):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_step": acct},
+        "verify_steps_per_s": (1e3 / ms) if R > 1 else None,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clocks,
         "sweep": sweep, "kernel": "megakernel (one persistent launch per step)",
     }
