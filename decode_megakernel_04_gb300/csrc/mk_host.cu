@@ -1,6 +1,6 @@
 // Host side of libmk: the C ABI (include/mk.h), the device memory plan of a handle, and the scheduler
 // that compiles one decode step of the layer stack into per-SM instruction queues for the persistent
-// kernel (mk_kernel.cu).
+// kernel (mk_kernel.cuh, built as mk_kernel_dense.cu and mk_kernel_full.cu).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -408,7 +408,7 @@ OpDesc gemv_desc(int K, std::initializer_list<std::pair<const void*, int>> mats)
   return d;
 }
 
-// Multi-head latent attention, absorbed form, of layer i (the ops are described in mk_kernel.cu):
+// Multi-head latent attention, absorbed form, of layer i (the ops are described in mk_kernel.cuh):
 //   GEMV [w_dq; w_dkv] on RMSNorm(x) -> proj;  MLA_PREP: c_q norm -> mla_cq, latent (norm + rope) -> cache;
 //   GEMV w_uq on c_q -> mla_qf;  MLA_QABS -> mla_qt;  MLA_ATTN over context chunks -> partials;
 //   ATTN_COMBINE -> mla_olat;  MLA_UV -> attn_out;  GEMV wo, residual add.

@@ -1,4 +1,4 @@
-// Internal layout shared by the host scheduler (mk_host.cu) and the persistent kernel (mk_kernel.cu).
+// Internal layout shared by the host scheduler (mk_host.cu) and the persistent kernel (mk_kernel.cuh).
 //
 // A decode step is compiled into a PROGRAM: a list of ops in topological order (embedding, then per
 // layer: projection GEMV, attention / delta-rule op, output GEMV, FFN GEMVs, then LM head and a final
