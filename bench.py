@@ -16,6 +16,7 @@ Under torchrun every rank runs an independent replica on its own GPU (the path h
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -165,43 +166,70 @@ def max_over_ranks(v: float, ws: int) -> float:
 # ------------------------------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the step
 # ------------------------------------------------------------------------------------------------
+class OracleSampler:
+    """The oracle's decode step on a bounded sample of the model, built once and timed per step: the first
+    k layers at full width (k = 4: three delta-rule layers and one attention layer; 1 for MoE models, whose
+    layers hold tens of GB of experts) and an LM head over the first 1/8 of the vocabulary, after a
+    16-token prefill. The layer time is scaled to the full depth and the head time to the full vocabulary."""
+
+    def __init__(self, cfg, weights_cpu_fn, batch: int, rows: int):
+        from oracle import Oracle
+        self.cfg, self.batch, self.rows = cfg, batch, rows
+        self.k = 1 if cfg.ffn == "moe" else (4 if cfg.n_layers >= 4 else cfg.n_layers)
+        self.head_frac = 8 if cfg.vocab >= 8 * 1024 else 1
+        self.sub = dataclasses.replace(cfg.with_layers(self.k), vocab=cfg.vocab // self.head_frac)
+        self.orc = Oracle(self.sub, weights_cpu_fn(self.sub), batch, 64 + 64 * rows)
+        self.rng = np.random.default_rng(0)
+        self.orc.prefill(self.rng.integers(0, self.sub.vocab, size=(batch, 16)))
+        self.pos = np.full(batch, 16)
+
+    def step(self) -> float:
+        """One timed step; returns the estimated seconds of a full-model step."""
+        from oracle import ops
+        sub = self.sub
+        toks = self.rng.integers(0, sub.vocab, size=(self.batch, self.rows))
+        t0 = time.perf_counter()
+        self.orc.step(toks, self.pos)
+        t_step = time.perf_counter() - t0
+        self.pos = self.pos + self.rows
+        h = ops.rmsnorm(self.orc.x_final, self.orc.W("final_norm"), sub.norm_eps)
+        t0 = time.perf_counter()
+        ops.linear(h, self.orc.W("embed") if sub.tied else self.orc.W("lm_head"))
+        t_head = time.perf_counter() - t0
+        return (t_step - t_head) * self.cfg.n_layers / self.k + t_head * self.head_frac
+
+    def describe(self, n_steps: int) -> str:
+        return (f"oracle (numpy float64) decode step of the first {self.k} of {self.cfg.n_layers} layers at full "
+                f"width plus an LM head over 1/{self.head_frac} of the vocabulary, batch {self.batch}, "
+                f"{self.rows} row(s), 16-token context, {n_steps} step(s); layer time scaled to "
+                f"{self.cfg.n_layers} layers, head time to the full vocabulary")
+
+
+def sample_weights_from(w: dict, sub):
+    """The tensors of `sub` (its first layers, embedding / LM head rows of its vocabulary) copied to the
+    host from a full model's weights."""
+    out = {}
+    for name, t in w.items():
+        if name.startswith("layers.") and int(name.split(".")[1]) >= sub.n_layers:
+            continue
+        if name in ("embed", "lm_head"):
+            t = t[: sub.vocab]
+        out[name] = t.cpu()
+    return out
+
+
 def oracle_sample(cfg, weights_cpu_fn, batch: int, rows: int, n_steps: int = 2):
-    """Time the oracle's decode step on the first `k` layers of the model at full width plus the LM head,
-    after a 16-token prefill, and scale the per-layer time to the full depth. Returns (tok/s, seconds per
-    step estimate, description)."""
-    from oracle import Oracle, ops
-    # MoE layers hold tens of GB of experts: one layer is enough of a sample there
-    k = 1 if cfg.ffn == "moe" else (4 if cfg.n_layers >= 4 else cfg.n_layers)
-    sub = cfg.with_layers(k)
-    w = weights_cpu_fn(sub)
-    orc = Oracle(sub, w, batch, 64)
-    rng = np.random.default_rng(0)
-    orc.prefill(rng.integers(0, cfg.vocab, size=(batch, 16)))
-    t_total = 0.0
-    t_head = 0.0
-    pos = np.full(batch, 16)
-    for s in range(n_steps):
-        toks = rng.integers(0, cfg.vocab, size=(batch, rows))
-        t0 = time.perf_counter()
-        orc.step(toks, pos)
-        t_total += time.perf_counter() - t0
-        pos = pos + rows
-        h = ops.rmsnorm(orc.x_final, orc.W("final_norm"), cfg.norm_eps)
-        t0 = time.perf_counter()
-        ops.linear(h, orc.W("embed") if cfg.tied else orc.W("lm_head"))
-        t_head += time.perf_counter() - t0
-    t_total /= n_steps
-    t_head /= n_steps
-    est = (t_total - t_head) * cfg.n_layers / k + t_head
-    desc = (f"oracle (numpy float64) decode step of the first {k} of {cfg.n_layers} layers at full width plus "
-            f"the LM head, batch {batch}, {rows} row(s), 16-token context, {n_steps} steps; layer time scaled "
-            f"to {cfg.n_layers} layers")
-    return batch * rows / est, est, desc
+    """Time the oracle on its bounded sample (OracleSampler). Returns (tok/s, seconds per step estimate,
+    description)."""
+    smp = OracleSampler(cfg, weights_cpu_fn, batch, rows)
+    est = statistics.median([smp.step() for _ in range(n_steps)])
+    return batch * rows / est, est, smp.describe(n_steps)
 
 
 # ------------------------------------------------------------------------------------------------
 def run_reference(args, wl, cfg):
-    """The oracle as the reference arm: timed on the host cores, rank 0 only."""
+    """The oracle as the reference arm: timed on the host cores, rank 0 only; the sample is built once
+    and each of the warm-up + timed steps is one oracle step on it."""
     import torch
     from synthetic import make_weights
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -211,15 +239,11 @@ def run_reference(args, wl, cfg):
     B, R = args.batch, wl.rows
     tok_per_step = B * (args.accept if R > 1 else 1)
 
-    def wfn(sub):
-        return make_weights(sub, seed=0, device="cpu")
-
-    rates = []
-    for i in range(args.warmup + args.steps):
-        rate, est, desc = oracle_sample(cfg, wfn, B, R, n_steps=1)
-        if i >= args.warmup:
-            rates.append(est)
-    sec = statistics.median(rates)
+    smp = OracleSampler(cfg, lambda sub: make_weights(sub, seed=0, device="cpu"), B, R)
+    for _ in range(args.warmup):
+        smp.step()
+    sec = statistics.median([smp.step() for _ in range(args.steps)])
+    desc = smp.describe(args.steps)
     val = tok_per_step / sec
     cores = os.cpu_count()
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -370,9 +394,7 @@ def run_mk(args, wl, cfg):
         return
     cpu = None
     if not args.no_cpu:
-        def wfn(sub):
-            return {k: v for k, v in ((k, w[k].cpu()) for k in w) if _in_sub(k, sub)}
-        rate, est, desc = oracle_sample(cfg, wfn, B, R)
+        rate, est, desc = oracle_sample(cfg, lambda sub: sample_weights_from(w, sub), B, R)
         cpu = {"value": rate * (adv / R if R > 1 else 1), "unit": "tokens/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": desc}
     key = (args.workload, B)
@@ -392,12 +414,6 @@ def run_mk(args, wl, cfg):
         "sweep": sweep, "kernel": "megakernel (one persistent launch per step)",
     }
     print(json.dumps(line))
-
-
-def _in_sub(name: str, sub) -> bool:
-    if not name.startswith("layers."):
-        return True
-    return int(name.split(".")[1]) < sub.n_layers
 
 
 def main():
