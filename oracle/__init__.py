@@ -7,8 +7,9 @@ share only the seeded inputs drawn by ``synthetic``.
 
 Everything is numpy in float64: activations, accumulations, the recurrent state. Weights are the
 bf16-rounded draws (exact in float64); NVFP4 weights are decoded exactly as e2m1 * e4m3 * fp32.
-The KV cache and the MLA latent cache hold bf16-rounded values, because bf16 is the cache's storage
-format in this design (the rounding is part of what the step computes, not an implementation detail).
+The KV cache and the MLA latent cache hold the exact (float64) keys, values and latents: the pages fix
+no cache precision, so a narrower storage type is the implementation's choice and its rounding is
+absorbed by the comparison tolerance, not built into the definition.
 
 Parity status of each function is recorded in its docstring; the pins live in tests/test_oracle_*.py.
 """

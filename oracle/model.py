@@ -18,7 +18,15 @@ accepted prefix is kept (Kimi K3's TPU megakernel, "What DSpark changes per step
 R = 1 with p_b advancing by one. A prefill is one block of T rows that is then committed whole.
 
 Parity status: every mixer, the router and the FFNs are pinned (tests/test_oracle_*.py). The block
-composition is pinned by a closed form at the first token (attention over one key returns v).
+composition is pinned by closed forms at the first token (attention over one key returns v; the delta
+rule from a zero state is one rank-1 update). The MLA front half (the c_q and c_kv norms, the nope /
+rope split of the up-projected query, RoPE on the query and on the rope key) is pinned against an
+independent torch formulation (complex-number RoPE, scaled_dot_product_attention on the unabsorbed
+heads) and by invariances that a dropped norm or a misplaced split breaks; the KDA decay layout (which
+row of the decay projection gates which head and key channel) by a two-token closed form. The caches
+hold exact (float64) keys, values and latents.
+This module is test infrastructure: only the tests, the package's smoke check and the benchmark's CPU
+baseline use it; the CUDA path never imports it.
 """
 from __future__ import annotations
 
@@ -153,7 +161,10 @@ class Oracle:
         raise ValueError(kind)
 
     def gqa(self, i, h, positions):
-        """Grouped-query attention layer over the KV cache (bf16 storage)."""
+        """Grouped-query attention layer over the KV cache. The cache keeps the rotated keys and the
+        values exactly (float64): the pages say nothing about cache precision, so the definition holds
+        them unrounded, and a cache stored in a narrower type is an implementation choice whose
+        rounding the comparison tolerance has to absorb."""
         cfg = self.cfg
         hq, hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
         B, R, _ = h.shape
@@ -167,8 +178,8 @@ class Oracle:
             pos = positions[b] + np.arange(R)
             qb = ops.rope(q[b], pos[:, None], cfg.rope_theta)
             kb = ops.rope(k[b], pos[:, None], cfg.rope_theta)
-            K[b, pos] = ops.bf16_round(kb)
-            V[b, pos] = ops.bf16_round(v[b])
+            K[b, pos] = kb
+            V[b, pos] = v[b]
             o = ops.gqa_block_attention(qb, K[b], V[b], int(positions[b]))
             out[b] = o.reshape(R, hq * hd)
         return ops.linear(out, self.W(p + "wo"))
@@ -217,7 +228,7 @@ class Oracle:
             pos = positions[b] + np.arange(R)
             q_rope[b] = ops.rope(qf[b, :, :, nope:], pos[:, None], cfg.rope_theta)
             k_r = ops.rope(kv[b, :, lora:], pos, cfg.rope_theta)
-            lat[b, pos] = ops.bf16_round(np.concatenate([c_kv[b], k_r], axis=-1))
+            lat[b, pos] = np.concatenate([c_kv[b], k_r], axis=-1)
         return q_nope, q_rope
 
     def mla(self, i, h, positions, absorbed: bool = True):

@@ -18,8 +18,9 @@ F64 = np.float64
 def bf16_round(x) -> np.ndarray:
     """Round to bfloat16 (round to nearest, ties to even) and return float64.
 
-    Used for the caches, whose storage type is bf16. The value is first rounded to float32
-    (as every fp32 producer would hold it), then its low 16 bits are rounded away.
+    The value is first rounded to float32 (as every fp32 producer would hold it), then its low 16 bits
+    are rounded away. The step itself rounds nothing; this serves the tests that reason about bf16
+    storage.
     Pinned: equals torch's float32 -> bfloat16 conversion (tests/test_oracle_ops.py)."""
     f = np.asarray(x, dtype=np.float32)
     bits = f.view(np.uint32).astype(np.uint64)

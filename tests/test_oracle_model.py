@@ -127,8 +127,8 @@ def test_batch_rows_independent(kind):
 
 def test_first_token_closed_form_dense():
     """One dense GQA layer at position 0: the only key is the token itself, so every query head h
-    returns the cached (bf16) v of kv head floor(h * Hkv / Hq) and the layer is a fixed chain of
-    matrix products."""
+    returns the cached v of kv head floor(h * Hkv / Hq) and the layer is a fixed chain of matrix
+    products."""
     cfg = tiny("dense", n_layers=1, n_q_heads=4, n_kv_heads=2)
     w = {k: v.float().numpy().astype(np.float64) for k, v in _weights(cfg, seed=3).items()}
     tok = 17
@@ -139,7 +139,6 @@ def test_first_token_closed_form_dense():
 
     x0 = w["embed"][tok]
     v = w["layers.0.wv"] @ n(x0, w["layers.0.attn_norm"])
-    v = torch.from_numpy(v).float().to(torch.bfloat16).double().numpy()  # the cache stores bf16
     hd = cfg.head_dim
     heads = [v[(h * cfg.n_kv_heads // cfg.n_q_heads) * hd:][:hd] for h in range(cfg.n_q_heads)]
     x1 = x0 + w["layers.0.wo"] @ np.concatenate(heads)
