@@ -65,6 +65,7 @@ struct mk_handle {
   std::vector<void*> allocs;
   int64_t bytes = 0;
   uint32_t epoch = 0;
+  unsigned long long wait_limit_ns = 2000000000ull;  // watchdog limit of every device-side wait
 
   // per-layer slot among layers of the same kind
   std::vector<int> slot;
@@ -872,7 +873,8 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.counters = h->counters;
   p.status = h->status;
   p.abort_flag = h->abort_flag;
-  p.timeout_ns = 2000000000ull;
+  p.timeout_ns = h->wait_limit_ns;
+  p.spin_mask = h->wait_limit_ns < 1000000ull ? 0u : 63u;
   p.n_ops = prog->n_ops;
   p.n_sm = h->n_sm;
   p.tokens = tokens;
@@ -1227,6 +1229,13 @@ mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log) {
   return MK_OK;
 }
 
+mk_status mk_set_wait_limit(mk_handle* h, uint64_t limit_ns) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (limit_ns == 0) return fail(h, MK_ERR_INVALID_ARG, "wait limit must be positive");
+  h->wait_limit_ns = limit_ns;
+  return MK_OK;
+}
+
 const char* mk_last_error(const mk_handle* h) { return h ? h->err.c_str() : ""; }
 
 mk_status mk_get_info(const mk_handle* h, mk_info* out) {
@@ -1292,6 +1301,18 @@ static __device__ __align__(256) unsigned char g_static_scratch[MK_STATIC_SCRATC
 
 std::mutex g_static_mu;
 void* g_static_addr[kMaxStaticDevices] = {};
+
+// The RoPE table the last call on each device wrote into the static array: where, for which shape. A call
+// whose table would be identical and sits at the same offset skips the rewrite (nothing else a call writes
+// can overlap it then: every buffer carved before it ends below it, and every buffer carved after it
+// starts above it); any other call rewrites its own table and becomes the record.
+struct StaticRope {
+  bool valid = false;
+  size_t offset = 0;
+  int max_ctx = 0, rot_dim = 0;
+  float theta = 0.f;
+};
+StaticRope g_static_rope[kMaxStaticDevices];
 
 // Device address of the static array on `device`, which must be current. Resolved once per device.
 mk_status static_scratch_address(int device, void** out) {
@@ -1431,9 +1452,26 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
     fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
     return MK_ERR_CUDA;
   }
-  if (tmp.rot_dim && (e = rope_table_launch(tmp.rope, D.max_ctx, tmp.rot_dim, (double)D.rope_theta, s)) != cudaSuccess) {
-    fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
-    return MK_ERR_CUDA;
+  if (tmp.rot_dim) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    StaticRope& rec = g_static_rope[tmp.device];
+    const bool same = rec.valid && rec.offset == o_rope && rec.max_ctx == D.max_ctx && rec.rot_dim == tmp.rot_dim &&
+                      rec.theta == D.rope_theta;
+    if (!same) {
+      rec.valid = false;
+      if ((e = rope_table_launch(tmp.rope, D.max_ctx, tmp.rot_dim, (double)D.rope_theta, s)) != cudaSuccess) {
+        fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+      }
+      rec.valid = true;
+      rec.offset = o_rope;
+      rec.max_ctx = D.max_ctx;
+      rec.rot_dim = tmp.rot_dim;
+      rec.theta = D.rope_theta;
+    }
+  } else {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    g_static_rope[tmp.device].valid = false;  // this call's buffers may cover the recorded table
   }
   st = launch_program(&tmp, &prog, tokens, rows, positions, batch, rows, logits_out, argmax_out, false, s);
   state->epoch = tmp.epoch;

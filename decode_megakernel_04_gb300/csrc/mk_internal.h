@@ -133,7 +133,8 @@ struct KParams {
   uint32_t* counters;       // [n_ops] completed instructions per op in this launch
   int32_t* status;
   int32_t* abort_flag;
-  unsigned long long timeout_ns;
+  unsigned long long timeout_ns;  // limit of every inter-SM / ring wait
+  uint32_t spin_mask;             // polls between clock reads, minus one (63, or 0 for limits below 1 ms)
   int32_t n_ops;
   int32_t n_sm;
   // step inputs

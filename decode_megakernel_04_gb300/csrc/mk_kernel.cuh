@@ -119,9 +119,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 struct Spin {
   unsigned long long t0 = 0;
   uint32_t n = 0;
-  // false = give up (abort raised elsewhere, or this wait timed out and raised it)
+  // false = give up (abort raised elsewhere, or this wait timed out and raised it). The clock and the abort
+  // flag are read every 64 polls, or on every poll when the limit is below a millisecond (spin_mask 0).
   __device__ __forceinline__ bool ok(const KParams& p) {
-    if ((++n & 63u) != 0u) return true;
+    if ((++n & p.spin_mask) != 0u) return true;
     if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) return false;
     const unsigned long long now = global_timer();
     if (t0 == 0) {

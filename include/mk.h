@@ -139,7 +139,10 @@ typedef struct mk_info {
  * latent caches, the recurrent states, activation scratch, instruction queues, counters and the
  * status word. Synchronous. Errors: MK_ERR_INVALID_ARG (inconsistent shape, missing weight,
  * alignment: every weight must be 16-byte aligned and every inner dimension a multiple of 8),
- * MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA. */
+ * MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA.
+ * Passage: the pages define no API for the kernel (their interface is a CLI and an HTTP server); this
+ * call holds what their kernel receives as arguments: the model's shapes and every weight as a raw
+ * reference into HBM (Kimi K3's TPU megakernel, "How it maps onto a TPU v7"). */
 mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int device, mk_handle** out);
 
 /* Fills the caches and recurrent states of sequences 0..batch-1 from a context of n_tokens tokens
@@ -147,7 +150,10 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
  * sequence has n_tokens committed tokens and the next mk_decode_step must pass positions[b] =
  * n_tokens. Runs ceil(n_tokens / max_rows) launches of the decode kernel with all rows accepted and
  * no LM head. Asynchronous on `stream`; `tokens` must stay valid until the work completes.
- * Errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch, n_tokens outside 1..max_ctx). */
+ * Errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch, n_tokens outside 1..max_ctx).
+ * Passage: the pages define no prefill call; their benchmark decodes after a context of about a thousand
+ * positions (Kimi K3's TPU megakernel, "Acceptance length and batch size"), and this call builds such a
+ * context's caches and states. */
 mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_tokens, void* stream);
 
 /* One decode (rows = 1) or speculative-verify (rows = 2..max_rows) step for `batch` sequences.
@@ -176,14 +182,26 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
 /* The same step from HOST buffers: copies tokens_host [batch*rows] and positions_host [batch] to
  * handle-owned device staging, runs the step, copies the greedy tokens back to argmax_host
  * [batch*rows] (and, when logits_host is not NULL, the logits [batch*rows, vocab]), and waits for
- * `stream`. Returns the device status of the step as mk_get_status would. */
+ * `stream`. Returns the device status of the step as mk_get_status would.
+ * Passage: none; the pages define no API. This is the end-to-end form of mk_decode_step (inputs and the
+ * greedy tokens cross the host boundary every step). */
 mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const int32_t* positions_host,
                               int batch, int rows, float* logits_host, int32_t* argmax_host, void* stream);
 
 /* Waits for `stream`, returns the device status word of the work enqueued so far and clears it.
  * After MK_ERR_TIMEOUT the handle's inter-SM counters are reset so it can be used again (the state
- * of the interrupted step is undefined: run mk_prefill_kv again). */
+ * of the interrupted step is undefined: run mk_prefill_kv again).
+ * Passage: none; the pages define no API and no error reporting for their kernel. */
 mk_status mk_get_status(mk_handle* h, void* stream);
+
+/* Sets the time limit, in nanoseconds, of every wait inside the kernel (an inter-SM dependency counter,
+ * a ring slot, a copy in flight); the default is 2 s. A wait that runs past it records MK_ERR_TIMEOUT in
+ * the status word and raises the abort flag: every CTA gives up at its next wait, lets its copies in flight
+ * land, and returns, so the context stays usable; mk_get_status reports the error and resets the handle's
+ * counters. Takes effect at the next launch. Below 1 ms the waits also read the clock on every poll
+ * instead of every 64th (what a test of the watchdog uses). Errors: MK_ERR_INVALID_ARG (limit 0).
+ * Passage: none; the pages' TPU program has no inter-core waits to bound. */
+mk_status mk_set_wait_limit(mk_handle* h, uint64_t limit_ns);
 
 /* Makes sequence `dst` a copy of sequence `src` (both in 0..max_batch-1): its KV / latent caches,
  * recurrent states, pending verify rows and committed / pending counts, so that dst continues exactly as
@@ -232,13 +250,15 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm
  * next launch. Errors: MK_ERR_INVALID_ARG (no MoE layer in the model, misaligned pointer). */
 mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log);
 
-/* Human-readable description of the last error on this handle ("" if none). Owned by the handle. */
+/* Human-readable description of the last error on this handle ("" if none). Owned by the handle.
+ * Passage: none; the pages define no API. */
 const char* mk_last_error(const mk_handle* h);
 
-/* Fills `out`. */
+/* Fills `out`. Passage: none; the pages define no API. */
 mk_status mk_get_info(const mk_handle* h, mk_info* out);
 
-/* Synchronises the device, frees everything the handle owns. NULL is ignored. */
+/* Synchronises the device, frees everything the handle owns. NULL is ignored.
+ * Passage: none; the pages define no API. */
 void mk_destroy(mk_handle* h);
 
 /* ---- A decode step that allocates no device memory ---------------------------------------------

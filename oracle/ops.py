@@ -114,16 +114,15 @@ def gqa_block_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, p0: int) ->
     hkv = K.shape[1]
     T = p0 + R
     kv_of = (np.arange(hq) * hkv) // hq
-    Kh = np.transpose(K[:T], (1, 0, 2))[kv_of]          # [Hq, T, hd]
-    Vh = np.transpose(V[:T], (1, 0, 2))[kv_of]
-    qh = np.transpose(q, (1, 0, 2))                        # [Hq, R, hd]
-    scores = qh @ np.transpose(Kh, (0, 2, 1)) / np.sqrt(hd)  # [Hq, R, T]
-    t = np.arange(T)[None, :]
-    r = np.arange(R)[:, None]
-    mask = t <= (p0 + r)
-    scores = np.where(mask[None], scores, -np.inf)
-    o = softmax_attend(scores, Vh)                         # [Hq, R, hd]
-    return np.transpose(o, (1, 0, 2))
+    mask = np.arange(T)[None, :] <= (p0 + np.arange(R))[:, None]   # [R, T]
+    o = np.empty((R, hq, hd))
+    for g in range(hkv):
+        heads = np.nonzero(kv_of == g)[0]                  # the query heads that read kv head g
+        Kg, Vg = K[:T, g], V[:T, g]                        # [T, hd]
+        scores = np.transpose(q[:, heads], (1, 0, 2)) @ Kg.T / np.sqrt(hd)   # [heads, R, T]
+        scores = np.where(mask[None], scores, -np.inf)
+        o[:, heads] = np.transpose(softmax_attend(scores, Vg), (1, 0, 2))
+    return o
 
 
 # ----------------------------------------------------------------------------------------------

@@ -79,11 +79,66 @@ def compare_logits(gpu: np.ndarray, ref: np.ndarray, tol: float, rep: Report, wh
                 rep.errors.append(f"{what} row {idx}: greedy {g_arg[idx]} vs oracle {o_arg[idx]} (gap {gap[idx]:.3g})")
 
 
+def oracle_prefill_blocks(orc, ctx: np.ndarray, block: int):
+    """The oracle's prefill of ctx [B, T] run as consecutive blocks of `block` rows, each committed by the
+    next call's positions (the same step semantics as one T-row block, with bounded memory)."""
+    orc.reset()
+    B, T = ctx.shape
+    for c0 in range(0, T, block):
+        orc.step(ctx[:, c0:c0 + block], np.full(B, c0, dtype=np.int64))
+    orc.commit(T - (T - 1) // block * block)
+
+
+def oracle_fork(orc1, B: int):
+    """A batch-B oracle whose every sequence is a copy of sequence 0 of `orc1` (caches, states, counts):
+    the oracle-side counterpart of mk_fork_sequence. Plain array copies; the weights are shared."""
+    o = Oracle(orc1.cfg, orc1.w, B, orc1.max_ctx)
+    o.c[:] = orc1.c[0]
+    o.u[:] = orc1.u[0]
+    for i, (K, V) in orc1.kv.items():
+        o.kv[i] = (np.repeat(K[:1], B, axis=0), np.repeat(V[:1], B, axis=0))
+    for i, lat in orc1.lat.items():
+        o.lat[i] = np.repeat(lat[:1], B, axis=0)
+    for i, S in orc1.S.items():
+        o.S[i] = np.repeat(S[:1], B, axis=0)
+        o.snaps[i] = [orc1.snaps[i][0].copy() for _ in range(B)]
+    return o
+
+
+def attention_ring_chunks(mk, B: int, R: int, T: int) -> list:
+    """For every attention op of the (B, R) program on this device: how many weight-ring chunks one
+    attention instruction streams at context T (positions per chunk instruction / positions per ring
+    chunk). What the long-context tests assert: the multi-chunk online-softmax loop really runs."""
+    from decode_megakernel_04_gb300 import binding
+    n_sm = mk.info().n_sm
+    ops, _ = binding.plan(mk.desc, mk.wtab, n_sm, B, R)
+    out = []
+    for op in ops:
+        if op["type"] == 3:      # GQA attention: K and V of P positions per 32 KB chunk
+            P = 32768 // (4 * op["head_dim"])
+        elif op["type"] == 6:    # MLA attention: 576-wide bf16 latents
+            P = 32768 // (2 * 576)
+        else:
+            continue
+        per_instr = -(-T // op["nchunk"])
+        out.append(-(-per_instr // P))
+    return out
+
+
+# long-context oracle prefills (one sequence), kept for the other batch sizes of the same model and context
+_PREFILLED: dict = {}
+
+
 def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_verify: int = 8,
-             seed: int = 0, tol: float = 2e-2, max_ctx: int | None = None, check_argmax: bool = True):
+             seed: int = 0, tol: float = 2e-2, max_ctx: int | None = None, check_argmax: bool = True,
+             fork: bool = False, oracle_block: int | None = None, min_ring_chunks: int = 0):
     """Prefill T context tokens per sequence, then `decode_steps` greedy single-row steps, then one
     R_verify-row verify step per entry of verify_accepts (the entry is the accepted length of that block,
-    applied by the next call's positions)."""
+    applied by the next call's positions).
+    fork: one context is prefilled for sequence 0 and copied to the others (mk_fork_sequence on the GPU,
+    array copies in the oracle); the steps then give every sequence its own tokens.
+    oracle_block: the oracle prefills in blocks of this many rows (long contexts).
+    min_ring_chunks: assert that every attention instruction streams at least this many ring chunks."""
     from decode_megakernel_04_gb300 import Megakernel
 
     dev = torch.device("cuda")
@@ -92,16 +147,35 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
     extra = decode_steps + (len(verify_accepts) + 1) * R_verify + 8
     max_ctx = max_ctx or (T + extra)
     mk = Megakernel(cfg, w, max_batch=B, max_rows=max(rows_max, 8), max_ctx=max_ctx)
-    orc = Oracle(cfg, w, B, max_ctx)
     rep = Report()
-    ctx = make_tokens(seed, "ctx", (B, T), cfg.vocab, device=dev).contiguous()
+    if min_ring_chunks:
+        for R_ in ([1] if decode_steps or not verify_accepts else []) + ([R_verify] if verify_accepts else []):
+            chunks = attention_ring_chunks(mk, B, R_, T)
+            assert chunks and min(chunks) >= min_ring_chunks, f"rows {R_}: ring chunks per instruction {chunks}"
+    Bc = 1 if fork else B
+    ctx = make_tokens(seed, "ctx", (Bc, T), cfg.vocab, device=dev).contiguous()
     log = None
     if cfg.ffn == "moe":
         log = torch.full((cfg.n_layers, B, max_ctx, cfg.top_k), -1, dtype=torch.int32, device=dev)
         mk.set_routing_log(log)
     mk.prefill(ctx)
-    orc.prefill(ctx.cpu().numpy())
-    check_routing(orc, log, np.zeros(B, dtype=np.int64), T, rep, "prefill")
+    for b in range(1, B if fork else 1):
+        mk.fork(0, b)
+    key = (cfg, T, seed, max_ctx, oracle_block)
+    if fork and oracle_block and key in _PREFILLED:
+        orc = _PREFILLED[key]
+    else:
+        orc = Oracle(cfg, w, Bc, max_ctx)
+        if oracle_block:
+            oracle_prefill_blocks(orc, ctx.cpu().numpy(), oracle_block)
+        else:
+            orc.prefill(ctx.cpu().numpy())
+        if not oracle_block:
+            check_routing(orc, log, np.zeros(Bc, dtype=np.int64), T, rep, "prefill")
+        if fork and oracle_block:
+            _PREFILLED[key] = orc
+    if fork:
+        orc = oracle_fork(orc, B)   # copies: the cached prefill stays untouched
     pos = np.full(B, T, dtype=np.int64)
     tok = make_tokens(seed, "start", (B, 1), cfg.vocab).numpy().astype(np.int64)
     V = cfg.vocab

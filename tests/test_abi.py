@@ -85,6 +85,7 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.mk_decode_step(None, None, None, 1, 1, None, None, None) == 1
     assert lib.mk_prefill_kv(None, None, 1, 1, None) == 1
     assert lib.mk_get_status(None, None) == 1
+    assert lib.mk_set_wait_limit(None, 1) == 1
     # an inconsistent description is rejected by the host checks (no device touched)
     d = binding.ModelDesc()
     d.n_layers = 0

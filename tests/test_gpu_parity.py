@@ -209,3 +209,38 @@ def test_hybrid_batch4_decode():
     cfg = config("hybrid_gdn_gqa", n_layers=4)
     rep = run_case(cfg, B=4, T=20, decode_steps=2, tol=TOL_BF16)
     _check(rep)
+
+
+def test_watchdog_timeout_then_recovery():
+    """The kernel's wait limit set to 1 ns: the first dependency or ring wait that polls twice runs out, the
+    step stops with MK_ERR_TIMEOUT in the status word (no trap, no fault, every CTA returns after its
+    copies in flight land), mk_get_status reports it and resets the counters, and the same handle then runs
+    a fresh prefill and a step that equal a new handle's bit for bit."""
+    from decode_megakernel_04_gb300 import Megakernel
+    from decode_megakernel_04_gb300.binding import MK_ERR_TIMEOUT
+    cfg = config("hybrid_gdn_gqa", n_layers=4, d_model=512, ffn_dim=1024, vocab=4096)
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=2, device=dev)
+    ctx = make_tokens(2, "ctx", (2, 24), cfg.vocab, device=dev)
+    tok = torch.tensor([[7], [9]], dtype=torch.int32, device=dev)
+    pos = torch.tensor([24, 24], dtype=torch.int32, device=dev)
+    mk = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64)
+    mk.prefill(ctx)
+    assert mk.status() == 0
+    mk.set_wait_limit(1)
+    logits = torch.empty((2, cfg.vocab), device=dev)
+    mk.step(tok, pos, logits)
+    assert mk.status() == MK_ERR_TIMEOUT
+    assert mk.status() == 0          # reported once, then cleared
+    mk.set_wait_limit(2_000_000_000)
+    mk.prefill(ctx)
+    mk.step(tok, pos, logits)
+    assert mk.status() == 0
+    ref = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64)
+    ref.prefill(ctx)
+    want = torch.empty_like(logits)
+    ref.step(tok, pos, want)
+    assert ref.status() == 0
+    assert torch.equal(logits, want)
+    mk.close()
+    ref.close()

@@ -19,13 +19,54 @@ TOL = 2e-2  # the bf16-path tolerance of the parity tests
 
 
 def _state_buffers(cfg, desc, dev):
-    """Zero-filled persistent buffers sized as include/mk.h describes (GQA-only model)."""
+    """Zero-filled persistent buffers sized as include/mk.h describes: the KV cache of the GQA layers, the
+    recurrent state and the two halves of the pending-row store of the delta-rule layers, and the
+    per-sequence counts. Returns the tensors (kept alive by the caller) and the StateBuffers record."""
+    from decode_megakernel_04_gb300 import binding
     n_gqa = sum(1 for m in cfg.mixers if m == "gqa")
+    n_lin = sum(1 for m in cfg.mixers if m in ("gdn", "kda"))
+    keep = []
+
+    def zeros(n, dtype):
+        if n == 0:
+            return None
+        t = torch.zeros(n, dtype=dtype, device=dev)
+        keep.append(t)
+        return t.data_ptr()
+
     kv = n_gqa * desc.max_batch * cfg.n_kv_heads * desc.max_ctx * cfg.head_dim
-    kc = torch.zeros(kv, dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros(kv, dtype=torch.bfloat16, device=dev)
-    seq = torch.zeros(desc.max_batch * 4, dtype=torch.int32, device=dev)
-    return (kc, vc, seq)
+    rec = (2 * cfg.lin_dk + cfg.lin_dv + 1 + 3) // 4 * 4
+    state = n_lin * desc.max_batch * cfg.lin_heads * cfg.lin_dv * cfg.lin_dk
+    pending = n_lin * 2 * desc.max_batch * desc.max_rows * cfg.lin_heads * rec
+    sb = binding.StateBuffers(kcache=zeros(kv, torch.bfloat16), vcache=zeros(kv, torch.bfloat16),
+                              state=zeros(state, torch.float32), pending=zeros(pending, torch.float32),
+                              seq=zeros(desc.max_batch * 4, torch.int32), epoch=0)
+    return keep, sb
+
+
+def _compare_calls(lib, mk, sb, cfg, calls, dev):
+    """Runs each (tokens, positions) call through mk_decode_step on the handle and through
+    mk_decode_step_static on the caller's buffers; logits within TOL, greedy tokens equal, and the
+    caller's call counter advanced by one per call."""
+    from decode_megakernel_04_gb300 import binding
+    for i, (toks, pos) in enumerate(calls):
+        toks = toks.contiguous()
+        B, R = toks.shape
+        pos_t = torch.tensor(pos, dtype=torch.int32, device=dev)
+        n = toks.numel()
+        la = torch.empty((n, cfg.vocab), device=dev)
+        aa = torch.empty((n,), dtype=torch.int32, device=dev)
+        mk.step(toks, pos_t, la, aa)
+        assert mk.status() == 0
+        lb = torch.full((n, cfg.vocab), float("nan"), device=dev)
+        ab = torch.full((n,), -1, dtype=torch.int32, device=dev)
+        rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(mk.wtab), C.byref(sb), toks.data_ptr(),
+                                       pos_t.data_ptr(), B, R, lb.data_ptr(), ab.data_ptr(), None)
+        assert rc == 0, binding.STATUS.get(rc, rc)
+        err = float((la - lb).abs().max())
+        assert err <= TOL, (i, err)
+        np.testing.assert_array_equal(aa.cpu().numpy(), ab.cpu().numpy())
+        assert sb.epoch == i + 1
 
 
 def test_static_entry_point_matches_handle_entry_point():
@@ -37,29 +78,33 @@ def test_static_entry_point_matches_handle_entry_point():
     w = make_weights(cfg, seed=4, device=dev)
     B, R, max_ctx = 2, 8, 64
     mk = Megakernel(cfg, w, max_batch=B, max_rows=R, max_ctx=max_ctx)
-    kc, vc, seq = _state_buffers(cfg, mk.desc, dev)
-    sb = binding.StateBuffers(kcache=kc.data_ptr(), vcache=vc.data_ptr(), state=None, pending=None,
-                              seq=seq.data_ptr(), epoch=0)
+    keep, sb = _state_buffers(cfg, mk.desc, dev)
     # two calls in a row: an 8-row block from an empty context, then one row after committing all 8
     calls = [(make_tokens(4, "a", (B, R), cfg.vocab, device=dev), [0, 0]),
              (make_tokens(4, "b", (B, 1), cfg.vocab, device=dev), [R, R])]
-    for toks, pos in calls:
-        toks = toks.contiguous()
-        pos_t = torch.tensor(pos, dtype=torch.int32, device=dev)
-        n = toks.numel()
-        la = torch.empty((n, cfg.vocab), device=dev)
-        aa = torch.empty((n,), dtype=torch.int32, device=dev)
-        mk.step(toks, pos_t, la, aa)
-        assert mk.status() == 0
-        lb = torch.full((n, cfg.vocab), float("nan"), device=dev)
-        ab = torch.full((n,), -1, dtype=torch.int32, device=dev)
-        rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(mk.wtab), C.byref(sb), toks.data_ptr(),
-                                       pos_t.data_ptr(), B, toks.shape[1], lb.data_ptr(), ab.data_ptr(), None)
-        assert rc == 0, binding.STATUS.get(rc, rc)
-        err = float((la - lb).abs().max())
-        assert err <= TOL, err
-        np.testing.assert_array_equal(aa.cpu().numpy(), ab.cpu().numpy())
-    assert sb.epoch == 2
+    _compare_calls(lib, mk, sb, cfg, calls, dev)
+    mk.close()
+
+
+def test_static_entry_point_hybrid_state_and_pending_rows():
+    """A gated-delta-net + GQA stack, where the step also depends on the caller's recurrent state and on
+    its pending-row store (which half a call reads and writes follows the caller's call counter): 8-row
+    verify blocks with partial acceptance and single rows in between, every call equal to the handle's."""
+    from decode_megakernel_04_gb300 import Megakernel, _build, binding
+    _build.build()
+    lib = binding.load()
+    cfg = config("hybrid_gdn_gqa", n_layers=4, d_model=256, ffn_dim=512, vocab=2048, n_q_heads=4, n_kv_heads=2,
+                 head_dim=64, lin_heads=4, lin_dk=64, lin_dv=32)
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=6, device=dev)
+    B, R, max_ctx = 2, 8, 64
+    mk = Megakernel(cfg, w, max_batch=B, max_rows=R, max_ctx=max_ctx)
+    keep, sb = _state_buffers(cfg, mk.desc, dev)
+    calls = [(make_tokens(6, "a", (B, R), cfg.vocab, device=dev), [0, 0]),      # verify block from empty
+             (make_tokens(6, "b", (B, 1), cfg.vocab, device=dev), [3, 5]),      # accept 3 and 5 of its rows
+             (make_tokens(6, "c", (B, R), cfg.vocab, device=dev), [4, 6]),      # another block
+             (make_tokens(6, "d", (B, 1), cfg.vocab, device=dev), [12, 8])]     # accept 8 and 2
+    _compare_calls(lib, mk, sb, cfg, calls, dev)
     mk.close()
 
 
@@ -75,9 +120,7 @@ def test_static_entry_point_rejects_oversized_step():
     dev = torch.device("cuda")
     w = make_weights(cfg, seed=0, device=dev)
     mk = Megakernel(cfg, w, max_batch=1, max_rows=8, max_ctx=32)
-    kc, vc, seq = _state_buffers(cfg, mk.desc, dev)
-    sb = binding.StateBuffers(kcache=kc.data_ptr(), vcache=vc.data_ptr(), state=None, pending=None,
-                              seq=seq.data_ptr(), epoch=0)
+    keep, sb = _state_buffers(cfg, mk.desc, dev)
     toks = torch.zeros((1, 8), dtype=torch.int32, device=dev)
     pos = torch.zeros((1,), dtype=torch.int32, device=dev)
     lg = torch.empty((8, cfg.vocab), device=dev)
