@@ -72,7 +72,8 @@ class StateBuffers(C.Structure):
 
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
            "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log",
-           "mk_fork_sequence", "mk_plan", "mk_set_wait_limit"]
+           "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
+           "mk_set_routing_override"]
 
 _lib = None
 
@@ -103,13 +104,15 @@ def load(path: str | None = None) -> C.CDLL:
     lib.mk_set_routing_log.argtypes = [_P, _P]
     lib.mk_fork_sequence.argtypes = [_P, C.c_int, C.c_int, _P]
     lib.mk_set_wait_limit.argtypes = [_P, C.c_uint64]
+    lib.mk_set_routing_override.argtypes = [_P, _P]
     lib.mk_plan.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, C.c_int,
                             C.POINTER(PlanOp), C.c_int, C.POINTER(C.c_int), C.POINTER(PlanInstr), C.c_int,
                             C.POINTER(C.c_int)]
     lib.mk_decode_step_static.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.POINTER(StateBuffers),
                                           _P, _P, C.c_int, C.c_int, _P, _P, _P]
     for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
-              "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence", "mk_plan", "mk_set_wait_limit"):
+              "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
+              "mk_set_routing_override"):
         getattr(lib, f).restype = C.c_int
     if path is None:
         _lib = lib
@@ -238,6 +241,12 @@ class Megakernel:
         top_k], kept alive by this object while set); None turns the log off."""
         self._route_log = log
         self._check(self.lib.mk_set_routing_log(self.h, None if log is None else log.data_ptr()))
+
+    def set_routing_override(self, ids=None):
+        """Make MoE rows use the expert ids in ``ids`` (device int32, the routing log's layout; rows whose
+        first id is < 0 use their own picks), kept alive by this object while set; None turns it off."""
+        self._route_force = ids
+        self._check(self.lib.mk_set_routing_override(self.h, None if ids is None else ids.data_ptr()))
 
     def set_wait_limit(self, limit_ns: int):
         """Time limit of every wait inside the kernel (default 2 s); see mk_set_wait_limit."""

@@ -1,6 +1,7 @@
 // Host side of libmk: the C ABI (include/mk.h), the device memory plan of a handle, and the scheduler
 // that compiles one decode step of the layer stack into per-SM instruction queues for the persistent
 // kernel (mk_kernel.cuh, built as mk_kernel_dense.cu and mk_kernel_full.cu).
+#include <cuda.h>  // CUtensorMap and the tensor-map encoder's types (the function comes from the runtime)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -48,8 +49,10 @@ struct Program {
   OpDesc* d_ops = nullptr;
   Instr* d_instr = nullptr;
   int32_t* d_qoff = nullptr;
+  TmaDesc* d_tmaps = nullptr;  // tensor maps of the tcgen05 GEMV ops
   int n_ops = 0;
   int n_instr = 0;
+  int n_tmaps = 0;
 };
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -101,6 +104,7 @@ struct mk_handle {
   float* hexp = nullptr;
   size_t hexp_floats = 0;
   int32_t* route_log = nullptr;  // caller's device buffer (mk_set_routing_log) or NULL
+  const int32_t* route_force = nullptr;  // caller's device buffer (mk_set_routing_override) or NULL
   uint32_t* counters = nullptr;
   int32_t* status = nullptr;
   int32_t* abort_flag = nullptr;
@@ -362,12 +366,33 @@ OpDesc blank(int type) {
 // part to x (the last one also writes the RMS partials of the new x).
 constexpr int kMmaSlice = 1024;  // 64 k-steps of 16; 16 rows x (1024 * 2 + 16) bytes fit one slot
 
+// 5 to 64 rows take the tcgen05 path when every matrix but the last has a multiple of 8 rows (its row blocks are
+// cut in 8-row units: one TMA box height per segment); one instruction per SM over a balanced run of 8-row units.
+bool tc_eligible(const OpDesc& d, int N) {
+  if (N <= 4 || N > kMaxN || d.K % 8 != 0 || d.K < 64) return false;
+  for (int m = 0; m + 1 < d.n_mat; ++m)
+    if (d.mat_rows[m] % 8 != 0) return false;
+  return true;
+}
+
 void gemv_op(Builder& bld, OpDesc d, int N) {
   d.type = OP_GEMV;
   d.rg = (N <= 4) ? 16 : 8;
   d.passes = (N <= 8) ? 1 : (N + 7) / 8;
   d.ldw = d.K;
   d.k_begin = 0;
+  if (tc_eligible(d, N)) {
+    d.mma = 2;
+    d.ncols = round_up(2 * N, 16);
+    d.kc = 64 * (256 / d.ncols);  // inputs per K part
+    const int op = bld.add(d);
+    const int units = (d.rows + 7) / 8;
+    for (int s = 0; s < bld.n_sm; ++s) {
+      const int u0 = (int)((int64_t)units * s / bld.n_sm), u1 = (int)((int64_t)units * (s + 1) / bld.n_sm);
+      bld.place(op, s, std::min(8 * u0, d.rows), std::min(8 * u1, d.rows), 0);
+    }
+    return;
+  }
   // a residual-add instruction also keeps its slice of x (N x its rows) in the staging area
   const int64_t xrows = d.out_kind == OUT_RESID ? (d.rows + bld.n_sm - 1) / bld.n_sm : 0;
   const int64_t cap = kActBytes / 4 - 8;  // floats
@@ -624,7 +649,61 @@ struct HostProgram {
   std::vector<OpDesc> ops;
   std::vector<Instr> flat;
   std::vector<int32_t> qoff;
+  std::vector<TmaDesc> tmaps;  // filled by encode_tmaps (needs the driver), not by construct_program
 };
+
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link against the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tensor maps of the program's tcgen05 GEMV ops: for each op (tm_base = its first map) and each of its weight
+// matrices, 16 maps with box heights 8, 16, .., 128 rows and a 64-input (128-byte) box width, 128-byte swizzle:
+// a box lands in shared memory as the K-major, 128B-swizzled tile tcgen05.mma reads. Heights above the
+// matrix's rows (rounded up to 8) are never used and stay zero. Rows and inputs past the matrix are filled
+// with zeros by the copy.
+mk_status encode_tmaps(mk_handle* h, HostProgram& hp) {
+  hp.tmaps.clear();
+  for (OpDesc& o : hp.ops) {
+    if (o.type != OP_GEMV || o.mma != 2) continue;
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return fail(h, MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    o.tm_base = (int)hp.tmaps.size();
+    for (int m = 0; m < o.n_mat; ++m) {
+      for (int hb = 1; hb <= 16; ++hb) {
+        TmaDesc d;
+        std::memset(&d, 0, sizeof(d));
+        if (8 * hb <= round_up(o.mat_rows[m], 8)) {
+          const cuuint64_t dims[2] = {(cuuint64_t)o.ldw, (cuuint64_t)o.mat_rows[m]};
+          const cuuint64_t strides[1] = {(cuuint64_t)o.ldw * 2};
+          const cuuint32_t box[2] = {64, (cuuint32_t)(8 * hb)};
+          const cuuint32_t es[2] = {1, 1};
+          const CUresult r = enc(reinterpret_cast<CUtensorMap*>(&d), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t*>(o.w[m]), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          if (r != CUDA_SUCCESS)
+            return fail(h, MK_ERR_CUDA, "tensor map of a %d x %d weight matrix (box 64 x %d): error %d", o.mat_rows[m],
+                        o.ldw, 8 * hb, (int)r);
+        }
+        hp.tmaps.push_back(d);
+      }
+    }
+  }
+  return MK_OK;
+}
 
 mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& hp) {
   const mk_model_desc& D = h->desc;
@@ -823,6 +902,7 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
   HostProgram hp;
   *st = construct_program(h, B, R, head, hp);
   if (*st != MK_OK) return prog;
+  if ((*st = encode_tmaps(h, hp)) != MK_OK) return prog;
   const std::vector<Instr>& flat = hp.flat;
   const std::vector<int32_t>& qoff = hp.qoff;
   prog.n_ops = (int)hp.ops.size();
@@ -842,6 +922,16 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     return prog;
   }
   h->bytes += (int64_t)(sizeof(OpDesc) * prog.n_ops + sizeof(Instr) * prog.n_instr + sizeof(int32_t) * (h->n_sm + 1));
+  prog.n_tmaps = (int)hp.tmaps.size();
+  if (prog.n_tmaps) {
+    if ((e = cudaMalloc(&prog.d_tmaps, sizeof(TmaDesc) * prog.n_tmaps)) != cudaSuccess ||
+        (e = cudaMemcpy(prog.d_tmaps, hp.tmaps.data(), sizeof(TmaDesc) * prog.n_tmaps, cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+      *st = cuda_fail(h, e, "tensor map upload");
+      return prog;
+    }
+    h->bytes += (int64_t)(sizeof(TmaDesc) * prog.n_tmaps);
+  }
   return prog;
 }
 
@@ -854,6 +944,7 @@ Program* get_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     cudaFree(p.d_ops);
     cudaFree(p.d_instr);
     cudaFree(p.d_qoff);
+    cudaFree(p.d_tmaps);
     return nullptr;
   }
   h->programs.push_back(p);
@@ -874,6 +965,8 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.status = h->status;
   p.abort_flag = h->abort_flag;
   p.timeout_ns = h->wait_limit_ns;
+  p.tmaps = prog->d_tmaps;
+  p.use_tc = prog->n_tmaps > 0 ? 1 : 0;
   p.spin_mask = h->wait_limit_ns < 1000000ull ? 0u : 63u;
   p.n_ops = prog->n_ops;
   p.n_sm = h->n_sm;
@@ -910,6 +1003,7 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.union_list = h->union_list;
   p.hexp = h->hexp;
   p.route_log = h->route_log;
+  p.route_force = h->route_force;
   p.seq = h->seq;
   p.rope = h->rope;
   p.rot_dim = h->rot_dim;
@@ -1236,6 +1330,15 @@ mk_status mk_set_wait_limit(mk_handle* h, uint64_t limit_ns) {
   return MK_OK;
 }
 
+mk_status mk_set_routing_override(mk_handle* h, const int32_t* device_ids) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (device_ids && h->desc.ffn_kind != MK_FFN_MOE) return fail(h, MK_ERR_INVALID_ARG, "the model has no MoE layers");
+  if (device_ids && (reinterpret_cast<uintptr_t>(device_ids) & 3u))
+    return fail(h, MK_ERR_INVALID_ARG, "routing override must be 4-byte aligned");
+  h->route_force = device_ids;
+  return MK_OK;
+}
+
 const char* mk_last_error(const mk_handle* h) { return h ? h->err.c_str() : ""; }
 
 mk_status mk_get_info(const mk_handle* h, mk_info* out) {
@@ -1280,6 +1383,7 @@ void mk_destroy(mk_handle* h) {
     cudaFree(p.d_ops);
     cudaFree(p.d_instr);
     cudaFree(p.d_qoff);
+    cudaFree(p.d_tmaps);
   }
   for (void* p : h->allocs) cudaFree(p);
   delete h;
@@ -1419,9 +1523,14 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
     fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
     return st;
   }
+  if ((st = encode_tmaps(&tmp, hp)) != MK_OK) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
+    return st;
+  }
   const size_t o_ops = carve(off, sizeof(OpDesc) * hp.ops.size());
   const size_t o_instr = carve(off, sizeof(Instr) * hp.flat.size());
   const size_t o_qoff = carve(off, sizeof(int32_t) * hp.qoff.size());
+  const size_t o_tmaps = carve(off, sizeof(TmaDesc) * hp.tmaps.size());
   if (off > (size_t)MK_STATIC_SCRATCH_BYTES) {
     fprintf(stderr,
             "mk_decode_step_static: this step needs %zu bytes of working memory, more than the %u-byte static "
@@ -1438,8 +1547,15 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   prog.d_qoff = reinterpret_cast<int32_t*>(base + o_qoff);
   prog.n_ops = (int)hp.ops.size();
   prog.n_instr = (int)hp.flat.size();
+  prog.n_tmaps = (int)hp.tmaps.size();
+  prog.d_tmaps = prog.n_tmaps ? reinterpret_cast<TmaDesc*>(base + o_tmaps) : nullptr;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (prog.n_tmaps && (e = cudaMemcpyAsync(prog.d_tmaps, hp.tmaps.data(), sizeof(TmaDesc) * hp.tmaps.size(),
+                                           cudaMemcpyHostToDevice, s)) != cudaSuccess) {
+    fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
+    return MK_ERR_CUDA;
+  }
   if ((e = cudaMemcpyAsync(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * hp.ops.size(), cudaMemcpyHostToDevice, s)) !=
           cudaSuccess ||
       (e = cudaMemcpyAsync(prog.d_instr, hp.flat.data(), sizeof(Instr) * hp.flat.size(), cudaMemcpyHostToDevice,

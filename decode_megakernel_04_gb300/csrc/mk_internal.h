@@ -67,7 +67,11 @@ struct OpDesc {
   int32_t ldw;              // elements between weight rows (the full input width)
   int32_t k_begin;          // first input column of this op (an op may cover a K range of the matrix)
   int32_t staged;           // 1: input rows staged in shared memory (fp32) for the whole instruction
-  int32_t mma;              // 1: tensor-core path (inputs staged as bf16 hi/lo pairs, padded weight rows)
+  int32_t mma;              // tensor cores: 1 = mma.sync (up to 4 rows; inputs staged whole as bf16 hi/lo
+                            // pairs, padded weight rows), 2 = tcgen05 with TMEM accumulators (5 and more rows;
+                            // weight tiles by TMA, inputs staged per K part), 0 = CUDA cores
+  int32_t tm_base;          // mma 2: first tensor map of this op (16 per matrix, box heights 8 .. 128 rows)
+  int32_t ncols;            // mma 2: TMEM columns per accumulator tile = bf16 hi / lo columns, 2 N rounded up to 16
   int32_t kc;               // inputs per weight slice (chunk width)
   int32_t passes;           // ceil(N / 8) when 8 activation rows are processed per pass, else 1
   int32_t n_mat;
@@ -114,6 +118,21 @@ struct OpDesc {
   int32_t aux_stride;
 };
 
+// An opaque TMA tensor map (the driver's CUtensorMap: 128 bytes, 64-byte aligned), encoded on the host.
+struct alignas(64) TmaDesc {
+  uint64_t w[16];
+};
+static_assert(sizeof(TmaDesc) == 128, "tensor map size");
+
+// tcgen05 GEMV geometry: accumulator tiles are 128 TMEM lanes (weight rows) x ncols columns; a row block
+// holds at most 128 physical weight rows (64 logical rows for SwiGLU: the gate and up tiles of the same
+// rows) split into segments at matrix boundaries; K is covered in K parts of 256 / ncols 64-wide atoms
+// (the staged activations of one part fill one 32 KB buffer); each ring chunk holds one row block's
+// weights over a run of atoms (at most 32 KB).
+constexpr int kTcMaxSeg = 4;      // segments (accumulator tiles) per row block
+constexpr int kTcCols = 512;      // TMEM columns allocated per CTA
+constexpr int kTcBBytes = 32768;  // one staged-activation buffer (two are used)
+
 struct Instr {
   int32_t op;
   int32_t a, b, c;
@@ -134,6 +153,8 @@ struct KParams {
   int32_t* status;
   int32_t* abort_flag;
   unsigned long long timeout_ns;  // limit of every inter-SM / ring wait
+  const TmaDesc* tmaps;     // tensor maps of the program's tcgen05 GEMV ops
+  int32_t use_tc;           // the program has tcgen05 ops: allocate TMEM
   uint32_t spin_mask;             // polls between clock reads, minus one (63, or 0 for limits below 1 ms)
   int32_t n_ops;
   int32_t n_sm;
@@ -172,6 +193,7 @@ struct KParams {
   int32_t* union_list;
   float* hexp;              // [n_shared + union][N][F] expert SwiGLU outputs
   int32_t* route_log;       // optional [n_layers][max_batch][max_ctx][top_k] expert ids by position
+  const int32_t* route_force;  // optional, same layout: expert ids a row must use (replay); < 0 = its own
   SeqState* seq;
   const float2* rope;       // [max_ctx][rot_dim / 2] (cos, sin)
   int32_t rot_dim;

@@ -172,6 +172,10 @@ struct CSmem {
   float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
   int32_t uni_c[kMaxExperts + 4];        // MoE: the step's expert union, consumers' copy (count, ids)
   int32_t uni_p[kMaxExperts + 4];        // the producer warp's copy
+  // tcgen05 GEMV: staged-activation buffer ready [2] / free [2], accumulators complete, drain at exit
+  uint64_t tcbar[6];
+  uint32_t tmem_base;
+  uint32_t tmem_pad;
 };
 
 struct Ring {
@@ -183,11 +187,17 @@ struct Ring {
   }
 };
 
-constexpr size_t kCSmemOff = (size_t)kSlots * kSlotBytes + 2 * kSlots * sizeof(uint64_t);
-constexpr size_t kActOff = (kCSmemOff + sizeof(CSmem) + 127) / 128 * 128;
-// ring | barriers | consumer scratch | activation / staging area (GEMV input rows as bf16; the attention
-// block's own K/V rows; the delta rule's row inputs)
-constexpr size_t kSmemBytes = kActOff + kActBytes;
+// ring | activation / staging area (GEMV input rows; the attention block's own K/V rows; the delta rule's
+// row inputs; the tcgen05 GEMV's two staged-activation buffers) | ring barriers | consumer scratch.
+// Ring slots and the staging area start on 1024-byte boundaries (the 128-byte swizzle atom of the
+// tcgen05 operands); an MMA that reads past a short tile at the end of the last slot stays inside the CTA's
+// shared memory (in the staging area).
+constexpr size_t kActOff = (size_t)kSlots * kSlotBytes;
+constexpr size_t kBarOff = kActOff + kActBytes;
+constexpr size_t kCSmemOff = kBarOff + 2 * kSlots * sizeof(uint64_t);
+constexpr size_t kSmemBytes = kCSmemOff + sizeof(CSmem);
+static_assert(kSlotBytes % 1024 == 0 && kActOff % 1024 == 0, "ring slots and staging area must be 1024-byte aligned");
+static_assert(2 * kTcBBytes <= kActBytes, "two staged-activation buffers must fit the staging area");
 // 227 KB per CTA, less the 1 KB of static shared memory the kernel also uses (the 1024-byte alignment of
 // the dynamic array and the launch-state word)
 static_assert(kSmemBytes + 1024 <= 232448, "dynamic shared memory above what a CTA may use");
@@ -526,6 +536,359 @@ __device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr
         for (int i = 0; i < 16; ++i) {
           const float v = cs.sq[i * N + ctid];
           const int ix = cs.best_idx[i * N + ctid];
+          if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
+        }
+        p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(bv, __int_as_float(bi));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core GEMV for 5 to 64 activation rows: tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) with the
+// accumulators in tensor memory (TMEM). The weight rows are the M side of the MMA (128 TMEM lanes), the
+// activations the N side, split into a bf16 "hi" and "lo" column each (hi = bf16(v), lo = bf16(v - hi)) so
+// the product keeps ~16 mantissa bits of the fp32 activations; column 2n + 1 is added to column 2n at the end.
+//   * Weight tiles come from the ring, loaded by the producer warp with TMA (2D tensor maps of each weight
+//     matrix, 64-element boxes with 128-byte swizzle: the canonical K-major layout the MMA reads directly).
+//   * An instruction's rows are cut into row blocks of at most 128 physical rows (64 logical rows of SwiGLU:
+//     its gate and up tiles), each split into segments at matrix boundaries; every segment accumulates in
+//     its own TMEM tile of ncols columns, so one row group (as many blocks as fit 512 columns) keeps all its
+//     accumulators in TMEM across the whole K loop and no cross-warp reduction is needed.
+//   * K is covered in parts of 256 / ncols atoms (64 inputs each); the activations of a part are staged by
+//     warps 1..7 into one of two 32 KB buffers while lane 0 of warp 0 issues the MMAs of the previous part.
+// ------------------------------------------------------------------------------------------------
+struct TcSeg {
+  int m;      // matrix index in the op (SwiGLU: 0 gate, 1 up)
+  int row;    // first row inside that matrix
+  int h;      // rows
+  int out0;   // first output row (physical concatenated row; SwiGLU: logical row)
+};
+struct TcBlock {
+  int nseg;
+  int rows8;  // sum of the segments' box heights (rows rounded up to 8)
+  int atoms;  // 64-input atoms per ring chunk
+  TcSeg seg[kTcMaxSeg];
+};
+
+__device__ __forceinline__ int tc_h8(int h) { return (h + 7) & ~7; }
+
+// the row block that starts at (concatenated / logical) row `start` of an instruction ending at `end`;
+// returns the next block's first row
+__device__ __forceinline__ int tc_block(const OpDesc& op, int start, int end, TcBlock& blk) {
+  if (op.out_kind == OUT_SWIGLU) {
+    const int h = min(64, end - start);
+    blk.nseg = 2;
+    blk.seg[0] = {0, start, h, start};
+    blk.seg[1] = {1, start, h, start};
+    blk.rows8 = 2 * tc_h8(h);
+  } else {
+    int r = start, m = 0, base = 0;
+    while (m < op.n_mat - 1 && r >= base + op.mat_rows[m]) base += op.mat_rows[m++];
+    blk.nseg = 0;
+    blk.rows8 = 0;
+    int left = 128;
+    while (r < end && left > 0 && blk.nseg < kTcMaxSeg) {
+      const int h = min(min(op.mat_rows[m] - (r - base), end - r), left);
+      blk.seg[blk.nseg++] = {m, r - base, h, r};
+      blk.rows8 += tc_h8(h);
+      left -= tc_h8(h);
+      r += h;
+      if (r - base >= op.mat_rows[m] && m < op.n_mat - 1) base += op.mat_rows[m++];
+    }
+    start = r;
+  }
+  blk.atoms = max(1, min(16, 256 / blk.rows8));
+  return op.out_kind == OUT_SWIGLU ? start + blk.seg[0].h : start;
+}
+
+// end of the row group that starts at `start` (as many blocks as fit the TMEM columns)
+__device__ __forceinline__ int tc_group_end(const OpDesc& op, int start, int end) {
+  int cols = 0, r = start;
+  while (r < end) {
+    TcBlock blk;
+    const int nxt = tc_block(op, r, end, blk);
+    if (cols > 0 && cols + blk.nseg * op.ncols > kTcCols) break;
+    cols += blk.nseg * op.ncols;
+    r = nxt;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int tc_atoms(const OpDesc& op) { return (op.K + 63) >> 6; }
+__device__ __forceinline__ int tc_part(const OpDesc& op) { return 256 / op.ncols; }
+
+// ring chunks of one instruction (every consumer thread advances its chunk counter by this)
+__device__ __forceinline__ uint32_t tc_instr_chunks(const OpDesc& op, const Instr& in) {
+  const int nat = tc_atoms(op), KP = tc_part(op);
+  uint32_t n = 0;
+  for (int r = in.a; r < in.b;) {
+    TcBlock blk;
+    r = tc_block(op, r, in.b, blk);
+    for (int a0 = 0; a0 < nat; a0 += KP) {
+      const int a1 = min(nat, a0 + KP);
+      n += (uint32_t)((a1 - a0 + blk.atoms - 1) / blk.atoms);
+    }
+  }
+  return n;
+}
+
+// --- tcgen05 / TMA primitives ---------------------------------------------------------------------
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = ncols
+__device__ __forceinline__ uint32_t umma_idesc(int ncols) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(ncols >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const TmaDesc* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// 8 consecutive fp32 TMEM columns of this warp's 32 lanes
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Activations of atoms [a0, a1) as bf16 hi / lo rows (row 2n = hi of activation row n, 2n + 1 = lo; rows
+// from 2N to ncols are zero) in the swizzled K-major layout: atom a at buf + (a - a0) * ncols * 128, row r at
+// + r * 128, its 16-byte chunk c at + ((c ^ (r & 7)) << 4). Warps 1..7 do this; inputs past K are zero.
+__device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, const CSmem& cs, uint8_t* buf, int a0,
+                                         int a1, int stid, int nthr) {
+  const bool norm = op.in_kind == IN_NORM;
+  const int N = p.N, K = op.K, nc = op.ncols;
+  const int pairs = nc >> 1;                 // activation rows incl. the zero padding
+  const int items = pairs * (a1 - a0) * 8;   // (activation row, atom, 16-byte chunk)
+  for (int it = stid; it < items; it += nthr) {
+    const int c = it & 7, rest = it >> 3;
+    const int a = a0 + rest % (a1 - a0), n = rest / (a1 - a0);
+    const int k = a * 64 + c * 8;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    if (n < N && k < K) {
+      const float* src = norm ? p.x + (size_t)n * p.d + k : op.in + (size_t)n * op.in_stride + k;
+      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
+      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      if (norm) {
+        const uint4 g = __ldg(reinterpret_cast<const uint4*>(op.gain + k));
+        const float s = cs.inv_rms[n];
+        v[0] *= s * bf_lo(g.x); v[1] *= s * bf_hi(g.x); v[2] *= s * bf_lo(g.y); v[3] *= s * bf_hi(g.y);
+        v[4] *= s * bf_lo(g.z); v[5] *= s * bf_hi(g.z); v[6] *= s * bf_lo(g.w); v[7] *= s * bf_hi(g.w);
+      }
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint16_t h0 = f2bf(v[2 * e]), h1 = f2bf(v[2 * e + 1]);
+      const uint16_t l0 = f2bf(v[2 * e] - bf2f(h0)), l1 = f2bf(v[2 * e + 1] - bf2f(h1));
+      hi[e] = h0 | ((uint32_t)h1 << 16);
+      lo[e] = l0 | ((uint32_t)l1 << 16);
+    }
+    uint8_t* atom = buf + (size_t)(a - a0) * nc * 128;
+    const int rh = 2 * n, rl = 2 * n + 1;
+    *reinterpret_cast<uint4*>(atom + rh * 128 + ((c ^ (rh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(atom + rl * 128 + ((c ^ (rl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// per-CTA state of the tcgen05 path: TMEM base, barriers, running counters (uniform over consumer threads)
+struct TcState {
+  uint32_t tmem;
+  uint32_t kp;   // K parts processed since launch (buffer = kp & 1)
+  uint32_t rg;   // row groups completed since launch (accumulator barrier parity)
+};
+
+__device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+                                CSmem& cs, uint8_t* act, TcState& ts, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int sm = blockIdx.x;
+  const int N = p.N, nc = op.ncols;
+  const bool norm = op.in_kind == IN_NORM;
+  const bool swiglu = op.out_kind == OUT_SWIGLU;
+  const int nat = tc_atoms(op), KP = tc_part(op);
+  uint64_t* bready = &cs.tcbar[0];
+  uint64_t* bfree = &cs.tcbar[2];
+  uint64_t* accb = &cs.tcbar[4];
+  float* pred = &cs.red[0][0];                                 // [8 warps][64]: ssq or argmax value partials
+  int32_t* pidx = reinterpret_cast<int32_t*>(cs.mred);         // [8 warps][64]: argmax index partials
+
+  if (norm) {
+    for (int n = warp; n < N; n += kConsumerWarps) {
+      float s = 0.f;
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      s = warp_sum(s);
+      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
+    }
+  }
+  for (int i = ctid; i < kConsumerWarps * 64; i += kConsumerThreads) {
+    pred[i] = op.out_kind == OUT_LOGITS ? -CUDART_INF_F : 0.f;
+    pidx[i] = 0x7fffffff;
+  }
+  consumer_sync();
+
+  const uint32_t idesc = umma_idesc(nc);
+  const uint32_t ring_s = smem_u32(rg.base);
+  uint32_t ck = chunk;  // ring position of the MMA thread
+  for (int g0 = in.a; g0 < in.b;) {
+    const int g1 = tc_group_end(op, g0, in.b);
+    for (int a0 = 0; a0 < nat; a0 += KP) {
+      const int a1 = min(nat, a0 + KP);
+      const uint32_t buf = ts.kp & 1u, use = ts.kp >> 1;
+      uint8_t* bb = act + buf * kTcBBytes;
+      if (warp >= 1) {
+        bool ok = true;
+        if (use > 0) ok = wait_bar(&bfree[buf], (use - 1) & 1u, p);
+        if (ok) tc_stage(p, op, cs, bb, a0, a1, ctid - 32, kConsumerThreads - 32);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&bready[buf]);
+      } else if (lane == 0) {
+        const bool bok = wait_bar(&bready[buf], use & 1u, p);
+        const uint32_t bsa = smem_u32(bb);
+        int col = 0;
+        for (int r = g0; r < g1;) {
+          TcBlock blk;
+          r = tc_block(op, r, g1, blk);
+          for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
+            const int na = min(blk.atoms, a1 - c0);
+            const bool ok = ring_wait_full(rg, ck, p) && bok;
+            tc_fence_after();
+            if (ok) {
+              const uint32_t slot = ring_s + (ck % kSlots) * kSlotBytes;
+              uint32_t soff = 0;
+              for (int s = 0; s < blk.nseg; ++s) {
+                const int h8 = tc_h8(blk.seg[s].h);
+                const uint32_t d = ts.tmem + (uint32_t)(col + s * nc);
+                for (int a = 0; a < na; ++a) {
+                  const uint32_t aa = slot + soff + (uint32_t)(a * h8 * 128);
+                  const uint32_t ba = bsa + (uint32_t)((c0 + a - a0) * nc * 128);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    umma_bf16(d, umma_desc(aa + j * 32), umma_desc(ba + j * 32), idesc,
+                              (c0 + a > 0 || j > 0) ? 1u : 0u);
+                }
+                soff += (uint32_t)(h8 * na * 128);
+              }
+            }
+            // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
+            mbar_arrive_n(&rg.empty[ck % kSlots], kConsumerWarps - 1);
+            umma_commit(&rg.empty[ck % kSlots]);
+            ++ck;
+          }
+          col += blk.nseg * nc;
+        }
+        umma_commit(&bfree[buf]);
+      }
+      ++ts.kp;
+    }
+    if (ctid == 0) umma_commit(accb);
+    wait_bar(accb, ts.rg & 1u, p);
+    ++ts.rg;
+    tc_fence_after();
+
+    // epilogue: warp w reads TMEM lanes 32 (w & 3) .. + 31 (rows of a tile), columns half (w >> 2) of each tile
+    const int q = warp & 3, half = warp >> 2;
+    const int hc = nc >> 1;  // columns per half (hi / lo pairs: hc / 2 activation rows)
+    int col = 0;
+    for (int r = g0; r < g1;) {
+      TcBlock blk;
+      r = tc_block(op, r, g1, blk);
+      const int nout = swiglu ? 1 : blk.nseg;
+      for (int s = 0; s < nout; ++s) {
+        const TcSeg& sg = blk.seg[s];
+        const int i = q * 32 + lane;
+        const bool valid = i < sg.h;
+        const int row = sg.out0 + i;
+        for (int pc = 0; pc < hc; pc += 8) {
+          const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + s * nc + half * hc + pc);
+          float v[8];
+          tmem_ld8(ta, v);
+          float u[8];
+          if (swiglu) tmem_ld8(ta + (uint32_t)nc, u);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int n = (half * hc + pc) / 2 + t;
+            const float val = v[2 * t] + v[2 * t + 1];
+            const bool live = valid && n < N;
+            if (swiglu) {
+              const float up = u[2 * t] + u[2 * t + 1];
+              if (live) op.out[(size_t)n * op.out_stride + row] = val / (1.0f + expf(-val)) * up;
+            } else if (op.out_kind == OUT_STORE) {
+              if (live) op.out[(size_t)n * op.out_stride + row] = val;
+            } else if (op.out_kind == OUT_RESID) {
+              float xn = 0.f;
+              if (live) {
+                xn = __ldcg(p.x + (size_t)n * p.d + row) + val;
+                __stcg(p.x + (size_t)n * p.d + row, xn);
+              }
+              const float s2 = warp_sum(xn * xn);
+              if (lane == 0 && n < N) pred[warp * 64 + n] += s2;
+            } else {  // OUT_LOGITS
+              if (live && p.logits) p.logits[(size_t)n * p.V + row] = val;
+              float bv = live ? val : -CUDART_INF_F;
+              int bi = live ? row : 0x7fffffff;
+#pragma unroll
+              for (int o = 16; o >= 1; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+              }
+              if (lane == 0 && n < N) {
+                const float cv = pred[warp * 64 + n];
+                const int ci = pidx[warp * 64 + n];
+                if (bv > cv || (bv == cv && bi < ci)) { pred[warp * 64 + n] = bv; pidx[warp * 64 + n] = bi; }
+              }
+            }
+          }
+        }
+      }
+      col += blk.nseg * nc;
+    }
+    tc_fence_before();
+    consumer_sync();  // TMEM reads done before the next row group's MMAs overwrite the tiles
+    g0 = g1;
+  }
+  chunk += tc_instr_chunks(op, in);
+
+  if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
+    if (ctid < N) {
+      if (op.out_kind == OUT_RESID) {
+        float s = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) s += pred[w * 64 + ctid];
+        if (op.ssq_out >= 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], s);
+      } else {
+        float bv = -CUDART_INF_F;
+        int bi = 0x7fffffff;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float v = pred[w * 64 + ctid];
+          const int ix = pidx[w * 64 + ctid];
           if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
         }
         p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(bv, __int_as_float(bi));
@@ -1242,6 +1605,14 @@ __device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, f
     }
     float ssum = 0.f;
     float ssel[kMaxTopK];
+    // routing replay: a row with caller-given expert ids uses them (an id outside [0, E) falls back to the
+    // row's own pick); its own picks still go to the routing log
+    const int b_row = n / p.R, pos_row = p.positions[b_row] + n % p.R;
+    const int32_t* frow = nullptr;
+    if (p.route_force) {
+      frow = p.route_force + (((size_t)op.layer * p.max_batch + b_row) * p.max_ctx + pos_row) * K;
+      if (__ldg(frow) < 0) frow = nullptr;
+    }
     for (int k = 0; k < K; ++k) {
       float bv = -CUDART_INF_F;
       int bi = 0x7fffffff;
@@ -1256,24 +1627,25 @@ __device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, f
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j)
+        if (lane + 32 * j == bi) bs[j] = -CUDART_INF_F;  // taken
+      int use = bi;
+      if (frow) {
+        const int f = __ldg(frow + k);
+        if (f >= 0 && f < E) use = f;
+      }
       float s_w = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) {
-        if (lane + 32 * j == bi) {
-          s_w = sc[j];
-          bs[j] = -CUDART_INF_F;  // taken
-        }
-      }
-      s_w = __shfl_sync(0xffffffffu, s_w, bi & 31);
+      for (int j = 0; j < kMaxExperts / 32; ++j)
+        if (lane + 32 * j == use) s_w = sc[j];
+      s_w = __shfl_sync(0xffffffffu, s_w, use & 31);
       ssel[k] = s_w;
       ssum += s_w;
       if (lane == 0) {
-        __stcg(p.route_idx + n * kMaxTopK + k, bi);
-        flags[bi] = 1;
-        if (p.route_log) {
-          const int b = n / p.R, pos = p.positions[b] + n % p.R;
-          p.route_log[(((size_t)op.layer * p.max_batch + b) * p.max_ctx + pos) * K + k] = bi;
-        }
+        __stcg(p.route_idx + n * kMaxTopK + k, use);
+        flags[use] = 1;
+        if (p.route_log) p.route_log[(((size_t)op.layer * p.max_batch + b_row) * p.max_ctx + pos_row) * K + k] = bi;
       }
     }
     if (lane == 0)
@@ -1859,6 +2231,10 @@ struct ChunkCursor {
   int32_t* uni;
   const uint8_t* mw;
   const uint8_t* ms;
+  // tcgen05 GEMV walk: the instruction's row range, current row group, K part, row block and first atom
+  // of the current chunk, its atom count; tma = 1 when the chunk is a set of TMA tile copies
+  int tma, adv, rb, g0, g1, a0, r, rnext, cc, na, nat, KP;
+  TcBlock blk;
 };
 
 __device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& c, int lane) {
@@ -1894,7 +2270,24 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       const OpDesc& op = p.ops[in.op];
       c.op = &op;
       const int type = op.type;
-      if (type == OP_GEMV) {
+      if (type == OP_GEMV && op.mma == 2) {
+        if (in.b <= in.a) {
+          ++c.qi;
+          continue;
+        }
+        c.a = in.a;
+        c.rb = in.b;
+        c.nat = tc_atoms(op);
+        c.KP = tc_part(op);
+        c.g0 = in.a;
+        c.g1 = tc_group_end(op, in.a, in.b);
+        c.a0 = 0;
+        c.r = in.a;
+        c.rnext = tc_block(op, c.r, c.g1, c.blk);
+        c.cc = 0;
+        c.adv = 0;
+        c.kind = 5;
+      } else if (type == OP_GEMV) {
         c.swiglu = op.out_kind == OUT_SWIGLU;
         c.glog = c.swiglu ? op.rg / 2 : op.rg;
         c.a = in.a;
@@ -1960,6 +2353,38 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         ++c.qi;
         continue;
       }
+    }
+    c.tma = 0;
+    if (c.kind == 5) {
+      if (c.adv) {  // step past the chunk returned last time, in the consumer's order: atoms, blocks, parts, groups
+        c.adv = 0;
+        c.cc += c.blk.atoms;
+        if (c.cc >= min(c.nat, c.a0 + c.KP)) {
+          c.r = c.rnext;
+          if (c.r >= c.g1) {
+            c.a0 += c.KP;
+            if (c.a0 >= c.nat) {
+              c.a0 = 0;
+              c.g0 = c.g1;
+              if (c.g0 >= c.rb) {
+                c.kind = 0;
+                ++c.qi;
+                continue;
+              }
+              c.g1 = tc_group_end(*c.op, c.g0, c.rb);
+            }
+            c.r = c.g0;
+          }
+          c.rnext = tc_block(*c.op, c.r, c.g1, c.blk);
+          c.cc = c.a0;
+        }
+      }
+      c.na = min(c.blk.atoms, min(c.nat, c.a0 + c.KP) - c.cc);
+      total = (uint32_t)(c.blk.rows8 * c.na * 128);
+      bytes = 0;
+      c.tma = 1;
+      c.adv = 1;
+      return true;
     }
     if (c.kind == 1) {
       const int kw = min(c.kc, c.K - c.k0);
@@ -2108,7 +2533,22 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
       last_qi = mc.qi;
     }
     if (!ring_acquire(rg, chunk, total, p, lane)) break;
-    if (bytes) bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + dst, src, bytes, &rg.full[chunk % kSlots]);
+    if (mc.tma) {
+      // one 2D TMA box per (segment, atom): segment s's atom a lands at its tile offset in the slot
+      const uint32_t slot = ring_base + (chunk % kSlots) * kSlotBytes;
+      const int na = mc.na, n = mc.blk.nseg * na;
+      for (int idx = lane; idx < n; idx += 32) {
+        const int s = idx / na, a = idx - s * na;
+        uint32_t soff = 0;
+        for (int t = 0; t < s; ++t) soff += (uint32_t)(tc_h8(mc.blk.seg[t].h) * na * 128);
+        const int h8 = tc_h8(mc.blk.seg[s].h);
+        const TmaDesc* map = p.tmaps + mc.op->tm_base + mc.blk.seg[s].m * 16 + (h8 / 8 - 1);
+        tma_load_2d(slot + soff + (uint32_t)(a * h8 * 128), map, (mc.cc + a) * 64, mc.blk.seg[s].row,
+                    &rg.full[chunk % kSlots]);
+      }
+    } else if (bytes) {
+      bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + dst, src, bytes, &rg.full[chunk % kSlots]);
+    }
     ++chunk;
     const void* psrc = nullptr;
     uint32_t pbytes = 0, pdst = 0, ptotal = 0;
@@ -2172,7 +2612,8 @@ __device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, 
   }
 }
 
-__device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16_t* act, int q0, int q1, int ctid) {
+__device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16_t* act, TcState& ts, int q0, int q1,
+                             int ctid) {
   uint32_t chunk = 0;
   float* actf = reinterpret_cast<float*>(act);
   const int nr = p.N <= 1 ? 1 : p.N <= 2 ? 2 : p.N <= 4 ? 4 : 8;
@@ -2195,7 +2636,9 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
     switch (op.type) {
       case OP_EMBED: embed_consume(p, op, in, ctid); break;
       case OP_GEMV:
-        if (op.mma) {
+        if (op.mma == 2) {
+          gemv_tc_consume(p, op, in, rg, chunk, cs, reinterpret_cast<uint8_t*>(act), ts, ctid);
+        } else if (op.mma) {
           gemv_mma_consume(p, op, in, rg, chunk, cs, actf, ctid);
         } else if (op.staged) {
           if (nr == 1) gemv_dispatch<16, 1, true>(p, op, in, rg, chunk, cs, actf, ctid);
@@ -2277,7 +2720,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem[];
   Ring rg;
   rg.base = smem;
-  rg.full = reinterpret_cast<uint64_t*>(smem + (size_t)kSlots * kSlotBytes);
+  rg.full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   rg.empty = rg.full + kSlots;
   CSmem& cs = *reinterpret_cast<CSmem*>(smem + kCSmemOff);
   uint16_t* act = reinterpret_cast<uint16_t*>(smem + kActOff);
@@ -2289,6 +2732,11 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       mbar_init(&rg.full[i], 1);
       mbar_init(&rg.empty[i], kConsumerWarps);
     }
+    if (p.use_tc) {
+      mbar_init(&cs.tcbar[0], kConsumerThreads - 32);  // staged-activation buffer ready: warps 1..7 arrive
+      mbar_init(&cs.tcbar[1], kConsumerThreads - 32);
+      for (int i = 2; i < 6; ++i) mbar_init(&cs.tcbar[i], 1);  // arrivals by tcgen05.commit
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -2296,9 +2744,41 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     if (s_state == 0 && blockIdx.x == 0 && tid == 0) atomicCAS(p.status, 0, kStatusDevice);
     return;
   }
+  // TMEM for the tcgen05 GEMV accumulators: one CTA per SM, so the 512 columns are always free here
+  if (p.use_tc && tid < 32) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&cs.tmem_base)),
+                 "r"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
-  if (tid >= kConsumerThreads) run_producer(p, rg, q0, q1, cs.uni_p);
-  else run_consumer(p, rg, cs, act, q0, q1, tid);
+  if (tid >= kConsumerThreads) {
+    run_producer(p, rg, q0, q1, cs.uni_p);
+  } else {
+    TcState ts;
+    ts.tmem = p.use_tc ? cs.tmem_base : 0u;
+    ts.kp = 0;
+    ts.rg = 0;
+    run_consumer(p, rg, cs, act, ts, q0, q1, tid);
+    if (p.use_tc) {
+      // every MMA this CTA issued has completed (bounded wait, also after an abort), then free the TMEM
+      if (tid == 0) {
+        umma_commit(&cs.tcbar[5]);
+        const unsigned long long t0 = global_timer();
+        while (!mbar_try_wait(&cs.tcbar[5], 0)) {
+          if (global_timer() - t0 > 200000000ull) break;
+        }
+      }
+      tc_fence_before();
+      consumer_sync();
+      tc_fence_after();
+      if (tid < 32)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(cs.tmem_base), "r"(kTcCols) : "memory");
+    }
+  }
 }
 
 }  // namespace MK_VARIANT_NS

@@ -250,6 +250,19 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm
  * next launch. Errors: MK_ERR_INVALID_ARG (no MoE layer in the model, misaligned pointer). */
 mk_status mk_set_routing_log(mk_handle* h, int32_t* device_log);
 
+/* Routing replay for MoE models: with a non-NULL `device_ids` — device int32, the routing log's layout
+ * [n_layers][max_batch][max_ctx][top_k], owned by the caller and kept alive while set — every later step and
+ * prefill makes the row of sequence b at position t of MoE layer l use the experts
+ * device_ids[((l * max_batch + b) * max_ctx + t) * top_k + k], k = 0 .. top_k - 1, instead of the ones its
+ * router picks, whenever the first of them is >= 0 (an id outside [0, n_experts) falls back to the row's own
+ * pick). The weights stay route_scale * s / sum(s) over the sigmoid scores of the experts used. The routing
+ * log (mk_set_routing_log) still records each row's own picks. For reproducing another run's routing
+ * exactly (comparing two implementations expert for expert, or keeping a rollout and its replay on the same
+ * experts); the decode path does not need it. NULL turns it off (the default). Takes effect at the next
+ * launch. Errors: MK_ERR_INVALID_ARG (no MoE layer, misaligned pointer).
+ * Passage: none; the pages' router always uses its own picks. */
+mk_status mk_set_routing_override(mk_handle* h, const int32_t* device_ids);
+
 /* Human-readable description of the last error on this handle ("" if none). Owned by the handle.
  * Passage: none; the pages define no API. */
 const char* mk_last_error(const mk_handle* h);

@@ -54,15 +54,33 @@ def _np(t):
 class Oracle:
     """The decode step of one model for a batch of ``batch`` sequences.
 
-    ``weights`` maps the names drawn by ``synthetic.make_weights`` to tensors or arrays."""
+    ``weights`` maps the names drawn by ``synthetic.make_weights`` to tensors or arrays.
 
-    def __init__(self, cfg, weights: dict, batch: int, max_ctx: int):
+    ``cache_round="bf16"`` stores the cached keys, values and MLA latents rounded to bf16 instead of exactly.
+    The definition keeps them exact; this mode is the pages' statement that the reference computes with a
+    bf16 trunk and bf16 activations (Kimi K3's TPU megakernel, "Is it like for like?"), used where floating
+    point decides an integer: the router's top-k is compared in that precision, because bf16-stored
+    activations move router scores by up to ~1e-3 and flip picks whose scores are that close.
+
+    ``forced_routing`` (a dict layer -> expert ids [B, R, top_k], consumed by the next ``step``) makes the MoE
+    layers use the given experts (weights renormalised over their own sigmoid scores) while ``routing`` still
+    records each row's own picks: how the exact oracle follows the routing decided in the pages' precision."""
+
+    def __init__(self, cfg, weights: dict, batch: int, max_ctx: int, cache_round: str | None = None):
         self.cfg = cfg
         self.B = batch
         self.max_ctx = max_ctx
         self.w = {k: _np(v) for k, v in weights.items()}
         self._dequant_cache: dict = {}
+        assert cache_round in (None, "bf16")
+        self.cache_round = cache_round
+        self.forced_routing = None
+        self._forced = None
         self.reset()
+
+    def _store(self, x):
+        """A value as the cache keeps it (exact, or bf16 in the ``cache_round`` reading)."""
+        return ops.bf16_round(x) if self.cache_round == "bf16" else x
 
     # ------------------------------------------------------------------------------------------
     def reset(self):
@@ -120,6 +138,7 @@ class Oracle:
             raise ValueError("token id out of range")
 
         x = self.W("embed")[tokens].astype(F64)  # [B, R, d]
+        self._forced, self.forced_routing = self.forced_routing, None
         for i, kind in enumerate(cfg.mixers):
             h = ops.rmsnorm(x, self.W(f"layers.{i}.attn_norm"), cfg.norm_eps)
             x = x + self.mixer(i, kind, h, positions)
@@ -178,8 +197,8 @@ class Oracle:
             pos = positions[b] + np.arange(R)
             qb = ops.rope(q[b], pos[:, None], cfg.rope_theta)
             kb = ops.rope(k[b], pos[:, None], cfg.rope_theta)
-            K[b, pos] = kb
-            V[b, pos] = v[b]
+            K[b, pos] = self._store(kb)
+            V[b, pos] = self._store(v[b])
             o = ops.gqa_block_attention(qb, K[b], V[b], int(positions[b]))
             out[b] = o.reshape(R, hq * hd)
         return ops.linear(out, self.W(p + "wo"))
@@ -228,7 +247,7 @@ class Oracle:
             pos = positions[b] + np.arange(R)
             q_rope[b] = ops.rope(qf[b, :, :, nope:], pos[:, None], cfg.rope_theta)
             k_r = ops.rope(kv[b, :, lora:], pos, cfg.rope_theta)
-            lat[b, pos] = np.concatenate([c_kv[b], k_r], axis=-1)
+            lat[b, pos] = self._store(np.concatenate([c_kv[b], k_r], axis=-1))
         return q_nope, q_rope
 
     def mla(self, i, h, positions, absorbed: bool = True):
@@ -301,6 +320,10 @@ class Oracle:
                 idx, wts, biased = ops.route(z[b, r], bias, cfg.top_k, cfg.route_scale)
                 idx_all[b, r] = idx
                 biased_all[b, r] = biased
+                if self._forced is not None and i in self._forced:
+                    idx = np.asarray(self._forced[i][b, r], dtype=np.int64)
+                    s_used = ops.sigmoid(z[b, r][idx])
+                    wts = cfg.route_scale * s_used / np.sum(s_used)
                 for e, we in zip(idx, wts):
                     acc += we * ops.swiglu(y, self.expert(i, "e", "gate", e), self.expert(i, "e", "up", e),
                                            self.expert(i, "e", "down", e))

@@ -2,10 +2,14 @@
 on the same seeded inputs and compares every step.
 
 Comparison rules (floating point decides an integer here, so near-ties are handled explicitly):
-  * logits: max |gpu - oracle| <= tol over every row of every step;
+  * logits: max |gpu - oracle| <= tol over every row of every step, against the exact oracle;
   * greedy tokens: equal, unless the oracle's top-1 / top-2 gap is below 2 * tol, in which case either
     token is accepted; the oracle's token is fed to both sides (teacher forcing), so one near-tie never
-    makes the two runs diverge.
+    makes the two runs diverge;
+  * MoE routing: the top-k is compared in the pages' precision (activations, hence the cached keys, values
+    and latents, stored in bf16): a second oracle with bf16-stored caches decides each row's experts, the
+    kernel's own picks must equal them except at near-ties (ROUTE_TIE), and the exact oracle and the kernel
+    (through its routing override) both compute with them.
 """
 from __future__ import annotations
 
@@ -24,7 +28,6 @@ class Report:
         self.near_ties = 0
         self.route_ties = 0
         self.routed_rows = 0
-        self.diverged = False
         self.compared = 0
         self.errors = []
 
@@ -33,11 +36,12 @@ ROUTE_TIE = 1e-4   # router scores this close at the top-k boundary may be picke
 
 
 def check_routing(orc, log, pos0, R: int, rep, what: str):
-    """Compares the experts the kernel selected (its routing log, by position) with the oracle's last call,
-    as sets per (layer, sequence, row). A difference is accepted only where the oracle's k-th and (k+1)-th
-    biased scores lie within ROUTE_TIE (a near-tie that fp32 may break the other way); from then on the
-    two runs hold different states, so later logits are not compared (rep.diverged)."""
-    if log is None or rep.diverged:
+    """Compares the experts the kernel picked itself (its routing log, by position) with the routing oracle's
+    own picks of its last call, as sets per (layer, sequence, row). A difference is accepted only where the
+    oracle's k-th and (k+1)-th biased scores lie within ROUTE_TIE (a near-tie that fp32 may break the other
+    way). Both sides then still compute with the routing oracle's picks (the kernel through its routing
+    override, the exact oracle through forced_routing), so one near-tie never makes the runs diverge."""
+    if log is None:
         return
     k = orc.cfg.top_k
     lg = log.cpu().numpy()
@@ -54,7 +58,6 @@ def check_routing(orc, log, pos0, R: int, rep, what: str):
                 gap = s[k - 1] - s[k] if s.shape[0] > k else np.inf
                 if gap < ROUTE_TIE:
                     rep.route_ties += 1
-                    rep.diverged = True
                 else:
                     rep.errors.append(f"{what}: layer {layer} seq {b} row {r}: experts {got.tolist()} vs oracle "
                                       f"{want.tolist()} (boundary gap {gap:.3g})")
@@ -154,43 +157,66 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
             assert chunks and min(chunks) >= min_ring_chunks, f"rows {R_}: ring chunks per instruction {chunks}"
     Bc = 1 if fork else B
     ctx = make_tokens(seed, "ctx", (Bc, T), cfg.vocab, device=dev).contiguous()
-    log = None
+    log = override = orc_r = None
     if cfg.ffn == "moe":
         log = torch.full((cfg.n_layers, B, max_ctx, cfg.top_k), -1, dtype=torch.int32, device=dev)
         mk.set_routing_log(log)
-    mk.prefill(ctx)
-    for b in range(1, B if fork else 1):
-        mk.fork(0, b)
+        override = torch.full((cfg.n_layers, B, max_ctx, cfg.top_k), -1, dtype=torch.int32, device=dev)
+        mk.set_routing_override(override)
+
+    def oracle_call(o, o_r, tok, pos):
+        """The exact oracle's logits of one call; for MoE models the routing oracle (bf16-stored caches, the
+        pages' activation precision) runs first, and its picks drive the exact oracle and the kernel."""
+        if o_r is not None:
+            o_r.step(tok, pos)
+            forced = {i: idx for i, (idx, _) in o_r.routing.items()}
+            o.forced_routing = forced
+            for i, idx in forced.items():
+                for b in range(idx.shape[0]):
+                    override[i, b, int(pos[b]):int(pos[b]) + idx.shape[1]] = torch.from_numpy(
+                        idx[b].astype(np.int32)).to(dev)
+        return o.step(tok, pos)
+
     key = (cfg, T, seed, max_ctx, oracle_block)
     if fork and oracle_block and key in _PREFILLED:
         orc = _PREFILLED[key]
     else:
         orc = Oracle(cfg, w, Bc, max_ctx)
+        if cfg.ffn == "moe":
+            orc_r = Oracle(cfg, orc.w, Bc, max_ctx, cache_round="bf16")
         if oracle_block:
             oracle_prefill_blocks(orc, ctx.cpu().numpy(), oracle_block)
         else:
-            orc.prefill(ctx.cpu().numpy())
-        if not oracle_block:
-            check_routing(orc, log, np.zeros(Bc, dtype=np.int64), T, rep, "prefill")
+            orc.reset()
+            if orc_r is not None:
+                orc_r.reset()
+            oracle_call(orc, orc_r, ctx.cpu().numpy(), np.zeros(Bc, dtype=np.int64))
+            orc.commit(T)
+            if orc_r is not None:
+                orc_r.commit(T)
         if fork and oracle_block:
             _PREFILLED[key] = orc
+    mk.prefill(ctx)
+    for b in range(1, B if fork else 1):
+        mk.fork(0, b)
+    if orc_r is not None:
+        check_routing(orc_r, log, np.zeros(Bc, dtype=np.int64), T, rep, "prefill")
     if fork:
         orc = oracle_fork(orc, B)   # copies: the cached prefill stays untouched
     pos = np.full(B, T, dtype=np.int64)
     tok = make_tokens(seed, "start", (B, 1), cfg.vocab).numpy().astype(np.int64)
     V = cfg.vocab
     for s in range(decode_steps):
+        ref = oracle_call(orc, orc_r, tok, pos)[:, 0]
         logits = torch.empty((B, V), device=dev, dtype=torch.float32)
         am = torch.empty((B,), device=dev, dtype=torch.int32)
         mk.step(torch.from_numpy(tok.astype(np.int32)).to(dev), torch.from_numpy(pos.astype(np.int32)).to(dev),
                 logits, am)
-        ref = orc.step(tok, pos)[:, 0]
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy()
-        check_routing(orc, log, pos, 1, rep, f"decode step {s}")
-        if not rep.diverged:
-            compare_logits(g, ref, tol, rep, f"decode step {s}")
+        check_routing(orc_r, log, pos, 1, rep, f"decode step {s}")
+        compare_logits(g, ref, tol, rep, f"decode step {s}")
         if check_argmax:
             # the kernel's own argmax must be the argmax of the logits it wrote
             assert np.array_equal(am.cpu().numpy(), g.argmax(-1)), "in-kernel argmax differs from logits argmax"
@@ -200,17 +226,16 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
     for vi, acc in enumerate(verify_accepts):
         drafts = make_tokens(seed, f"draft{vi}", (B, R_verify - 1), cfg.vocab).numpy().astype(np.int64)
         block = np.concatenate([tok, drafts], axis=1)
+        ref = oracle_call(orc, orc_r, block, pos)
         logits = torch.empty((B * R_verify, V), device=dev, dtype=torch.float32)
         am = torch.empty((B * R_verify,), device=dev, dtype=torch.int32)
         mk.step(torch.from_numpy(block.astype(np.int32)).to(dev).contiguous(),
                 torch.from_numpy(pos.astype(np.int32)).to(dev), logits, am)
-        ref = orc.step(block, pos)
         st = mk.status()
         assert st == 0, f"device status {st}"
         g = logits.cpu().numpy().reshape(B, R_verify, V)
-        check_routing(orc, log, pos, R_verify, rep, f"verify block {vi}")
-        if not rep.diverged:
-            compare_logits(g, ref, tol, rep, f"verify block {vi}")
+        check_routing(orc_r, log, pos, R_verify, rep, f"verify block {vi}")
+        compare_logits(g, ref, tol, rep, f"verify block {vi}")
         if check_argmax:
             assert np.array_equal(am.cpu().numpy().reshape(B, R_verify), g.argmax(-1))
         # accept `acc` rows: the next anchor is the oracle's greedy token after the last accepted row
@@ -219,13 +244,12 @@ def run_case(cfg, B: int, T: int, decode_steps: int = 0, verify_accepts=(), R_ve
         rep.steps += 1
     # one more decode step to check the commit of the last verify block
     if verify_accepts:
+        ref = oracle_call(orc, orc_r, tok, pos)[:, 0]
         logits = torch.empty((B, V), device=dev, dtype=torch.float32)
         mk.step(torch.from_numpy(tok.astype(np.int32)).to(dev), torch.from_numpy(pos.astype(np.int32)).to(dev),
                 logits, None)
-        ref = orc.step(tok, pos)[:, 0]
         assert mk.status() == 0
-        check_routing(orc, log, pos, 1, rep, "decode after verify")
-        if not rep.diverged:
-            compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
+        check_routing(orc_r, log, pos, 1, rep, "decode after verify")
+        compare_logits(logits.cpu().numpy(), ref, tol, rep, "decode after verify")
     mk.close()
     return rep

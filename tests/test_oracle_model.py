@@ -207,3 +207,54 @@ def test_moe_closed_form_one_row():
     code0 = q[0, 0] & 15
     sc = ops.e4m3_value(wt["layers.0.e_gate.s"][1].numpy()[0, 0])
     assert dec[0, 0] == ops.e2m1_value(code0) * sc * np.float64(wt["layers.0.e_gate.g"][1].item())
+
+
+@pytest.mark.parametrize("kind", ["dense", "kda_mla_moe"])
+def test_bf16_cache_reading_rounds_only_the_cache(kind):
+    """cache_round="bf16" stores exactly the bf16 rounding of what the exact oracle stores (in the first
+    cached layer, whose inputs are the same in both)."""
+    cfg = tiny(kind)
+    w = _weights(cfg)
+    toks = make_tokens(0, "ctx", (2, 5), cfg.vocab).numpy()
+    a, b = Oracle(cfg, w, 2, 16), Oracle(cfg, w, 2, 16, cache_round="bf16")
+    a.step(toks, np.zeros(2, dtype=int))
+    b.step(toks, np.zeros(2, dtype=int))
+    first = 0 if cfg.mixers[0] == "gqa" else 3
+    if cfg.mixers[first] == "gqa":
+        for x, y in zip(a.kv[first], b.kv[first]):
+            np.testing.assert_array_equal(ops.bf16_round(x), y)
+    else:
+        # layer 3 is the first MLA layer; its inputs differ only through layers 0..2, which have no cache
+        np.testing.assert_array_equal(ops.bf16_round(a.lat[first][:, :5]), b.lat[first][:, :5])
+
+
+def test_forced_routing_uses_given_experts():
+    """forced_routing = the oracle's own picks changes nothing; a different forced set gives the MoE closed
+    form over those experts with weights renormalised over their sigmoid scores, while `routing` still
+    records the row's own picks."""
+    cfg = tiny("nvfp4_moe", n_layers=1, router_bias_std=0.05)
+    wt = _weights(cfg, seed=9)
+    rng = np.random.default_rng(11)
+    h = rng.standard_normal((1, 1, cfg.d_model))
+    o = Oracle(cfg, wt, 1, 4)
+    base = o.moe(0, h)
+    own = o.routing[0][0].copy()
+    o._forced = {0: own}
+    np.testing.assert_array_equal(o.moe(0, h), base)
+    pick = np.array([[[5, 1]]])
+    assert not np.array_equal(np.sort(pick[0, 0]), np.sort(own[0, 0]))
+    o._forced = {0: pick}
+    got = o.moe(0, h)[0, 0]
+    np.testing.assert_array_equal(o.routing[0][0], own)
+    y = h[0, 0]
+    z = wt["layers.0.w_router"].float().numpy().astype(np.float64) @ y
+    s = 1 / (1 + np.exp(-z))
+    wts = cfg.route_scale * s[[5, 1]] / s[[5, 1]].sum()
+
+    def ffn(kind, e):
+        gw, uw, dw = (o.expert(0, kind, m, e) for m in ("gate", "up", "down"))
+        g = gw @ y
+        return dw @ ((g / (1 + np.exp(-g))) * (uw @ y))
+
+    want = ffn("s", 0) + wts[0] * ffn("e", 5) + wts[1] * ffn("e", 1)
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-13)

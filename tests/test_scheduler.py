@@ -86,8 +86,15 @@ def check_program(cfg, n_sm, B, R, head=True):
         elif t == GEMV:
             partition(k, o["rows"])
             assert 0 <= o["k_begin"] and o["k_begin"] + o["K"] <= o["ldw"]
-            if o["mma"]:
+            if o["mma"] == 1:
                 assert N <= 4 and o["K"] % 16 == 0 and o["kc"] == 1024 and o["rg"] == 16
+            elif o["mma"] == 2:
+                # tcgen05: 5 to 64 rows, rows cut in 8-row units (the TMA box heights), K parts of 256 / ncols atoms
+                ncols = -(-2 * N // 16) * 16
+                assert 5 <= N <= 64 and o["kc"] == 64 * (256 // ncols)
+                assert o["k_begin"] == 0 and o["K"] == o["ldw"], "no K split on the tcgen05 path"
+                for x in by_op[k]:
+                    assert x["a"] % 8 == 0 and (x["b"] % 8 == 0 or x["b"] == o["rows"])
             else:
                 assert o["kc"] * o["rg"] == 16384
                 if o["staged"]:
@@ -196,10 +203,12 @@ def test_layer_op_sequences():
 
 
 def test_staging_decisions():
-    """Batch 1 to 4 of the d = 5120 stack take the tensor-core GEMV for every projection (4 rows of width
-    5120 fit the staging area as hi/lo pairs); 8 rows use the CUDA-core path."""
+    """Batch 1 to 4 of the d = 5120 stack take the mma.sync GEMV for every projection (4 rows of width 5120
+    fit the staging area as hi/lo pairs); 8 rows (and 8-row verify) take the tcgen05 / TMEM GEMV."""
     cfg = config("hybrid_gdn_gqa", n_layers=4)
-    for B, want in ((1, 1), (2, 1), (4, 1), (8, 0)):
+    ops, _ = make_plan(cfg, 152, 1, 8)
+    assert all(o["mma"] == 2 for o in ops if o["type"] == GEMV)
+    for B, want in ((1, 1), (2, 1), (4, 1), (8, 2)):
         ops, _ = make_plan(cfg, 152, B, 1)
         gemvs = [o for o in ops if o["type"] == GEMV and o["K"] == cfg.d_model]
         assert gemvs and all(o["mma"] == want for o in gemvs), B
