@@ -73,7 +73,7 @@ class StateBuffers(C.Structure):
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
            "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log",
            "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
-           "mk_set_routing_override"]
+           "mk_set_routing_override", "mk_decode_steps", "mk_decode_steps_host", "mk_verify_step"]
 
 _lib = None
 
@@ -105,6 +105,9 @@ def load(path: str | None = None) -> C.CDLL:
     lib.mk_fork_sequence.argtypes = [_P, C.c_int, C.c_int, _P]
     lib.mk_set_wait_limit.argtypes = [_P, C.c_uint64]
     lib.mk_set_routing_override.argtypes = [_P, _P]
+    lib.mk_decode_steps.argtypes = [_P, _P, _P, C.c_int, C.c_int, _P, _P, _P]
+    lib.mk_decode_steps_host.argtypes = [_P, _P, _P, C.c_int, C.c_int, _P, _P]
+    lib.mk_verify_step.argtypes = [_P, _P, _P, C.c_int, C.c_int, _P, _P, _P, _P]
     lib.mk_plan.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, C.c_int,
                             C.POINTER(PlanOp), C.c_int, C.POINTER(C.c_int), C.POINTER(PlanInstr), C.c_int,
                             C.POINTER(C.c_int)]
@@ -112,7 +115,7 @@ def load(path: str | None = None) -> C.CDLL:
                                           _P, _P, C.c_int, C.c_int, _P, _P, _P]
     for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
               "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
-              "mk_set_routing_override"):
+              "mk_set_routing_override", "mk_decode_steps", "mk_decode_steps_host", "mk_verify_step"):
         getattr(lib, f).restype = C.c_int
     if path is None:
         _lib = lib
@@ -231,6 +234,26 @@ class Megakernel:
             self.h, tokens_np.ctypes.data, positions_np.ctypes.data, B, R,
             None if logits_np is None else logits_np.ctypes.data, argmax_np.ctypes.data, stream)
         self._check(rc)
+
+    def verify(self, tokens, positions, accept_out, logits=None, argmax=None, stream=None):
+        """Verify step with on-device greedy acceptance. tokens: device int32 [B, R] (anchor + drafts);
+        accept_out: device int32 [3, B] (accepted length, bonus token, next position)."""
+        B, R = tokens.shape
+        self._check(self.lib.mk_verify_step(self.h, tokens.data_ptr(), positions.data_ptr(), B, R, _ptr(logits),
+                                             _ptr(argmax), accept_out.data_ptr(), stream))
+
+    def steps(self, tokens, positions, n_steps: int, tokens_out, logits=None, stream=None):
+        """n_steps greedy steps in one launch. tokens, positions: device int32 [B]; tokens_out: device int32
+        [n_steps, B]; logits: device fp32 [B, V] or None (the last step's)."""
+        B = tokens.shape[0]
+        self._check(self.lib.mk_decode_steps(self.h, tokens.data_ptr(), positions.data_ptr(), B, n_steps,
+                                              tokens_out.data_ptr(), _ptr(logits), stream))
+
+    def steps_host(self, tokens_np, positions_np, n_steps: int, tokens_out_np, stream=None):
+        """Host (numpy int32) variant of steps: copies in, runs, copies the tokens [n_steps, B] out, waits."""
+        B = tokens_np.shape[0]
+        self._check(self.lib.mk_decode_steps_host(self.h, tokens_np.ctypes.data, positions_np.ctypes.data, B,
+                                                   n_steps, tokens_out_np.ctypes.data, stream))
 
     def fork(self, src: int, dst: int, stream=None):
         """Make sequence ``dst`` a copy of sequence ``src`` (caches, states, pending rows, counts)."""

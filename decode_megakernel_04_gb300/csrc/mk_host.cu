@@ -116,6 +116,8 @@ struct mk_handle {
   int32_t* stage_pos = nullptr;
   int32_t* stage_argmax = nullptr;
   float* stage_logits = nullptr;
+  int32_t* stage_steps = nullptr;  // mk_decode_steps_host: the greedy tokens of every step
+  size_t steps_cap = 0;
   int max_ops = 0;
   int n_ops_last = 0;
   std::deque<Program> programs;  // stable addresses: launches and the trace keep pointers into it
@@ -170,8 +172,9 @@ mk_status check_desc(mk_handle* h, const mk_model_desc& d, const mk_weights& w) 
   if (d.n_layers < 1 || d.n_layers > MK_MAX_LAYERS) return fail(h, MK_ERR_INVALID_ARG, "n_layers %d", d.n_layers);
   if (d.d_model < 8 || d.d_model % 8) return fail(h, MK_ERR_INVALID_ARG, "d_model %d must be a multiple of 8", d.d_model);
   if (d.vocab < 1) return fail(h, MK_ERR_INVALID_ARG, "vocab %d", d.vocab);
-  if (d.max_batch < 1 || d.max_rows < 1 || d.max_rows > kMaxRows || d.max_batch * d.max_rows > kMaxN)
-    return fail(h, MK_ERR_UNSUPPORTED, "max_batch*max_rows must be <= %d and max_rows <= %d", kMaxN, kMaxRows);
+  // a handle may hold up to kMaxN sequences; one call processes at most kMaxN rows (batch x rows)
+  if (d.max_batch < 1 || d.max_rows < 1 || d.max_rows > kMaxRows || d.max_batch > kMaxN)
+    return fail(h, MK_ERR_UNSUPPORTED, "max_batch must be <= %d and max_rows <= %d", kMaxN, kMaxRows);
   if (d.max_ctx < d.max_rows) return fail(h, MK_ERR_INVALID_ARG, "max_ctx %d", d.max_ctx);
   if (!w.embed || !w.final_norm || (!d.tied_embedding && !w.lm_head))
     return fail(h, MK_ERR_INVALID_ARG, "embed / final_norm / lm_head missing");
@@ -267,7 +270,7 @@ void derive_layout(mk_handle* h) {
     else if (D.mixer[i] == MK_MIXER_MLA) h->slot[i] = h->n_mla++;
     else h->slot[i] = h->n_delta++;
   }
-  h->nmax = D.max_batch * D.max_rows;
+  h->nmax = std::min(D.max_batch * D.max_rows, kMaxN);  // rows of the largest call
   h->full_ops = h->n_mla > 0 || D.ffn_kind == MK_FFN_MOE;
   int proj = 8, attn = 8;
   for (int i = 0; i < D.n_layers; ++i) {
@@ -954,7 +957,7 @@ Program* get_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
 // Fills the kernel parameters from the handle's buffers and the device copy of a program; launches.
 mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* tokens, int tok_stride,
                          const int32_t* positions, int B, int R, float* logits, int32_t* argmax, bool commit_all,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int n_steps = 1, int32_t* accept_out = nullptr) {
   const mk_model_desc& D = h->desc;
   KParams p;
   std::memset(&p, 0, sizeof(p));
@@ -976,10 +979,13 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.B = B;
   p.R = R;
   p.N = B * R;
-  p.epoch = ++h->epoch;
+  p.epoch = h->epoch + 1;  // step s of the launch uses epoch + s: the pending-row halves alternate per step
+  h->epoch += (uint32_t)n_steps;
+  p.n_steps = n_steps;
   p.commit_all = commit_all ? 1 : 0;
   p.logits = logits;
   p.argmax = argmax;
+  p.accept_out = accept_out;
   p.d = D.d_model;
   p.V = D.vocab;
   p.max_ctx = D.max_ctx;
@@ -1024,12 +1030,14 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
 }
 
 mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const int32_t* positions, int B, int R,
-                      float* logits, int32_t* argmax, bool commit_all, cudaStream_t stream) {
+                      float* logits, int32_t* argmax, bool commit_all, cudaStream_t stream, int n_steps = 1,
+                      int32_t* accept_out = nullptr) {
   mk_status st = MK_OK;
-  const bool head = logits != nullptr || argmax != nullptr;
+  const bool head = logits != nullptr || argmax != nullptr || accept_out != nullptr;
   Program* prog = get_program(h, B, R, head, &st);
   if (!prog) return st;
-  return launch_program(h, prog, tokens, tok_stride, positions, B, R, logits, argmax, commit_all, stream);
+  return launch_program(h, prog, tokens, tok_stride, positions, B, R, logits, argmax, commit_all, stream, n_steps,
+                        accept_out);
 }
 
 }  // namespace
@@ -1161,8 +1169,9 @@ mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_to
       if (e != cudaSuccess) return cuda_fail(h, e, "state reset");
     }
   }
-  for (int c0 = 0; c0 < n_tokens; c0 += D.max_rows) {
-    const int rc = std::min(D.max_rows, n_tokens - c0);
+  const int chunk_rows = std::max(1, std::min(D.max_rows, kMaxN / batch));  // rows per launch: batch x rows <= kMaxN
+  for (int c0 = 0; c0 < n_tokens; c0 += chunk_rows) {
+    const int rc = std::min(chunk_rows, n_tokens - c0);
     if ((e = fill_i32_launch(h->pos_buf, batch, c0, s)) != cudaSuccess) return cuda_fail(h, e, "positions");
     mk_status st = launch_step(h, tokens + c0, n_tokens, h->pos_buf, batch, rc, nullptr, nullptr,
                                c0 + rc == n_tokens, s);
@@ -1177,6 +1186,7 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
   const mk_model_desc& D = h->desc;
   if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, D.max_batch);
   if (rows < 1 || rows > D.max_rows) return fail(h, MK_ERR_INVALID_ARG, "rows %d outside 1..%d", rows, D.max_rows);
+  if (batch * rows > kMaxN) return fail(h, MK_ERR_INVALID_ARG, "batch x rows = %d above %d", batch * rows, kMaxN);
   if (!logits_out && !argmax_out) return fail(h, MK_ERR_INVALID_ARG, "no output requested");
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
@@ -1188,7 +1198,7 @@ mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const in
                               int rows, float* logits_host, int32_t* argmax_host, void* stream) {
   if (!h || !tokens_host || !positions_host || !argmax_host) return MK_ERR_INVALID_ARG;
   const mk_model_desc& D = h->desc;
-  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows)
+  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows || batch * rows > kMaxN)
     return fail(h, MK_ERR_INVALID_ARG, "batch %d / rows %d out of range", batch, rows);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSetDevice(h->device);
@@ -1206,6 +1216,61 @@ mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, const in
   if (logits_host &&
       (e = cudaMemcpyAsync(logits_host, h->stage_logits, sizeof(float) * (size_t)n * D.vocab, cudaMemcpyDeviceToHost,
                            s)) != cudaSuccess)
+    return cuda_fail(h, e, "device to host copy");
+  return mk_get_status(h, stream);
+}
+
+mk_status mk_verify_step(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch, int rows,
+                         float* logits_out, int32_t* argmax_out, int32_t* accept_out, void* stream) {
+  if (!h || !tokens || !positions || !accept_out) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, D.max_batch);
+  if (rows < 2 || rows > D.max_rows) return fail(h, MK_ERR_INVALID_ARG, "rows %d outside 2..%d", rows, D.max_rows);
+  if (batch * rows > kMaxN) return fail(h, MK_ERR_INVALID_ARG, "batch x rows = %d above %d", batch * rows, kMaxN);
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  return launch_step(h, tokens, rows, positions, batch, rows, logits_out, argmax_out, false,
+                     reinterpret_cast<cudaStream_t>(stream), 1, accept_out);
+}
+
+mk_status mk_decode_steps(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch, int n_steps,
+                          int32_t* tokens_out, float* logits_out, void* stream) {
+  if (!h || !tokens || !positions || !tokens_out) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, D.max_batch);
+  if (n_steps < 1 || n_steps > D.max_ctx) return fail(h, MK_ERR_INVALID_ARG, "n_steps %d", n_steps);
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  return launch_step(h, tokens, 1, positions, batch, 1, logits_out, tokens_out, false,
+                     reinterpret_cast<cudaStream_t>(stream), n_steps);
+}
+
+mk_status mk_decode_steps_host(mk_handle* h, const int32_t* tokens_host, const int32_t* positions_host, int batch,
+                               int n_steps, int32_t* tokens_out_host, void* stream) {
+  if (!h || !tokens_host || !positions_host || !tokens_out_host) return MK_ERR_INVALID_ARG;
+  const mk_model_desc& D = h->desc;
+  if (batch < 1 || batch > D.max_batch || n_steps < 1 || n_steps > D.max_ctx)
+    return fail(h, MK_ERR_INVALID_ARG, "batch %d / n_steps %d out of range", batch, n_steps);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  if ((size_t)n_steps * batch > h->steps_cap) {
+    // grows the handle's token staging (synchronous cudaMalloc, only when a longer run is asked for)
+    if (h->stage_steps) cudaFree(h->stage_steps);
+    h->stage_steps = nullptr;
+    h->steps_cap = 0;
+    if ((e = cudaMalloc(&h->stage_steps, sizeof(int32_t) * (size_t)n_steps * batch)) != cudaSuccess)
+      return cuda_fail(h, e, "token staging");
+    h->steps_cap = (size_t)n_steps * batch;
+  }
+  if ((e = cudaMemcpyAsync(h->stage_tok, tokens_host, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(h->stage_pos, positions_host, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s)) !=
+          cudaSuccess)
+    return cuda_fail(h, e, "host to device copy");
+  mk_status st = launch_step(h, h->stage_tok, 1, h->stage_pos, batch, 1, nullptr, h->stage_steps, false, s, n_steps);
+  if (st != MK_OK) return st;
+  if ((e = cudaMemcpyAsync(tokens_out_host, h->stage_steps, sizeof(int32_t) * (size_t)n_steps * batch,
+                           cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return cuda_fail(h, e, "device to host copy");
   return mk_get_status(h, stream);
 }
@@ -1239,7 +1304,8 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm
   tmp.n_sm = n_sm;
   mk_status st = check_desc(&tmp, tmp.desc, tmp.w);
   if (st != MK_OK) return st;
-  if (batch < 1 || batch > desc->max_batch || rows < 1 || rows > desc->max_rows) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > desc->max_batch || rows < 1 || rows > desc->max_rows || batch * rows > kMaxN)
+    return MK_ERR_INVALID_ARG;
   derive_layout(&tmp);
   HostProgram hp;
   if ((st = construct_program(&tmp, batch, rows, with_head != 0, hp)) != MK_OK) return st;
@@ -1386,6 +1452,7 @@ void mk_destroy(mk_handle* h) {
     cudaFree(p.d_tmaps);
   }
   for (void* p : h->allocs) cudaFree(p);
+  if (h->stage_steps) cudaFree(h->stage_steps);
   delete h;
 }
 
@@ -1459,7 +1526,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
     return st;
   }
   const mk_model_desc& D = tmp.desc;
-  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > D.max_batch || rows < 1 || rows > D.max_rows || batch * rows > kMaxN)
+    return MK_ERR_INVALID_ARG;
   bool has_mla = false;
   for (int i = 0; i < D.n_layers; ++i) has_mla = has_mla || D.mixer[i] == MK_MIXER_MLA;
   if (has_mla || D.ffn_kind == MK_FFN_MOE) {

@@ -165,8 +165,10 @@ struct KParams {
   int32_t B, R, N;
   uint32_t epoch;
   int32_t commit_all;       // prefill: the rows of this call count as committed for c_spec
-  float* logits;
-  int32_t* argmax;
+  int32_t n_steps;          // greedy decode steps in this launch (R = 1 when above 1)
+  float* logits;            // [N, V] (a multi-step launch leaves the last step's)
+  int32_t* argmax;          // [n_steps][N] greedy tokens; step s > 0 embeds the tokens of step s - 1
+  int32_t* accept_out;      // verify: [3][B] accepted length, bonus token, next position (or NULL)
   // model
   int32_t d, V, max_ctx, max_batch, max_rows;
   float eps;
@@ -204,7 +206,9 @@ struct KParams {
   unsigned long long* trace;
 };
 
-// trace words per instruction: consumer begin, dependencies met, done; producer first / last issue
-constexpr int kTraceWords = 5;
+// trace words per instruction: consumer begin, dependencies met, done; producer first issue
+// (tcgen05 GEMV instructions also: first activation part staged, first weight chunk arrived, last MMA issued,
+// last activation part staged)
+constexpr int kTraceWords = 9;
 
 }  // namespace mk

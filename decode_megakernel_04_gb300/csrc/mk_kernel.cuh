@@ -681,41 +681,55 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 // + r * 128, its 16-byte chunk c at + ((c ^ (r & 7)) << 4). Warps 1..7 do this; inputs past K are zero.
 __device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, const CSmem& cs, uint8_t* buf, int a0,
                                          int a1, int stid, int nthr) {
+  constexpr int kBatch = 4;  // items whose loads are all in flight before any of them is converted
   const bool norm = op.in_kind == IN_NORM;
   const int N = p.N, K = op.K, nc = op.ncols;
   const int pairs = nc >> 1;                 // activation rows incl. the zero padding
-  const int items = pairs * (a1 - a0) * 8;   // (activation row, atom, 16-byte chunk)
-  for (int it = stid; it < items; it += nthr) {
-    const int c = it & 7, rest = it >> 3;
-    const int a = a0 + rest % (a1 - a0), n = rest / (a1 - a0);
-    const int k = a * 64 + c * 8;
-    float v[8];
+  const int na = a1 - a0;
+  const int items = pairs * na * 8;          // (activation row, atom, 16-byte chunk)
+  for (int it0 = stid; it0 < items; it0 += nthr * kBatch) {
+    float4 x0[kBatch], x1[kBatch];
+    uint4 g[kBatch];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-    if (n < N && k < K) {
-      const float* src = norm ? p.x + (size_t)n * p.d + k : op.in + (size_t)n * op.in_stride + k;
-      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
-      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-      if (norm) {
-        const uint4 g = __ldg(reinterpret_cast<const uint4*>(op.gain + k));
-        const float s = cs.inv_rms[n];
-        v[0] *= s * bf_lo(g.x); v[1] *= s * bf_hi(g.x); v[2] *= s * bf_lo(g.y); v[3] *= s * bf_hi(g.y);
-        v[4] *= s * bf_lo(g.z); v[5] *= s * bf_hi(g.z); v[6] *= s * bf_lo(g.w); v[7] *= s * bf_hi(g.w);
+    for (int u = 0; u < kBatch; ++u) {
+      const int it = it0 + u * nthr;
+      const int c = it & 7, rest = it >> 3;
+      const int a = a0 + rest % na, n = rest / na;
+      const int k = a * 64 + c * 8;
+      x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (it < items && n < N && k < K) {
+        const float* src = norm ? p.x + (size_t)n * p.d + k : op.in + (size_t)n * op.in_stride + k;
+        x0[u] = __ldcg(reinterpret_cast<const float4*>(src));
+        x1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        if (norm) g[u] = __ldg(reinterpret_cast<const uint4*>(op.gain + k));
       }
     }
-    uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint16_t h0 = f2bf(v[2 * e]), h1 = f2bf(v[2 * e + 1]);
-      const uint16_t l0 = f2bf(v[2 * e] - bf2f(h0)), l1 = f2bf(v[2 * e + 1] - bf2f(h1));
-      hi[e] = h0 | ((uint32_t)h1 << 16);
-      lo[e] = l0 | ((uint32_t)l1 << 16);
+    for (int u = 0; u < kBatch; ++u) {
+      const int it = it0 + u * nthr;
+      if (it >= items) break;
+      const int c = it & 7, rest = it >> 3;
+      const int a = a0 + rest % na, n = rest / na;
+      float v[8] = {x0[u].x, x0[u].y, x0[u].z, x0[u].w, x1[u].x, x1[u].y, x1[u].z, x1[u].w};
+      if (norm && n < N) {
+        const float s = cs.inv_rms[n];
+        v[0] *= s * bf_lo(g[u].x); v[1] *= s * bf_hi(g[u].x); v[2] *= s * bf_lo(g[u].y); v[3] *= s * bf_hi(g[u].y);
+        v[4] *= s * bf_lo(g[u].z); v[5] *= s * bf_hi(g[u].z); v[6] *= s * bf_lo(g[u].w); v[7] *= s * bf_hi(g[u].w);
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t h0 = f2bf(v[2 * e]), h1 = f2bf(v[2 * e + 1]);
+        const uint16_t l0 = f2bf(v[2 * e] - bf2f(h0)), l1 = f2bf(v[2 * e + 1] - bf2f(h1));
+        hi[e] = h0 | ((uint32_t)h1 << 16);
+        lo[e] = l0 | ((uint32_t)l1 << 16);
+      }
+      uint8_t* atom = buf + (size_t)(a - a0) * nc * 128;
+      const int rh = 2 * n, rl = 2 * n + 1;
+      *reinterpret_cast<uint4*>(atom + rh * 128 + ((c ^ (rh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(atom + rl * 128 + ((c ^ (rl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    uint8_t* atom = buf + (size_t)(a - a0) * nc * 128;
-    const int rh = 2 * n, rl = 2 * n + 1;
-    *reinterpret_cast<uint4*>(atom + rh * 128 + ((c ^ (rh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(atom + rl * 128 + ((c ^ (rl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -727,7 +741,7 @@ struct TcState {
 };
 
 __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
-                                CSmem& cs, uint8_t* act, TcState& ts, int ctid) {
+                                CSmem& cs, uint8_t* act, TcState& ts, unsigned long long* tr, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int sm = blockIdx.x;
   const int N = p.N, nc = op.ncols;
@@ -769,8 +783,10 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
         if (ok) tc_stage(p, op, cs, bb, a0, a1, ctid - 32, kConsumerThreads - 32);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&bready[buf]);
+        if (tr && ctid == 32) tr[8] = global_timer();
       } else if (lane == 0) {
         const bool bok = wait_bar(&bready[buf], use & 1u, p);
+        if (tr && g0 == in.a && a0 == 0) tr[5] = global_timer();
         const uint32_t bsa = smem_u32(bb);
         int col = 0;
         for (int r = g0; r < g1;) {
@@ -779,6 +795,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
           for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
             const int na = min(blk.atoms, a1 - c0);
             const bool ok = ring_wait_full(rg, ck, p) && bok;
+            if (tr && ck == chunk) tr[6] = global_timer();
             tc_fence_after();
             if (ok) {
               const uint32_t slot = ring_s + (ck % kSlots) * kSlotBytes;
@@ -805,6 +822,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
           col += blk.nseg * nc;
         }
         umma_commit(&bfree[buf]);
+        if (tr) tr[7] = global_timer();
       }
       ++ts.kp;
     }
@@ -1116,14 +1134,18 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
 // ------------------------------------------------------------------------------------------------
 // embedding: x[n, a:b] = E[token_n, a:b] (fp32) and the RMS partial of this SM's columns
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ int token_of(const KParams& p, int n) {
+// A launch may run several greedy decode steps (one row per sequence each): step s sits at position
+// positions[b] + s, and its tokens are the greedy tokens step s - 1 wrote (argmax[(s - 1) * N + b]).
+__device__ __forceinline__ int seq_pos(const KParams& p, int b, int step) { return p.positions[b] + step; }
+__device__ __forceinline__ int token_of(const KParams& p, int n, int step) {
+  if (step > 0) return __ldcg(p.argmax + (size_t)(step - 1) * p.N + n);
   return p.tokens[(n / p.R) * p.tok_stride + (n % p.R)];
 }
 
-__device__ MK_OUTLINE void embed_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+__device__ MK_OUTLINE void embed_consume(const KParams& p, const OpDesc& op, const Instr& in, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   for (int n = warp; n < p.N; n += kConsumerWarps) {
-    const int tok = token_of(p, n);
+    const int tok = token_of(p, n, step);
     const uint16_t* e = p.embed + (size_t)tok * p.d;
     float s = 0.f;
     for (int c = in.a + lane; c < in.b; c += 32) {
@@ -1143,7 +1165,7 @@ __device__ __forceinline__ size_t kv_index(const KParams& p, const OpDesc& op, i
   return ((((size_t)op.slot * p.max_batch + b) * op.n_kv_heads + g) * p.max_ctx + t) * op.head_dim;
 }
 
-__device__ MK_OUTLINE void rope_append_consume(const KParams& p, const OpDesc& op, int ctid) {
+__device__ MK_OUTLINE void rope_append_consume(const KParams& p, const OpDesc& op, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hq = op.n_heads, hkv = op.n_kv_heads, hd = op.head_dim, half = hd / 2;
   const int per_row = hq + 2 * hkv;
@@ -1151,7 +1173,7 @@ __device__ MK_OUTLINE void rope_append_consume(const KParams& p, const OpDesc& o
   for (int it = blockIdx.x * kConsumerWarps + warp; it < total; it += p.n_sm * kConsumerWarps) {
     const int n = it / per_row, h = it % per_row;
     const int b = n / p.R, r = n % p.R;
-    const int pos = p.positions[b] + r;
+    const int pos = seq_pos(p, b, step) + r;
     float* vec = op.out + (size_t)n * op.out_stride + (size_t)h * hd;
     const float2* cs = p.rope + (size_t)pos * (p.rot_dim / 2);
     if (h < hq + hkv) {
@@ -1181,8 +1203,9 @@ __device__ MK_OUTLINE void rope_append_consume(const KParams& p, const OpDesc& o
 // also takes the block's own rows p_b .. p_b + R - 1 (causal). Scores are kept in log2 units.
 // Each warp owns up to J (row, head) pairs; lane L owns dims [L*E, L*E + E) of the head.
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ void attn_range(const KParams& p, const OpDesc& op, int b, int c, int& t0, int& t1) {
-  const int pos0 = p.positions[b];
+__device__ __forceinline__ void attn_range(const KParams& p, const OpDesc& op, int b, int c, int step, int& t0,
+                                           int& t1) {
+  const int pos0 = seq_pos(p, b, step);
   const int tc = (pos0 + op.nchunk - 1) / op.nchunk;
   t0 = min(c * tc, pos0);
   t1 = min(t0 + tc, pos0);
@@ -1252,7 +1275,7 @@ __device__ __forceinline__ void attn_block(const uint16_t* Ks, const uint16_t* V
 
 template <int E, int J>
 __device__ MK_OUTLINE void attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
-                             CSmem& cs, uint16_t* stage_u16, int ctid) {
+                             CSmem& cs, uint16_t* stage_u16, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int hd = E * 32;
   const int hkv = op.n_kv_heads, G = op.groups;
@@ -1261,8 +1284,8 @@ __device__ MK_OUTLINE void attn_consume(const KParams& p, const OpDesc& op, cons
   const int npairs = (rhi - rlo) * G;
   const int R = p.R;
   int t0, t1;
-  attn_range(p, op, b, c, t0, t1);
-  const int pos0 = p.positions[b];
+  attn_range(p, op, b, c, step, t0, t1);
+  const int pos0 = seq_pos(p, b, step);
   const int P = kChunkBytes / (4 * hd);
   const float qscale = rsqrtf((float)hd) * kLog2e;
 
@@ -1415,7 +1438,7 @@ __device__ MK_OUTLINE void attn_combine_consume(const KParams& p, const OpDesc& 
 // ------------------------------------------------------------------------------------------------
 template <int CW>
 __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, const Instr& in, CSmem& cs,
-                                          float* stage, int ctid) {
+                                          float* stage, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int b = in.a, h = in.b, jg = in.c;
   const int H = op.n_heads, dk = op.dk, dv = op.dv;
@@ -1425,10 +1448,10 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
   const bool kda = op.per_channel_decay != 0;
   const int na = kda ? dk : 1;
   const int R = p.R;
-  const int pos0 = p.positions[b];
-  const int a = pos0 - p.seq[b].c_int;
+  const int pos0 = seq_pos(p, b, step);
+  const int a = pos0 - __ldcg(&p.seq[b].c_int);  // the previous step of this launch may have moved it
   const int rec = p.pend_rec;
-  const uint32_t cur = p.epoch & 1u, prev = cur ^ 1u;
+  const uint32_t cur = (p.epoch + (uint32_t)step) & 1u, prev = cur ^ 1u;
   auto pend_at = [&](uint32_t par, int r) -> float* {
     return p.pend + (((((size_t)op.slot * 2 + par) * p.max_batch + b) * p.max_rows + r) * H + h) * rec;
   };
@@ -1583,7 +1606,7 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
 // its top-k as sequential argmax passes: Kimi K3's TPU megakernel, "How it maps onto a TPU v7"); the
 // weights are route_scale * s_sel / sum(s_sel). Also the union of the picked experts, ascending.
 // ------------------------------------------------------------------------------------------------
-__device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, float* stage, int ctid) {
+__device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, float* stage, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int E = op.n_experts, K = op.top_k, N = p.N;
   int* flags = reinterpret_cast<int*>(stage);
@@ -1607,7 +1630,7 @@ __device__ __noinline__ void route_consume(const KParams& p, const OpDesc& op, f
     float ssel[kMaxTopK];
     // routing replay: a row with caller-given expert ids uses them (an id outside [0, E) falls back to the
     // row's own pick); its own picks still go to the routing log
-    const int b_row = n / p.R, pos_row = p.positions[b_row] + n % p.R;
+    const int b_row = n / p.R, pos_row = seq_pos(p, b_row, step) + n % p.R;
     const int32_t* frow = nullptr;
     if (p.route_force) {
       frow = p.route_force + (((size_t)op.layer * p.max_batch + b_row) * p.max_ctx + pos_row) * K;
@@ -1936,7 +1959,7 @@ __device__ __forceinline__ size_t lat_index(const KParams& p, const OpDesc& op, 
   return (((size_t)op.slot * p.max_batch + b) * p.max_ctx + t) * (op.kv_lora + op.rope);
 }
 
-__device__ __noinline__ void mla_prep_consume(const KParams& p, const OpDesc& op, int ctid) {
+__device__ __noinline__ void mla_prep_consume(const KParams& p, const OpDesc& op, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int total = p.N * 2;
   const int ql = op.q_lora, kl = op.kv_lora, rp = op.rope, half = rp / 2;
@@ -1954,7 +1977,7 @@ __device__ __noinline__ void mla_prep_consume(const KParams& p, const OpDesc& op
         __stcg(op.aux + (size_t)n * op.aux_stride + i, __ldcg(row + i) * inv * bf2f(op.q_norm[i]));
     } else {
       const int b = n / p.R, r = n % p.R;
-      const int pos = p.positions[b] + r;
+      const int pos = seq_pos(p, b, step) + r;
       uint16_t* lat = p.latent + lat_index(p, op, b, pos);
       float s = 0.f;
       for (int i = lane; i < kl; i += 32) {
@@ -1978,7 +2001,7 @@ __device__ __noinline__ void mla_prep_consume(const KParams& p, const OpDesc& op
 // also writes the rotated rope query qt[n][h][kv_lora ..]. Warp w owns 16 latent columns: their W_UK rows
 // (lane L holds inputs [L*E, L*E + E) of each) are loaded together up front, then each query row costs 16
 // dot products folded across the warp by one multi-value reduction.
-__device__ __noinline__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int ctid) {
+__device__ __noinline__ void mla_qabs_consume(const KParams& p, const OpDesc& op, const Instr& in, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int h = in.a, cb = in.b;
   const int nope = op.nope, rp = op.rope, kl = op.kv_lora, half = rp / 2;
@@ -2014,7 +2037,7 @@ __device__ __noinline__ void mla_qabs_consume(const KParams& p, const OpDesc& op
   if (cb == 0) {
     for (int n = warp; n < N; n += kConsumerWarps) {
       const int b = n / p.R, r = n % p.R;
-      const int pos = p.positions[b] + r;
+      const int pos = seq_pos(p, b, step) + r;
       const float* q = op.in + (size_t)n * ldq + (size_t)h * qw + nope;
       const float2* cs = p.rope + (size_t)pos * (p.rot_dim / 2);
       float* dst = op.out + (size_t)n * ldt + (size_t)h * (kl + rp) + kl;
@@ -2089,7 +2112,7 @@ __device__ __forceinline__ void mla_block(const uint16_t* lat, int nb, int ldl, 
 // group*8 + w for the rows of the instruction (J rows per warp)
 template <int J>
 __device__ __noinline__ void mla_attn_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                                 uint32_t& chunk, uint16_t* stage, int ctid) {
+                                 uint32_t& chunk, uint16_t* stage, int step, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int ngr = op.n_kv_heads, G = op.groups;  // head groups, heads per group
   const int b = in.a / ngr, hg = in.a % ngr, c = in.b;
@@ -2098,8 +2121,8 @@ __device__ __noinline__ void mla_attn_consume(const KParams& p, const OpDesc& op
   const int R = p.R;
   const int h = hg * G + warp;
   int t0, t1;
-  attn_range(p, op, b, c, t0, t1);
-  const int pos0 = p.positions[b];
+  attn_range(p, op, b, c, step, t0, t1);
+  const int pos0 = seq_pos(p, b, step);
   const int P = kChunkBytes / (ldl * 2);
   float q[J][16], qr[J][2], o[J][16], m[J], l[J];
   int prow[J];
@@ -2213,7 +2236,8 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 }
 
 struct ChunkCursor {
-  int qi, q1;
+  int qi, q0, q1;
+  int step;  // decode step of a multi-step launch: the queue is walked once per step
   int kind;  // 0: load the next instruction, 1: GEMV chunks, 2: attention KV chunks
   // the instruction's fields, cached in registers when it is loaded
   int K, kc, pad, passes, ng, n, a, glog, swiglu;
@@ -2265,7 +2289,12 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
                                             uint32_t& bytes, uint32_t& dst, uint32_t& total) {
   for (;;) {
     if (c.kind == 0) {
-      if (c.qi >= c.q1) return false;
+      if (c.qi >= c.q1) {
+        if (c.step + 1 >= p.n_steps) return false;
+        ++c.step;
+        c.qi = c.q0;
+        continue;
+      }
       const Instr in = p.instrs[c.qi];
       const OpDesc& op = p.ops[in.op];
       c.op = &op;
@@ -2307,7 +2336,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       } else if (type == OP_ATTN) {
         const int hkv = op.n_kv_heads, hd = op.head_dim;
         const int b = in.a / hkv, g = in.a % hkv;
-        attn_range(p, op, b, in.b, c.t, c.t1);
+        attn_range(p, op, b, in.b, c.step, c.t, c.t1);
         c.P = kChunkBytes / (4 * hd);
         c.pos_bytes = hd * 2;
         c.ncopy = 2;
@@ -2316,7 +2345,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       } else if (kFull && type == OP_MLA_ATTN) {
         const int b = in.a / op.n_kv_heads;
         const int ldl = op.kv_lora + op.rope;
-        attn_range(p, op, b, in.b, c.t, c.t1);
+        attn_range(p, op, b, in.b, c.step, c.t, c.t1);
         c.P = kChunkBytes / (2 * ldl);
         c.pos_bytes = ldl * 2;
         c.ncopy = 1;
@@ -2326,7 +2355,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         // the expert list is known once the router op has finished
         int ok = 1;
         if (lane == 0)
-          ok = wait_counter(&p.counters[op.route_op], (uint32_t)p.ops[op.route_op].n_instr, p) ? 1 : 0;
+          ok = wait_counter(&p.counters[op.route_op], (uint32_t)p.ops[op.route_op].n_instr * (uint32_t)(c.step + 1), p) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return false;
         c.up = type == OP_MOE_UP;
@@ -2474,8 +2503,8 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
 // ------------------------------------------------------------------------------------------------
 // final op: greedy argmax over the LM-head partials, sequence bookkeeping, counter reset
 // ------------------------------------------------------------------------------------------------
-__device__ MK_OUTLINE void final_consume(const KParams& p, int ctid) {
-  if (p.argmax) {
+__device__ MK_OUTLINE void final_consume(const KParams& p, CSmem& cs, int step, int ctid) {
+  if (p.argmax || p.accept_out) {
     const int warp = ctid >> 5, lane = ctid & 31;
     for (int n = warp; n < p.N; n += kConsumerWarps) {
       float bv = -CUDART_INF_F;
@@ -2491,11 +2520,28 @@ __device__ MK_OUTLINE void final_consume(const KParams& p, int ctid) {
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
-      if (lane == 0) p.argmax[n] = bi;
+      if (lane == 0) {
+        if (p.argmax) __stcg(p.argmax + (size_t)step * p.N + n, bi);
+        cs.best_idx[n] = bi;
+      }
+    }
+  }
+  if (p.accept_out && p.R > 1) {
+    // greedy acceptance of a verify block (row 0 the anchor, rows 1.. the drafts): draft r + 1 is accepted
+    // while it equals the greedy target of row r; the accepted prefix plus the target after it (the bonus
+    // token) is what the block emits (Kimi K3's TPU megakernel, "What DSpark changes per step")
+    consumer_sync();
+    if (ctid < p.B) {
+      const int b = ctid, R = p.R;
+      int a = 1;
+      while (a < R && cs.best_idx[b * R + a - 1] == p.tokens[b * p.tok_stride + a]) ++a;
+      p.accept_out[b] = a;
+      p.accept_out[p.B + b] = cs.best_idx[b * R + a - 1];
+      p.accept_out[2 * p.B + b] = seq_pos(p, b, step) + a;
     }
   }
   if (ctid < p.B) {
-    const int pos = p.positions[ctid];
+    const int pos = seq_pos(p, ctid, step);
     SeqState s;
     s.c_int = pos;
     s.u_int = p.R;
@@ -2503,7 +2549,9 @@ __device__ MK_OUTLINE void final_consume(const KParams& p, int ctid) {
     s.pad = 0;
     p.seq[ctid] = s;
   }
-  for (int i = ctid; i < p.n_ops; i += kConsumerThreads) p.counters[i] = 0u;
+  // the last step leaves the counters at zero for the next launch (every other CTA is done by now)
+  if (step == p.n_steps - 1)
+    for (int i = ctid; i < p.n_ops; i += kConsumerThreads) p.counters[i] = 0u;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -2515,7 +2563,9 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
   const uint32_t ring_base = smem_u32(rg.base);
   ChunkCursor mc, pc;
   mc.qi = pc.qi = q0;
+  mc.q0 = pc.q0 = q0;
   mc.q1 = pc.q1 = q1;
+  mc.step = pc.step = 0;
   mc.kind = pc.kind = 0;
   mc.uni = pc.uni = uni;
   const void* src = nullptr;
@@ -2528,7 +2578,7 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
   }
   int last_qi = -1;
   while (cursor_next(p, mc, lane, src, bytes, dst, total)) {
-    if (p.trace && lane == 0 && mc.qi != last_qi) {
+    if (p.trace && lane == 0 && mc.step == 0 && mc.qi != last_qi) {
       p.trace[(size_t)mc.qi * kTraceWords + 3] = global_timer();
       last_qi = mc.qi;
     }
@@ -2576,9 +2626,10 @@ __device__ MK_OUTLINE void gemv_dispatch(const KParams& p, const OpDesc& op, con
 
 // The MLA and MoE ops (full variant only).
 __device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                                            uint32_t& chunk, CSmem& cs, uint16_t* act, float* actf, int nr, int ctid) {
+                                            uint32_t& chunk, CSmem& cs, uint16_t* act, float* actf, int nr, int step,
+                                            int ctid) {
   switch (op.type) {
-      case OP_ROUTE: route_consume(p, op, actf, ctid); break;
+      case OP_ROUTE: route_consume(p, op, actf, step, ctid); break;
       case OP_MOE_UP:
       case OP_MOE_DOWN:
         if (op.fp4) {
@@ -2601,11 +2652,11 @@ __device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, 
           }
         }
         break;
-      case OP_MLA_PREP: mla_prep_consume(p, op, ctid); break;
-      case OP_MLA_QABS: mla_qabs_consume(p, op, in, ctid); break;
+      case OP_MLA_PREP: mla_prep_consume(p, op, step, ctid); break;
+      case OP_MLA_QABS: mla_qabs_consume(p, op, in, step, ctid); break;
       case OP_MLA_ATTN:
-        if (((in.c >> 8) - (in.c & 0xff)) <= 1) mla_attn_consume<1>(p, op, in, rg, chunk, act, ctid);
-        else mla_attn_consume<2>(p, op, in, rg, chunk, act, ctid);
+        if (((in.c >> 8) - (in.c & 0xff)) <= 1) mla_attn_consume<1>(p, op, in, rg, chunk, act, step, ctid);
+        else mla_attn_consume<2>(p, op, in, rg, chunk, act, step, ctid);
         break;
       case OP_MLA_UV: mla_uv_consume(p, op, in, ctid); break;
     default: break;
@@ -2617,27 +2668,34 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
   uint32_t chunk = 0;
   float* actf = reinterpret_cast<float*>(act);
   const int nr = p.N <= 1 ? 1 : p.N <= 2 ? 2 : p.N <= 4 ? 4 : 8;
+  const bool trace = p.trace != nullptr;
+  for (int step = 0; step < p.n_steps; ++step) {
   for (int qi = q0; qi < q1; ++qi) {
     const Instr in = p.instrs[qi];
     const OpDesc& op = p.ops[in.op];
     if (ctid == 0) {
       int ok = 1;
-      if (p.trace) p.trace[(size_t)qi * kTraceWords + 0] = global_timer();
+      if (trace && step == 0) p.trace[(size_t)qi * kTraceWords + 0] = global_timer();
+      // counters accumulate over the steps of a launch: op k of step s needs n_instr * (s + 1) completions
       for (int d = 0; d < op.n_deps && ok; ++d) {
         const int dop = op.deps[d];
-        ok = wait_counter(&p.counters[dop], (uint32_t)p.ops[dop].n_instr, p) ? 1 : 0;
+        ok = wait_counter(&p.counters[dop], (uint32_t)p.ops[dop].n_instr * (uint32_t)(step + 1), p) ? 1 : 0;
       }
+      // the embedding of step s reads the greedy tokens the final op of step s - 1 wrote
+      if (ok && step > 0 && op.type == OP_EMBED)
+        ok = wait_counter(&p.counters[p.n_ops - 1], (uint32_t)step, p) ? 1 : 0;
       if (*reinterpret_cast<volatile int32_t*>(p.abort_flag) != 0) ok = 0;
-      if (p.trace) p.trace[(size_t)qi * kTraceWords + 1] = global_timer();
+      if (trace && step == 0) p.trace[(size_t)qi * kTraceWords + 1] = global_timer();
       cs.flag = ok;
     }
     consumer_sync();
-    if (!cs.flag) break;
+    if (!cs.flag) return;
     switch (op.type) {
-      case OP_EMBED: embed_consume(p, op, in, ctid); break;
+      case OP_EMBED: embed_consume(p, op, in, step, ctid); break;
       case OP_GEMV:
         if (op.mma == 2) {
-          gemv_tc_consume(p, op, in, rg, chunk, cs, reinterpret_cast<uint8_t*>(act), ts, ctid);
+          gemv_tc_consume(p, op, in, rg, chunk, cs, reinterpret_cast<uint8_t*>(act), ts,
+                          (trace && step == 0) ? p.trace + (size_t)qi * kTraceWords : nullptr, ctid);
         } else if (op.mma) {
           gemv_mma_consume(p, op, in, rg, chunk, cs, actf, ctid);
         } else if (op.staged) {
@@ -2650,22 +2708,22 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
           else gemv_dispatch<8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
         }
         break;
-      case OP_ROPE_APPEND: rope_append_consume(p, op, ctid); break;
+      case OP_ROPE_APPEND: rope_append_consume(p, op, step, ctid); break;
       case OP_ATTN: {
         const int pairs = ((in.c >> 8) - (in.c & 0xff)) * op.groups;
         const int J = (pairs + kConsumerWarps - 1) / kConsumerWarps;
         if (op.head_dim == 256) {
-          if (J <= 1) attn_consume<8, 1>(p, op, in, rg, chunk, cs, act, ctid);
-          else if (J <= 2) attn_consume<8, 2>(p, op, in, rg, chunk, cs, act, ctid);
-          else attn_consume<8, 4>(p, op, in, rg, chunk, cs, act, ctid);
+          if (J <= 1) attn_consume<8, 1>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else if (J <= 2) attn_consume<8, 2>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else attn_consume<8, 4>(p, op, in, rg, chunk, cs, act, step, ctid);
         } else if (op.head_dim == 128) {
-          if (J <= 1) attn_consume<4, 1>(p, op, in, rg, chunk, cs, act, ctid);
-          else if (J <= 2) attn_consume<4, 2>(p, op, in, rg, chunk, cs, act, ctid);
-          else attn_consume<4, 4>(p, op, in, rg, chunk, cs, act, ctid);
+          if (J <= 1) attn_consume<4, 1>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else if (J <= 2) attn_consume<4, 2>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else attn_consume<4, 4>(p, op, in, rg, chunk, cs, act, step, ctid);
         } else {
-          if (J <= 1) attn_consume<2, 1>(p, op, in, rg, chunk, cs, act, ctid);
-          else if (J <= 2) attn_consume<2, 2>(p, op, in, rg, chunk, cs, act, ctid);
-          else attn_consume<2, 4>(p, op, in, rg, chunk, cs, act, ctid);
+          if (J <= 1) attn_consume<2, 1>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else if (J <= 2) attn_consume<2, 2>(p, op, in, rg, chunk, cs, act, step, ctid);
+          else attn_consume<2, 4>(p, op, in, rg, chunk, cs, act, step, ctid);
         }
         break;
       }
@@ -2682,22 +2740,23 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
       case OP_MLA_QABS:
       case OP_MLA_ATTN:
       case OP_MLA_UV:
-        if constexpr (kFull) run_full_op(p, op, in, rg, chunk, cs, act, actf, nr, ctid);
+        if constexpr (kFull) run_full_op(p, op, in, rg, chunk, cs, act, actf, nr, step, ctid);
         break;
       case OP_DELTA:
-        if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
-        else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
-        else delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), ctid);
+        if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         break;
-      case OP_FINAL: final_consume(p, ctid); break;
+      case OP_FINAL: final_consume(p, cs, step, ctid); break;
       default: break;
     }
     consumer_sync();
-    if (ctid == 0 && op.type != OP_FINAL) {
+    if (ctid == 0 && (op.type != OP_FINAL || step + 1 < p.n_steps)) {
       __threadfence();
       red_release_add(&p.counters[in.op], 1u);
     }
-    if (ctid == 0 && p.trace) p.trace[(size_t)qi * kTraceWords + 2] = global_timer();
+    if (ctid == 0 && trace && step == 0) p.trace[(size_t)qi * kTraceWords + 2] = global_timer();
+  }
   }
 }
 
@@ -2707,7 +2766,7 @@ __device__ int validate(const KParams& p) {
   for (int b = 0; b < p.B; ++b) {
     const int pos = p.positions[b];
     const SeqState s = p.seq[b];
-    if (pos < 0 || pos < s.c_spec || pos > s.c_int + s.u_int || pos + p.R > p.max_ctx) return 0;
+    if (pos < 0 || pos < s.c_spec || pos > s.c_int + s.u_int || pos + p.R + p.n_steps - 1 > p.max_ctx) return 0;
     for (int r = 0; r < p.R; ++r) {
       const int t = p.tokens[b * p.tok_stride + r];
       if (t < 0 || t >= p.V) return 0;

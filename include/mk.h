@@ -77,8 +77,9 @@ typedef struct mk_model_desc {
   int32_t n_experts, top_k, n_shared, expert_dim, expert_format;
   float route_scale;               /* routed weights = route_scale * s_sel / sum(s_sel)         */
   /* capacity of the handle */
-  int32_t max_batch;               /* sequences per call                                       */
-  int32_t max_rows;                /* query rows per sequence per call (8 for speculative verify)*/
+  int32_t max_batch;               /* sequences per call (at most 64)                          */
+  int32_t max_rows;                /* query rows per sequence per call (at most 8; a call's batch x
+                                      rows may not exceed 64)                                    */
   int32_t max_ctx;                 /* positions per sequence (KV / latent cache length)         */
 } mk_model_desc;
 
@@ -178,6 +179,43 @@ mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_to
  * then skipped and no state changes), MK_ERR_TIMEOUT. */
 mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch,
                          int rows, float* logits_out, int32_t* argmax_out, void* stream);
+
+/* A speculative-verify step (rows = 2..max_rows: row 0 the anchor, rows 1.. the drafts) that also decides,
+ * on the device, how much of each block greedy decoding accepts: draft r + 1 is accepted while it equals the
+ * greedy token of row r, so sequence b accepts a_b rows (1 <= a_b <= rows) and emits them plus one bonus
+ * token, the greedy token of row a_b - 1 (the accepted prefix plus one bonus token of the pages' verify step:
+ * Kimi K3's TPU megakernel, "What DSpark changes per step").
+ *   accept_out  device int32 [3][batch]: accept_out[b] = a_b, accept_out[batch + b] = the bonus token (the
+ *               next anchor), accept_out[2 * batch + b] = positions[b] + a_b (the next call's position, which
+ *               commits exactly the accepted rows).
+ * So the next call can take its anchor and positions straight from accept_out without a host round trip.
+ * The other arguments and the step itself are mk_decode_step's. One launch, asynchronous.
+ * Errors: MK_ERR_INVALID_ARG (rows < 2, missing accept_out, as mk_decode_step). */
+mk_status mk_verify_step(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch, int rows,
+                         float* logits_out, int32_t* argmax_out, int32_t* accept_out, void* stream);
+
+/* `n_steps` greedy decode steps of `batch` sequences in ONE kernel launch: step s feeds each sequence the
+ * greedy token step s - 1 produced, on the device, so the host is involved once per call (the pages run 24
+ * steps inside one device call and meet the host once every 24: Kimi K3's TPU megakernel, "What DSpark
+ * changes per step"). Equivalent to n_steps calls of mk_decode_step with rows = 1, the first with `tokens`
+ * and `positions`, call s with positions + s and the previous call's greedy tokens.
+ *   tokens      device int32 [batch]: the first step's token of each sequence
+ *   positions   device int32 [batch]: the first step's position (as for mk_decode_step)
+ *   tokens_out  device int32 [n_steps][batch]: the greedy token each step produced (required)
+ *   logits_out  device fp32 [batch, vocab] or NULL: the last step's logits
+ * Positions + n_steps must stay within max_ctx (checked on the device: MK_ERR_DEVICE, nothing runs).
+ * Inside the launch the weight ring runs on from one step into the next. Asynchronous, one launch.
+ * Errors: MK_ERR_INVALID_ARG (batch, n_steps, missing tokens_out). */
+mk_status mk_decode_steps(mk_handle* h, const int32_t* tokens, const int32_t* positions, int batch, int n_steps,
+                          int32_t* tokens_out, float* logits_out, void* stream);
+
+/* mk_decode_steps from HOST buffers: copies tokens_host [batch] and positions_host [batch] in, runs the
+ * n_steps launch, copies the greedy tokens [n_steps][batch] back to tokens_out_host and waits for `stream`;
+ * returns the device status as mk_get_status would. The first call asking for more steps than before grows
+ * the handle's token staging with a synchronous cudaMalloc.
+ * Passage: as mk_decode_steps. */
+mk_status mk_decode_steps_host(mk_handle* h, const int32_t* tokens_host, const int32_t* positions_host, int batch,
+                               int n_steps, int32_t* tokens_out_host, void* stream);
 
 /* The same step from HOST buffers: copies tokens_host [batch*rows] and positions_host [batch] to
  * handle-owned device staging, runs the step, copies the greedy tokens back to argmax_host

@@ -181,6 +181,20 @@ def route(z: np.ndarray, bias: np.ndarray, top_k: int, scale: float):
     return idx, w, biased
 
 
+def greedy_accept(logits: np.ndarray, block_tokens) -> tuple:
+    """Greedy acceptance of one verify block: logits [R, V] of rows 0..R-1 (row 0 the anchor, rows 1.. the
+    drafts), block_tokens [R] their tokens. Draft r + 1 is accepted while it equals the greedy token of row r
+    (lowest index on ties); returns (accepted rows a, 1 <= a <= R, and the bonus token: the greedy token of
+    row a - 1). The block emits its accepted prefix plus that one bonus token (Kimi K3's TPU megakernel,
+    "What DSpark changes per step"). Pinned: equals the prefix that sequential greedy decoding from the
+    anchor would have produced."""
+    R = logits.shape[0]
+    a = 1
+    while a < R and int(np.argmax(logits[a - 1])) == int(block_tokens[a]):
+        a += 1
+    return a, int(np.argmax(logits[a - 1]))
+
+
 def swiglu(y: np.ndarray, w_gate, w_up, w_down) -> np.ndarray:
     """SwiGLU feed-forward: (silu(y Wg^T) * (y Wu^T)) Wd^T."""
     return linear(silu(linear(y, w_gate)) * linear(y, w_up), w_down)

@@ -244,3 +244,13 @@ def test_watchdog_timeout_then_recovery():
     assert torch.equal(logits, want)
     mk.close()
     ref.close()
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_hybrid_batch_above_8(B):
+    """Concurrency above batch 8: 16 and 64 sequences decoding in one launch (tcgen05 GEMV tiles of 32 and 128
+    TMEM columns; prefill in launches of 64 / B rows per sequence), against the oracle."""
+    from gpu_harness import run_case
+    cfg = config("hybrid_gdn_gqa", n_layers=4, d_model=512, ffn_dim=1024, vocab=4096)
+    rep = run_case(cfg, B=B, T=12, decode_steps=2, tol=TOL_BF16)
+    _check(rep)

@@ -258,3 +258,29 @@ def test_forced_routing_uses_given_experts():
 
     want = ffn("s", 0) + wts[0] * ffn("e", 5) + wts[1] * ffn("e", 1)
     np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("k", [0, 2, 7])
+def test_greedy_accept_equals_sequential_greedy_prefix(k):
+    """A verify block whose first k drafts are what sequential greedy decoding from the anchor produces, and
+    whose next draft differs, accepts k + 1 rows and emits that decoding's (k + 1)-th token as the bonus."""
+    import copy
+    cfg = tiny("gdn_gqa")
+    w = _weights(cfg)
+    o = Oracle(cfg, w, 1, 32)
+    o.prefill(make_tokens(0, "ctx", (1, 6), cfg.vocab).numpy())
+    anchor = 5
+    seq = copy.deepcopy(o)
+    greedy, tok = [], anchor
+    for t in range(8):
+        tok = int(np.argmax(seq.step(np.array([[tok]]), np.array([6 + t]))[0, 0]))
+        greedy.append(tok)
+    drafts = list(greedy[:k])
+    if k < 7:
+        drafts.append((greedy[k] + 1) % cfg.vocab)
+    drafts += [0] * (7 - len(drafts))
+    block = np.array([anchor] + drafts)
+    logits = o.step(block[None], np.array([6]))[0]
+    a, bonus = ops.greedy_accept(logits, block)
+    assert a == k + 1
+    assert bonus == greedy[k]

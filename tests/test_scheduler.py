@@ -241,3 +241,17 @@ def test_plan_refuses_what_one_sm_cannot_stage():
     scheduler refuses instead of overflowing the staging area."""
     with pytest.raises(binding.MKError):
         make_plan(config("hybrid_gdn_gqa", n_layers=4), 1, 2, 8)
+
+
+def test_batch_above_eight_rows_per_call():
+    """Concurrency above batch 8: a handle may hold up to 64 sequences; one call takes at most 64 rows, so 64
+    single-row sequences run (every GEMV on the tcgen05 path, 128 TMEM columns per tile) and 16 sequences of
+    8-row verify blocks are refused."""
+    cfg = config("hybrid_gdn_gqa", n_layers=4)
+    ops, ins = make_plan(cfg, 152, 64, 1, max_batch=64)
+    gemvs = [o for o in ops if o["type"] == GEMV]
+    assert gemvs and all(o["mma"] == 2 and o["kc"] == 64 * (256 // 128) for o in gemvs)
+    ops, _ = make_plan(cfg, 152, 8, 8, max_batch=64)
+    assert all(o["mma"] == 2 for o in ops if o["type"] == GEMV)
+    with pytest.raises(binding.MKError):
+        make_plan(cfg, 152, 16, 8, max_batch=64)
