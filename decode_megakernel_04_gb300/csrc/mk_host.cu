@@ -172,9 +172,9 @@ mk_status check_desc(mk_handle* h, const mk_model_desc& d, const mk_weights& w) 
   if (d.n_layers < 1 || d.n_layers > MK_MAX_LAYERS) return fail(h, MK_ERR_INVALID_ARG, "n_layers %d", d.n_layers);
   if (d.d_model < 8 || d.d_model % 8) return fail(h, MK_ERR_INVALID_ARG, "d_model %d must be a multiple of 8", d.d_model);
   if (d.vocab < 1) return fail(h, MK_ERR_INVALID_ARG, "vocab %d", d.vocab);
-  // a handle may hold up to kMaxN sequences; one call processes at most kMaxN rows (batch x rows)
-  if (d.max_batch < 1 || d.max_rows < 1 || d.max_rows > kMaxRows || d.max_batch > kMaxN)
-    return fail(h, MK_ERR_UNSUPPORTED, "max_batch must be <= %d and max_rows <= %d", kMaxN, kMaxRows);
+  // a handle may hold up to kMaxSeqs sequences (caches and states); one call processes at most kMaxN rows
+  if (d.max_batch < 1 || d.max_rows < 1 || d.max_rows > kMaxRows || d.max_batch > kMaxSeqs)
+    return fail(h, MK_ERR_UNSUPPORTED, "max_batch must be <= %d and max_rows <= %d", kMaxSeqs, kMaxRows);
   if (d.max_ctx < d.max_rows) return fail(h, MK_ERR_INVALID_ARG, "max_ctx %d", d.max_ctx);
   if (!w.embed || !w.final_norm || (!d.tied_embedding && !w.lm_head))
     return fail(h, MK_ERR_INVALID_ARG, "embed / final_norm / lm_head missing");
@@ -1156,7 +1156,7 @@ fail_out:
 mk_status mk_prefill_kv(mk_handle* h, const int32_t* tokens, int batch, int n_tokens, void* stream) {
   if (!h || !tokens) return MK_ERR_INVALID_ARG;
   const mk_model_desc& D = h->desc;
-  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d", batch);
+  if (batch < 1 || batch > D.max_batch || batch > kMaxN) return fail(h, MK_ERR_INVALID_ARG, "batch %d", batch);
   if (n_tokens < 1 || n_tokens > D.max_ctx) return fail(h, MK_ERR_INVALID_ARG, "n_tokens %d", n_tokens);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSetDevice(h->device);
@@ -1237,7 +1237,8 @@ mk_status mk_decode_steps(mk_handle* h, const int32_t* tokens, const int32_t* po
                           int32_t* tokens_out, float* logits_out, void* stream) {
   if (!h || !tokens || !positions || !tokens_out) return MK_ERR_INVALID_ARG;
   const mk_model_desc& D = h->desc;
-  if (batch < 1 || batch > D.max_batch) return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, D.max_batch);
+  if (batch < 1 || batch > D.max_batch || batch > kMaxN)
+    return fail(h, MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, std::min(D.max_batch, kMaxN));
   if (n_steps < 1 || n_steps > D.max_ctx) return fail(h, MK_ERR_INVALID_ARG, "n_steps %d", n_steps);
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
@@ -1249,7 +1250,7 @@ mk_status mk_decode_steps_host(mk_handle* h, const int32_t* tokens_host, const i
                                int n_steps, int32_t* tokens_out_host, void* stream) {
   if (!h || !tokens_host || !positions_host || !tokens_out_host) return MK_ERR_INVALID_ARG;
   const mk_model_desc& D = h->desc;
-  if (batch < 1 || batch > D.max_batch || n_steps < 1 || n_steps > D.max_ctx)
+  if (batch < 1 || batch > D.max_batch || batch > kMaxN || n_steps < 1 || n_steps > D.max_ctx)
     return fail(h, MK_ERR_INVALID_ARG, "batch %d / n_steps %d out of range", batch, n_steps);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSetDevice(h->device);

@@ -26,7 +26,8 @@ constexpr int kSlots = MK_RING_SLOTS;
 constexpr int kActBytes = 82176;
 constexpr int kSlotBytes = 33 * 1024;   // ring slot allocation (payload <= kChunkBytes + row padding)
 constexpr int kChunkBytes = 32768;      // weight bytes per chunk
-constexpr int kMaxN = 64;        // rows per step (batch * rows)
+constexpr int kMaxN = 64;        // rows per call (batch * rows)
+constexpr int kMaxSeqs = 256;    // sequences a handle can hold
 constexpr int kMaxRows = 8;      // query rows per sequence
 constexpr int kMaxOpMats = 6;
 constexpr int kMaxDeps = 2;

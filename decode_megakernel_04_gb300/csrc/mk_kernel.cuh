@@ -171,7 +171,9 @@ struct CSmem {
   int32_t pad[2];
   float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
   int32_t uni_c[kMaxExperts + 4];        // MoE: the step's expert union, consumers' copy (count, ids)
-  int32_t uni_p[kMaxExperts + 4];        // the producer warp's copy
+  // the producer warp's copy of the union during an expert op; during a tcgen05 GEMV op the same words hold
+  // the producer's current row block (a TcBlock, kept here so the producer's chunk cursor stays in registers)
+  int32_t uni_p[kMaxExperts + 4];
   // tcgen05 GEMV: staged-activation buffer ready [2] / free [2], accumulators complete, drain at exit
   uint64_t tcbar[6];
   uint32_t tmem_base;
@@ -363,33 +365,53 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // hi/lo bf16 columns of the staged activations: slot n (n < N) = hi of row n, slot N + n = lo of row n,
 // each K + 8 elements long (the 8 pad elements put successive slots in different banks)
 __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, CSmem& cs, uint16_t* cols, int ctid) {
+  constexpr int kBatch = 8;  // loads of this many items are in flight before any of them is converted
   const bool norm = op.in_kind == IN_NORM;
   const int K = op.K, N = p.N, cp = op.K + 8;
   const int total4 = N * K / 4;
-  for (int i = ctid; i < total4; i += kConsumerThreads) {
-    const int e = i * 4;
-    const int n = e / K, k = e % K;
-    const float* src = norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
-    float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-    if (norm) {
-      const uint2 g = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
-      const float s = cs.inv_rms[n];
-      v.x *= s * bf_lo(g.x);
-      v.y *= s * bf_hi(g.x);
-      v.z *= s * bf_lo(g.y);
-      v.w *= s * bf_hi(g.y);
-    }
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    uint16_t hi[4], lo[4];
+  for (int i0 = ctid; i0 < total4; i0 += kConsumerThreads * kBatch) {
+    float4 v[kBatch];
+    uint2 g[kBatch];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      hi[j] = f2bf(f[j]);
-      lo[j] = f2bf(f[j] - bf2f(hi[j]));
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[u] = make_uint2(0u, 0u);
+      if (i < total4) {
+        const int e = i * 4;
+        const int n = e / K, k = e % K;
+        const float* src =
+            norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
+        v[u] = __ldcg(reinterpret_cast<const float4*>(src));
+        if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+      }
     }
-    *reinterpret_cast<uint2*>(cols + (size_t)n * cp + k) =
-        make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
-    *reinterpret_cast<uint2*>(cols + (size_t)(N + n) * cp + k) =
-        make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      if (i >= total4) break;
+      const int e = i * 4;
+      const int n = e / K, k = e % K;
+      float4 x = v[u];
+      if (norm) {
+        const float s = cs.inv_rms[n];
+        x.x *= s * bf_lo(g[u].x);
+        x.y *= s * bf_hi(g[u].x);
+        x.z *= s * bf_lo(g[u].y);
+        x.w *= s * bf_hi(g[u].y);
+      }
+      const float f[4] = {x.x, x.y, x.z, x.w};
+      uint16_t hi[4], lo[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        hi[j] = f2bf(f[j]);
+        lo[j] = f2bf(f[j] - bf2f(hi[j]));
+      }
+      *reinterpret_cast<uint2*>(cols + (size_t)n * cp + k) =
+          make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+      *reinterpret_cast<uint2*>(cols + (size_t)(N + n) * cp + k) =
+          make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+    }
   }
 }
 
@@ -551,10 +573,13 @@ __device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr
 // the product keeps ~16 mantissa bits of the fp32 activations; column 2n + 1 is added to column 2n at the end.
 //   * Weight tiles come from the ring, loaded by the producer warp with TMA (2D tensor maps of each weight
 //     matrix, 64-element boxes with 128-byte swizzle: the canonical K-major layout the MMA reads directly).
-//   * An instruction's rows are cut into row blocks of at most 128 physical rows (64 logical rows of SwiGLU:
-//     its gate and up tiles), each split into segments at matrix boundaries; every segment accumulates in
-//     its own TMEM tile of ncols columns, so one row group (as many blocks as fit 512 columns) keeps all its
-//     accumulators in TMEM across the whole K loop and no cross-warp reduction is needed.
+//   * An instruction's rows are cut into row blocks of at most 128 physical rows, each split into segments
+//     at matrix boundaries (one TMA box per segment and atom). In shared memory a chunk is laid out atom by
+//     atom, each atom holding the block's segments stacked row after row, so one 128-row MMA per 16-input
+//     step covers the whole block, and the block accumulates in one TMEM tile of ncols columns (lane i = the
+//     block's row i). SwiGLU blocks take 64 logical rows: gate rows then up rows, two tiles. One row group
+//     (as many blocks as fit 512 columns) keeps all its accumulators in TMEM across the whole K loop, so no
+//     cross-warp reduction is needed.
 //   * K is covered in parts of 256 / ncols atoms (64 inputs each); the activations of a part are staged by
 //     warps 1..7 into one of two 32 KB buffers while lane 0 of warp 0 issues the MMAs of the previous part.
 // ------------------------------------------------------------------------------------------------
@@ -563,13 +588,17 @@ struct TcSeg {
   int row;    // first row inside that matrix
   int h;      // rows
   int out0;   // first output row (physical concatenated row; SwiGLU: logical row)
+  int roff;   // first row of the segment inside each stacked atom (a multiple of 8)
 };
 struct TcBlock {
   int nseg;
-  int rows8;  // sum of the segments' box heights (rows rounded up to 8)
+  int rows8;  // stacked rows of one atom: sum of the segments' box heights (rows rounded up to 8)
   int atoms;  // 64-input atoms per ring chunk
+  int tiles;  // TMEM tiles of the block: 1, or 2 for SwiGLU (gate, up)
   TcSeg seg[kTcMaxSeg];
 };
+
+static_assert(sizeof(TcBlock) <= sizeof(CSmem::uni_p), "the producer's row block must fit its shared-memory slot");
 
 __device__ __forceinline__ int tc_h8(int h) { return (h + 7) & ~7; }
 
@@ -579,18 +608,20 @@ __device__ __forceinline__ int tc_block(const OpDesc& op, int start, int end, Tc
   if (op.out_kind == OUT_SWIGLU) {
     const int h = min(64, end - start);
     blk.nseg = 2;
-    blk.seg[0] = {0, start, h, start};
-    blk.seg[1] = {1, start, h, start};
+    blk.tiles = 2;
+    blk.seg[0] = {0, start, h, start, 0};
+    blk.seg[1] = {1, start, h, start, tc_h8(h)};
     blk.rows8 = 2 * tc_h8(h);
   } else {
     int r = start, m = 0, base = 0;
     while (m < op.n_mat - 1 && r >= base + op.mat_rows[m]) base += op.mat_rows[m++];
     blk.nseg = 0;
     blk.rows8 = 0;
+    blk.tiles = 1;
     int left = 128;
     while (r < end && left > 0 && blk.nseg < kTcMaxSeg) {
       const int h = min(min(op.mat_rows[m] - (r - base), end - r), left);
-      blk.seg[blk.nseg++] = {m, r - base, h, r};
+      blk.seg[blk.nseg++] = {m, r - base, h, r, blk.rows8};
       blk.rows8 += tc_h8(h);
       left -= tc_h8(h);
       r += h;
@@ -608,8 +639,8 @@ __device__ __forceinline__ int tc_group_end(const OpDesc& op, int start, int end
   while (r < end) {
     TcBlock blk;
     const int nxt = tc_block(op, r, end, blk);
-    if (cols > 0 && cols + blk.nseg * op.ncols > kTcCols) break;
-    cols += blk.nseg * op.ncols;
+    if (cols > 0 && cols + blk.tiles * op.ncols > kTcCols) break;
+    cols += blk.tiles * op.ncols;
     r = nxt;
   }
   return r;
@@ -799,19 +830,17 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             tc_fence_after();
             if (ok) {
               const uint32_t slot = ring_s + (ck % kSlots) * kSlotBytes;
-              uint32_t soff = 0;
-              for (int s = 0; s < blk.nseg; ++s) {
-                const int h8 = tc_h8(blk.seg[s].h);
-                const uint32_t d = ts.tmem + (uint32_t)(col + s * nc);
-                for (int a = 0; a < na; ++a) {
-                  const uint32_t aa = slot + soff + (uint32_t)(a * h8 * 128);
-                  const uint32_t ba = bsa + (uint32_t)((c0 + a - a0) * nc * 128);
+              for (int a = 0; a < na; ++a) {
+                const uint32_t atom = slot + (uint32_t)(a * blk.rows8 * 128);
+                const uint32_t ba = bsa + (uint32_t)((c0 + a - a0) * nc * 128);
+                for (int t = 0; t < blk.tiles; ++t) {
+                  const uint32_t aa = atom + (uint32_t)(blk.seg[t].roff * 128);  // tile t starts at segment t
+                  const uint32_t d = ts.tmem + (uint32_t)(col + t * nc);
 #pragma unroll
                   for (int j = 0; j < 4; ++j)
                     umma_bf16(d, umma_desc(aa + j * 32), umma_desc(ba + j * 32), idesc,
                               (c0 + a > 0 || j > 0) ? 1u : 0u);
                 }
-                soff += (uint32_t)(h8 * na * 128);
               }
             }
             // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
@@ -819,7 +848,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             umma_commit(&rg.empty[ck % kSlots]);
             ++ck;
           }
-          col += blk.nseg * nc;
+          col += blk.tiles * nc;
         }
         umma_commit(&bfree[buf]);
         if (tr) tr[7] = global_timer();
@@ -838,12 +867,13 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
     for (int r = g0; r < g1;) {
       TcBlock blk;
       r = tc_block(op, r, g1, blk);
-      const int nout = swiglu ? 1 : blk.nseg;
-      for (int s = 0; s < nout; ++s) {
-        const TcSeg& sg = blk.seg[s];
+      {
+        // lane i of the tile is the block's row i (rows of consecutive segments follow each other)
+        const int s = 0;
         const int i = q * 32 + lane;
-        const bool valid = i < sg.h;
-        const int row = sg.out0 + i;
+        const int hrows = swiglu ? blk.seg[0].h : blk.seg[blk.nseg - 1].out0 + blk.seg[blk.nseg - 1].h - blk.seg[0].out0;
+        const bool valid = i < hrows;
+        const int row = blk.seg[0].out0 + i;
         for (int pc = 0; pc < hc; pc += 8) {
           const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + s * nc + half * hc + pc);
           float v[8];
@@ -887,7 +917,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
           }
         }
       }
-      col += blk.nseg * nc;
+      col += blk.tiles * nc;
     }
     tc_fence_before();
     consumer_sync();  // TMEM reads done before the next row group's MMAs overwrite the tiles
@@ -920,23 +950,43 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
 // memory. (Rounding them to bf16 instead costs up to ~5e-2 in the logits at full model width.)
 __device__ __forceinline__ void stage_activations(const KParams& p, const OpDesc& op, CSmem& cs, float* act,
                                                   int ctid) {
+  constexpr int kBatch = 8;  // loads of this many items are in flight before any of them is stored
   const bool norm = op.in_kind == IN_NORM;
   const int K = op.K, N = p.N;
   const int total4 = N * K / 4;
-  for (int i = ctid; i < total4; i += kConsumerThreads) {
-    const int e = i * 4;
-    const int n = e / K, k = e % K;
-    const float* src = norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
-    float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-    if (norm) {
-      const uint2 g = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
-      const float s = cs.inv_rms[n];
-      v.x *= s * bf_lo(g.x);
-      v.y *= s * bf_hi(g.x);
-      v.z *= s * bf_lo(g.y);
-      v.w *= s * bf_hi(g.y);
+  for (int i0 = ctid; i0 < total4; i0 += kConsumerThreads * kBatch) {
+    float4 v[kBatch];
+    uint2 g[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[u] = make_uint2(0u, 0u);
+      if (i < total4) {
+        const int e = i * 4;
+        const int n = e / K, k = e % K;
+        const float* src =
+            norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
+        v[u] = __ldcg(reinterpret_cast<const float4*>(src));
+        if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+      }
     }
-    *reinterpret_cast<float4*>(act + (size_t)n * K + k) = v;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      if (i >= total4) break;
+      const int e = i * 4;
+      const int n = e / K, k = e % K;
+      float4 x = v[u];
+      if (norm) {
+        const float s = cs.inv_rms[n];
+        x.x *= s * bf_lo(g[u].x);
+        x.y *= s * bf_hi(g[u].x);
+        x.z *= s * bf_lo(g[u].y);
+        x.w *= s * bf_hi(g[u].y);
+      }
+      *reinterpret_cast<float4*>(act + (size_t)n * K + k) = x;
+    }
   }
 }
 
@@ -2258,8 +2308,17 @@ struct ChunkCursor {
   // tcgen05 GEMV walk: the instruction's row range, current row group, K part, row block and first atom
   // of the current chunk, its atom count; tma = 1 when the chunk is a set of TMA tile copies
   int tma, adv, rb, g0, g1, a0, r, rnext, cc, na, nat, KP;
-  TcBlock blk;
+  TcBlock* blk;  // in shared memory (written by lane 0)
 };
+
+// the producer's row block: lane 0 computes it into shared memory, the warp reads it from there
+__device__ __forceinline__ int tc_cursor_block(const OpDesc& op, int start, int end, TcBlock* blk, int lane) {
+  int nxt = 0;
+  __syncwarp();
+  if (lane == 0) nxt = tc_block(op, start, end, *blk);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, nxt, 0);
+}
 
 __device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& c, int lane) {
   const int g0 = gemv_group_row(c.a, c.n, c.ng, c.grp);
@@ -2312,7 +2371,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         c.g1 = tc_group_end(op, in.a, in.b);
         c.a0 = 0;
         c.r = in.a;
-        c.rnext = tc_block(op, c.r, c.g1, c.blk);
+        c.rnext = tc_cursor_block(op, c.r, c.g1, c.blk, lane);
         c.cc = 0;
         c.adv = 0;
         c.kind = 5;
@@ -2387,7 +2446,7 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
     if (c.kind == 5) {
       if (c.adv) {  // step past the chunk returned last time, in the consumer's order: atoms, blocks, parts, groups
         c.adv = 0;
-        c.cc += c.blk.atoms;
+        c.cc += c.blk->atoms;
         if (c.cc >= min(c.nat, c.a0 + c.KP)) {
           c.r = c.rnext;
           if (c.r >= c.g1) {
@@ -2404,12 +2463,12 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
             }
             c.r = c.g0;
           }
-          c.rnext = tc_block(*c.op, c.r, c.g1, c.blk);
+          c.rnext = tc_cursor_block(*c.op, c.r, c.g1, c.blk, lane);
           c.cc = c.a0;
         }
       }
-      c.na = min(c.blk.atoms, min(c.nat, c.a0 + c.KP) - c.cc);
-      total = (uint32_t)(c.blk.rows8 * c.na * 128);
+      c.na = min(c.blk->atoms, min(c.nat, c.a0 + c.KP) - c.cc);
+      total = (uint32_t)(c.blk->rows8 * c.na * 128);
       bytes = 0;
       c.tma = 1;
       c.adv = 1;
@@ -2557,7 +2616,7 @@ __device__ MK_OUTLINE void final_consume(const KParams& p, CSmem& cs, int step, 
 // ------------------------------------------------------------------------------------------------
 // the two roles
 // ------------------------------------------------------------------------------------------------
-__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, int32_t* uni) {
+__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, int32_t* uni, TcBlock* tc_blk) {
   const int lane = threadIdx.x & 31;
   uint32_t chunk = 0;
   const uint32_t ring_base = smem_u32(rg.base);
@@ -2566,6 +2625,7 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
   mc.q0 = pc.q0 = q0;
   mc.q1 = pc.q1 = q1;
   mc.step = pc.step = 0;
+  mc.blk = pc.blk = tc_blk;
   mc.kind = pc.kind = 0;
   mc.uni = pc.uni = uni;
   const void* src = nullptr;
@@ -2586,14 +2646,13 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
     if (mc.tma) {
       // one 2D TMA box per (segment, atom): segment s's atom a lands at its tile offset in the slot
       const uint32_t slot = ring_base + (chunk % kSlots) * kSlotBytes;
-      const int na = mc.na, n = mc.blk.nseg * na;
+      const TcBlock& blk = *mc.blk;
+      const int na = mc.na, n = blk.nseg * na;
       for (int idx = lane; idx < n; idx += 32) {
         const int s = idx / na, a = idx - s * na;
-        uint32_t soff = 0;
-        for (int t = 0; t < s; ++t) soff += (uint32_t)(tc_h8(mc.blk.seg[t].h) * na * 128);
-        const int h8 = tc_h8(mc.blk.seg[s].h);
-        const TmaDesc* map = p.tmaps + mc.op->tm_base + mc.blk.seg[s].m * 16 + (h8 / 8 - 1);
-        tma_load_2d(slot + soff + (uint32_t)(a * h8 * 128), map, (mc.cc + a) * 64, mc.blk.seg[s].row,
+        const int h8 = tc_h8(blk.seg[s].h);
+        const TmaDesc* map = p.tmaps + mc.op->tm_base + blk.seg[s].m * 16 + (h8 / 8 - 1);
+        tma_load_2d(slot + (uint32_t)((a * blk.rows8 + blk.seg[s].roff) * 128), map, (mc.cc + a) * 64, blk.seg[s].row,
                     &rg.full[chunk % kSlots]);
       }
     } else if (bytes) {
@@ -2815,7 +2874,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   tc_fence_after();
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
   if (tid >= kConsumerThreads) {
-    run_producer(p, rg, q0, q1, cs.uni_p);
+    run_producer(p, rg, q0, q1, cs.uni_p, reinterpret_cast<TcBlock*>(cs.uni_p));
   } else {
     TcState ts;
     ts.tmem = p.use_tc ? cs.tmem_base : 0u;

@@ -77,7 +77,7 @@ typedef struct mk_model_desc {
   int32_t n_experts, top_k, n_shared, expert_dim, expert_format;
   float route_scale;               /* routed weights = route_scale * s_sel / sum(s_sel)         */
   /* capacity of the handle */
-  int32_t max_batch;               /* sequences per call (at most 64)                          */
+  int32_t max_batch;               /* sequences the handle holds (at most 256; a call uses 64 at most)*/
   int32_t max_rows;                /* query rows per sequence per call (at most 8; a call's batch x
                                       rows may not exceed 64)                                    */
   int32_t max_ctx;                 /* positions per sequence (KV / latent cache length)         */
@@ -151,7 +151,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
  * sequence has n_tokens committed tokens and the next mk_decode_step must pass positions[b] =
  * n_tokens. Runs ceil(n_tokens / max_rows) launches of the decode kernel with all rows accepted and
  * no LM head. Asynchronous on `stream`; `tokens` must stay valid until the work completes.
- * Errors: MK_ERR_INVALID_ARG (batch outside 1..max_batch, n_tokens outside 1..max_ctx).
+ * Errors: MK_ERR_INVALID_ARG (batch outside 1..min(max_batch, 64), n_tokens outside 1..max_ctx).
  * Passage: the pages define no prefill call; their benchmark decodes after a context of about a thousand
  * positions (Kimi K3's TPU megakernel, "Acceptance length and batch size"), and this call builds such a
  * context's caches and states. */
