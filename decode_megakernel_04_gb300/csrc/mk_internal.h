@@ -176,7 +176,7 @@ struct KParams {
   const uint16_t* embed;
   // activations
   float* x;                 // [N, d] residual stream
-  float* ssq;               // [slots][n_sm][kMaxN] RMS partials (sum of squares)
+  float* ssq;               // [slots][kMaxN][n_sm] RMS partials (sum of squares per row and SM)
   float2* amax_part;        // [n_sm][kMaxN] (value, index) LM-head argmax partials
   float* attn_part;         // attention chunk partials
   int32_t attn_part_stride; // floats per partial record

@@ -33,14 +33,10 @@ namespace MK_VARIANT_NS {
 
 constexpr bool kFull = MK_VARIANT_FULL != 0;
 
-// The full build compiles every op handler out of line: each gets its own register allocation, and the
-// kernel's main loop stops spilling (measured: the MoE / MLA stack runs 2x faster). In the dense build the
-// handlers stay inline, which measured faster there at 1, 2 and 8 rows.
-#if MK_VARIANT_FULL
+// Every op handler is compiled out of line: each gets its own register allocation within the kernel's
+// 168-register budget (288 threads per CTA), and the kernel's main loop stops spilling (measured: the MoE /
+// MLA stack runs 2x faster; the dense stack 17% faster at 8 rows and the same at 1 row).
 #define MK_OUTLINE __noinline__
-#else
-#define MK_OUTLINE
-#endif
 constexpr int kStatusTimeout = 5;
 constexpr int kStatusDevice = 6;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -225,6 +221,12 @@ __device__ __forceinline__ bool ring_acquire(const Ring& rg, uint32_t chunk, uin
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
+}
+
+// RMSNorm partials: sum of squares of activation row n over the columns SM `sm` owns, for norm point `slot`;
+// laid out [slot][row][SM] so the 32 lanes reading one row's partials read consecutive words
+__device__ __forceinline__ size_t ssq_index(const KParams& p, int slot, int n, int sm) {
+  return ((size_t)slot * kMaxN + n) * p.n_sm + sm;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -415,7 +417,7 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
   }
 }
 
-__device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
+__device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
                                  CSmem& cs, float* act, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int sm = blockIdx.x;
@@ -431,7 +433,7 @@ __device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr
   if (norm) {
     for (int n = warp; n < N; n += kConsumerWarps) {
       float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
       s = warp_sum(s);
       if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
     }
@@ -551,7 +553,7 @@ __device__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr
       if (op.out_kind == OUT_RESID) {
         float s2 = 0.f;
         for (int i = 0; i < 16; ++i) s2 += cs.sq[i * N + ctid];
-        if (op.ssq_out >= 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], s2);
+        if (op.ssq_out >= 0) __stcg(&p.ssq[ssq_index(p, op.ssq_out, ctid, sm)], s2);
       } else {
         float bv = -CUDART_INF_F;
         int bi = 0x7fffffff;
@@ -712,7 +714,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 // + r * 128, its 16-byte chunk c at + ((c ^ (r & 7)) << 4). Warps 1..7 do this; inputs past K are zero.
 __device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, const CSmem& cs, uint8_t* buf, int a0,
                                          int a1, int stid, int nthr) {
-  constexpr int kBatch = 4;  // items whose loads are all in flight before any of them is converted
+  constexpr int kBatch = 8;  // items whose loads are all in flight before any of them is converted
   const bool norm = op.in_kind == IN_NORM;
   const int N = p.N, K = op.K, nc = op.ncols;
   const int pairs = nc >> 1;                 // activation rows incl. the zero padding
@@ -788,7 +790,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
   if (norm) {
     for (int n = warp; n < N; n += kConsumerWarps) {
       float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
       s = warp_sum(s);
       if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
     }
@@ -930,7 +932,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
       if (op.out_kind == OUT_RESID) {
         float s = 0.f;
         for (int w = 0; w < kConsumerWarps; ++w) s += pred[w * 64 + ctid];
-        if (op.ssq_out >= 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], s);
+        if (op.ssq_out >= 0) __stcg(&p.ssq[ssq_index(p, op.ssq_out, ctid, sm)], s);
       } else {
         float bv = -CUDART_INF_F;
         int bi = 0x7fffffff;
@@ -1030,7 +1032,7 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
     // 1/rms of each input row from the per-SM partial sums of squares: warp per row, lanes over SMs
     for (int n = warp; n < N; n += kConsumerWarps) {
       float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
       s = warp_sum(s);
       if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
     }
@@ -1176,7 +1178,7 @@ __device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in
     }
   }
   if (op.out_kind == OUT_RESID && op.ssq_out >= 0 && ctid < N)
-    __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + sm) * kMaxN + ctid], cs.ssq_acc[ctid]);
+    __stcg(&p.ssq[ssq_index(p, op.ssq_out, ctid, sm)], cs.ssq_acc[ctid]);
   if (op.out_kind == OUT_LOGITS && ctid < N)
     p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(cs.best_val[ctid], __int_as_float(cs.best_idx[ctid]));
 }
@@ -1204,7 +1206,7 @@ __device__ MK_OUTLINE void embed_consume(const KParams& p, const OpDesc& op, con
       s += v * v;
     }
     s = warp_sum(s);
-    if (lane == 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + blockIdx.x) * kMaxN + n], s);
+    if (lane == 0) __stcg(&p.ssq[ssq_index(p, op.ssq_out, n, blockIdx.x)], s);
   }
 }
 
@@ -1829,7 +1831,7 @@ __device__ __noinline__ void moe_consume(const KParams& p, const OpDesc& op, con
   if (up) {
     for (int n = warp; n < N; n += kConsumerWarps) {
       float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[((size_t)op.ssq_in * p.n_sm + q) * kMaxN + n]);
+      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
       s = warp_sum(s);
       if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)p.d + p.eps);
     }
@@ -1989,7 +1991,7 @@ __device__ __noinline__ void moe_consume(const KParams& p, const OpDesc& op, con
         s += xn * xn;
       }
       s = warp_sum(s);
-      if (lane == 0) __stcg(&p.ssq[((size_t)op.ssq_out * p.n_sm + blockIdx.x) * kMaxN + n], s);
+      if (lane == 0) __stcg(&p.ssq[ssq_index(p, op.ssq_out, n, blockIdx.x)], s);
     }
   }
 }
