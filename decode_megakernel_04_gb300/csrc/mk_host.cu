@@ -408,6 +408,19 @@ void gemv_op(Builder& bld, OpDesc d, int N) {
   }
   const int kpart = round_up((d.K + parts - 1) / parts, 16);
   const int ssq_out = d.ssq_out;
+  // mma.sync chunks: as many inputs per row as keep a chunk of the op's largest row group (plus the 16-byte row
+  // padding) within one ring slot, so SMs with few rows still move ~32 KB per chunk
+  int kc_mma = kMmaSlice;
+  {
+    const int glog = d.out_kind == OUT_SWIGLU ? 8 : 16;
+    int nl_max = 1;
+    for (int n : {d.rows / bld.n_sm, (d.rows + bld.n_sm - 1) / bld.n_sm}) {
+      if (n <= 0) continue;
+      const int ng = (n + glog - 1) / glog;
+      nl_max = std::max(nl_max, (n + ng - 1) / ng * (d.out_kind == OUT_SWIGLU ? 2 : 1));
+    }
+    kc_mma = std::max(kMmaSlice, ((kSlotBytes / nl_max - 16) / 2) / 16 * 16);
+  }
   for (int part = 0; part < parts; ++part) {
     OpDesc q = d;
     q.k_begin = part * kpart;
@@ -415,7 +428,7 @@ void gemv_op(Builder& bld, OpDesc d, int N) {
     q.ssq_out = (part == parts - 1) ? ssq_out : -1;
     q.mma = fits_mma(q.K) ? 1 : 0;
     q.staged = (!q.mma && fits_staged(q.K)) ? 1 : 0;
-    q.kc = q.mma ? kMmaSlice : kChunkBytes / 2 / q.rg;
+    q.kc = q.mma ? kc_mma : kChunkBytes / 2 / q.rg;
     const int op = bld.add(q);
     for (int s = 0; s < bld.n_sm; ++s) {
       const int r0 = (int)((int64_t)q.rows * s / bld.n_sm);

@@ -467,12 +467,15 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
     const int g0 = gemv_group_row(in.a, nrows, ng, grp);
     const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    // a group of fewer than 16 weight rows reads its last row again in the unused tile rows, so that the 16-row
+    // tile never reaches past the rows the chunk holds (a chunk of few rows is wider than one of 16)
+    const int lr = min(lrow, (swiglu ? 2 * nl : nl) - 1);
     for (int k0 = 0; k0 < K; k0 += KC) {
       const int kw = min(KC, K - k0);
       const int pitch = kw * 2 + 16;
       const int nsteps = kw >> 4;
       ring_wait_full(rg, chunk, p);
-      const uint32_t abase = ring_s + (chunk % kSlots) * kSlotBytes + lrow * pitch + lk * 2;
+      const uint32_t abase = ring_s + (chunk % kSlots) * kSlotBytes + lr * pitch + lk * 2;
       int s = warp;
       for (; s + kConsumerWarps < nsteps; s += 2 * kConsumerWarps) {
         uint32_t a0, a1, a2, a3, c0, c1, c2, c3;

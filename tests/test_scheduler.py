@@ -87,7 +87,13 @@ def check_program(cfg, n_sm, B, R, head=True):
             partition(k, o["rows"])
             assert 0 <= o["k_begin"] and o["k_begin"] + o["K"] <= o["ldw"]
             if o["mma"] == 1:
-                assert N <= 4 and o["K"] % 16 == 0 and o["kc"] == 1024 and o["rg"] == 16
+                # chunks of up to one 33 KB ring slot: the largest row group x (kc inputs + 8 pad) x 2 bytes
+                assert N <= 4 and o["K"] % 16 == 0 and o["kc"] >= 1024 and o["kc"] % 16 == 0 and o["rg"] == 16
+                rows_max = -(-o["rows"] // n_sm)
+                glog = 8 if o["out_kind"] == 2 else 16
+                ng = -(-rows_max // glog)
+                nl = -(-rows_max // ng) * (2 if o["out_kind"] == 2 else 1)
+                assert nl * (o["kc"] * 2 + 16) <= 33 * 1024 or o["kc"] == 1024
             elif o["mma"] == 2:
                 # tcgen05: 5 to 64 rows, rows cut in 8-row units (the TMA box heights), K parts of 256 / ncols atoms
                 ncols = -(-2 * N // 16) * 16
