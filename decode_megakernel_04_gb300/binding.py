@@ -45,7 +45,8 @@ class LayerWeights(C.Structure):
 
 
 class Weights(C.Structure):
-    _fields_ = [("embed", _P), ("final_norm", _P), ("lm_head", _P), ("layers", LayerWeights * MK_MAX_LAYERS)]
+    _fields_ = [("embed", _P), ("final_norm", _P), ("lm_head", _P), ("layers", LayerWeights * MK_MAX_LAYERS),
+                ("packed", _P)]
 
 
 class Info(C.Structure):
@@ -57,8 +58,11 @@ PLAN_OP_FIELDS = ["type", "n_instr", "layer", "rows", "K", "k_begin", "ldw", "mm
                   "out_kind", "nchunk", "groups", "head_dim", "n_heads", "n_kv_heads", "col_group"]
 
 
+PLAN_OP_FIELDS += ["ncols", "pa0", "patoms", "pk_offset"]
+
+
 class PlanOp(C.Structure):
-    _fields_ = [(f, _I) for f in PLAN_OP_FIELDS]
+    _fields_ = [(f, _I) for f in PLAN_OP_FIELDS[:-1]] + [("pk_offset", C.c_int64)]
 
 
 class PlanInstr(C.Structure):
@@ -73,7 +77,8 @@ class StateBuffers(C.Structure):
 EXPORTS = ["mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status",
            "mk_last_error", "mk_get_info", "mk_destroy", "mk_decode_step_static", "mk_set_routing_log",
            "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
-           "mk_set_routing_override", "mk_decode_steps", "mk_decode_steps_host", "mk_verify_step"]
+           "mk_set_routing_override", "mk_decode_steps", "mk_decode_steps_host", "mk_verify_step",
+           "mk_packed_weight_bytes", "mk_pack_weights"]
 
 _lib = None
 
@@ -113,7 +118,9 @@ def load(path: str | None = None) -> C.CDLL:
                             C.POINTER(C.c_int)]
     lib.mk_decode_step_static.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.POINTER(StateBuffers),
                                           _P, _P, C.c_int, C.c_int, _P, _P, _P]
-    for f in ("mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
+    lib.mk_packed_weight_bytes.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.c_int, C.POINTER(C.c_uint64)]
+    lib.mk_pack_weights.argtypes = [C.POINTER(ModelDesc), C.POINTER(Weights), C.c_int, _P, _P]
+    for f in ("mk_packed_weight_bytes", "mk_pack_weights", "mk_create", "mk_prefill_kv", "mk_decode_step", "mk_decode_step_host", "mk_get_status", "mk_get_info",
               "mk_decode_step_static", "mk_set_routing_log", "mk_fork_sequence", "mk_plan", "mk_set_wait_limit",
               "mk_set_routing_override", "mk_decode_steps", "mk_decode_steps_host", "mk_verify_step"):
         getattr(lib, f).restype = C.c_int
@@ -140,6 +147,22 @@ def plan(desc: ModelDesc, weights: Weights, n_sm: int, batch: int, rows: int, he
     as_dict = lambda r, names: {f: getattr(r, f) for f in names}
     return ([as_dict(ops[i], PLAN_OP_FIELDS) for i in range(n_ops.value)],
             [as_dict(ins[i], ("op", "sm", "a", "b", "c")) for i in range(n_instr.value)])
+
+
+def packed_weight_bytes(desc: ModelDesc, weights: Weights, device: int = 0) -> int:
+    """mk_packed_weight_bytes: size of the tiled copy of the projection matrices on `device`."""
+    n = C.c_uint64(0)
+    rc = load().mk_packed_weight_bytes(C.byref(desc), C.byref(weights), device, C.byref(n))
+    if rc != MK_OK:
+        raise MKError(rc, "mk_packed_weight_bytes")
+    return n.value
+
+
+def pack_weights(desc: ModelDesc, weights: Weights, packed_ptr: int, device: int = 0, stream: int = 0) -> None:
+    """mk_pack_weights: fill the caller's device buffer (packed_weight_bytes long, 1024-byte aligned)."""
+    rc = load().mk_pack_weights(C.byref(desc), C.byref(weights), device, packed_ptr, stream or None)
+    if rc != MK_OK:
+        raise MKError(rc, "mk_pack_weights")
 
 
 class MKError(RuntimeError):
@@ -200,12 +223,16 @@ def weight_table(cfg, w: dict) -> Weights:
 class Megakernel:
     """One handle of the C library: a model on one GPU plus its caches and states."""
 
-    def __init__(self, cfg, weights: dict, max_batch: int, max_rows: int, max_ctx: int, device: int = 0):
+    def __init__(self, cfg, weights: dict, max_batch: int, max_rows: int, max_ctx: int, device: int = 0,
+                 packed: int = 0):
+        """packed: device address of a tiled copy of the projection matrices written by pack_weights for this
+        model (kept alive by the caller), or 0 to let the handle make its own."""
         self.lib = load()
         self.cfg = cfg
         self._weights = weights  # keep the tensors alive for the handle's lifetime
         self.desc = model_desc(cfg, max_batch, max_rows, max_ctx)
         self.wtab = weight_table(cfg, weights)
+        self.wtab.packed = packed or None
         h = _P()
         rc = self.lib.mk_create(C.byref(self.desc), C.byref(self.wtab), device, C.byref(h))
         if rc != MK_OK:

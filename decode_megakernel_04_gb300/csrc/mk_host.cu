@@ -1,7 +1,6 @@
 // Host side of libmk: the C ABI (include/mk.h), the device memory plan of a handle, and the scheduler
 // that compiles one decode step of the layer stack into per-SM instruction queues for the persistent
 // kernel (mk_kernel.cuh, built as mk_kernel_dense.cu and mk_kernel_full.cu).
-#include <cuda.h>  // CUtensorMap and the tensor-map encoder's types (the function comes from the runtime)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -31,6 +30,7 @@ cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream);
 }  // namespace full
 cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream);
 cudaError_t fill_i32_launch(int32_t* dst, int n, int32_t value, cudaStream_t stream);
+cudaError_t pack_gemv_launch(uint8_t* dst, const PackSrc& src, cudaStream_t stream);
 }  // namespace mk
 
 using namespace mk;
@@ -49,13 +49,49 @@ struct Program {
   OpDesc* d_ops = nullptr;
   Instr* d_instr = nullptr;
   int32_t* d_qoff = nullptr;
-  TmaDesc* d_tmaps = nullptr;  // tensor maps of the tcgen05 GEMV ops
   int n_ops = 0;
   int n_instr = 0;
-  int n_tmaps = 0;
+  bool use_tc = false;  // the program has tcgen05 GEMV ops (the kernel allocates TMEM)
 };
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// The packed GEMV weights of a model (layout in mk_internal.h): one group per set of matrices a GEMV op
+// reads, in the order the step program first meets them, each at a 1024-byte aligned offset of one copy.
+// The groups depend on the model and the SM count only, so every step shape finds its groups here.
+struct PackTable {
+  struct Group {
+    PackSrc src;
+    size_t offset;
+  };
+  std::vector<Group> groups;
+  size_t total = 0;
+  const uint8_t* base = nullptr;  // device address of the copy (never dereferenced on the host)
+  int n_sm = 0;
+
+  // device address of the packed group of GEMV `d` (its first matrix, width, rows, SwiGLU pairing), adding
+  // the group on first sight
+  const uint8_t* find(const OpDesc& d) {
+    const int sw = d.out_kind == OUT_SWIGLU ? 1 : 0;
+    for (const Group& g : groups)
+      if (g.src.w[0] == d.w[0] && g.src.K == d.K && g.src.rows == d.rows && g.src.swiglu == sw) return base + g.offset;
+    Group g;
+    std::memset(&g, 0, sizeof(g));
+    for (int m = 0; m < d.n_mat; ++m) {
+      g.src.w[m] = d.w[m];
+      g.src.mat_rows[m] = d.mat_rows[m];
+    }
+    g.src.n_mat = d.n_mat;
+    g.src.rows = d.rows;
+    g.src.K = d.K;
+    g.src.swiglu = sw;
+    g.src.n_sm = n_sm;
+    g.offset = total;
+    total += (size_t)((pk_bytes(d.rows, d.K, sw) + 1023) / 1024 * 1024);
+    groups.push_back(g);
+    return base + g.offset;
+  }
+};
 
 }  // namespace
 
@@ -121,6 +157,8 @@ struct mk_handle {
   int max_ops = 0;
   int n_ops_last = 0;
   std::deque<Program> programs;  // stable addresses: launches and the trace keep pointers into it
+  PackTable pk;                  // packed GEMV weights: the groups and the copy's address
+  void* packed_own = nullptr;    // the copy when this handle made it (NULL: the caller's mk_weights.packed)
   // optional per-instruction timestamp trace of the last step (env MK_TRACE=<file>), written at destroy
   std::string trace_path;
   unsigned long long* trace = nullptr;
@@ -329,9 +367,10 @@ size_t attn_part_records(const mk_handle* h, int B, int R) {
 // ------------------------------------------------------------------------------------------------
 struct Builder {
   int n_sm;
+  PackTable* pk;
   std::vector<OpDesc> ops;
   std::vector<std::vector<Instr>> q;
-  explicit Builder(int n) : n_sm(n), q(n) {}
+  Builder(int n, PackTable* table) : n_sm(n), pk(table), q(n) {}
 
   int add(OpDesc d) {
     const int idx = (int)ops.size();
@@ -362,79 +401,52 @@ OpDesc blank(int type) {
   return d;
 }
 
-// One instruction per SM over a balanced range of output rows. Up to 4 activation rows take the tensor-core
-// path (inputs staged in shared memory as bf16 hi/lo pairs) when they fit the staging area; up to 2 rows
-// otherwise use the CUDA-core path with fp32 inputs staged; more rows read their inputs from L2 per chunk.
-// A residual-add GEMV whose input does not fit is split along K into sequential ops that each add their
-// part to x (the last one also writes the RMS partials of the new x).
-constexpr int kMmaSlice = 1024;  // 64 k-steps of 16; 16 rows x (1024 * 2 + 16) bytes fit one slot
-
-// 5 to 64 rows take the tcgen05 path when every matrix but the last has a multiple of 8 rows (its row blocks are
-// cut in 8-row units: one TMA box height per segment); one instruction per SM over a balanced run of 8-row units.
-bool tc_eligible(const OpDesc& d, int N) {
-  if (N <= 4 || N > kMaxN || d.K % 8 != 0 || d.K < 64) return false;
-  for (int m = 0; m + 1 < d.n_mat; ++m)
-    if (d.mat_rows[m] % 8 != 0) return false;
-  return true;
-}
-
+// A GEMV op reads the packed copy of its weights. Every SM takes a share of whole 8-row units (the packed row
+// blocks are cut from the shares). Up to 4 activation rows take the mma.sync path when their bf16 hi / lo
+// columns (and, for a residual add, the SM's slice of x) fit the staging area; a residual-add GEMV whose input
+// does not fit is split along K into sequential ops over runs of whole atoms that each add their part to x
+// (the last one also writes the RMS partials of the new x). Everything else takes the tcgen05 path.
 void gemv_op(Builder& bld, OpDesc d, int N) {
   d.type = OP_GEMV;
-  d.rg = (N <= 4) ? 16 : 8;
-  d.passes = (N <= 8) ? 1 : (N + 7) / 8;
   d.ldw = d.K;
   d.k_begin = 0;
-  if (tc_eligible(d, N)) {
+  d.wp = bld.pk->find(d);
+  d.patoms = pk_atoms(d.K);
+  d.pa0 = 0;
+  const int A = d.patoms;
+  auto place_all = [&](int op) {
+    for (int s = 0; s < bld.n_sm; ++s)
+      bld.place(op, s, pk_split(d.rows, bld.n_sm, s), pk_split(d.rows, bld.n_sm, s + 1), 0);
+  };
+  // a residual-add instruction also keeps its slice of x (N x its rows) in the staging area
+  int64_t xrows = 0;
+  if (d.out_kind == OUT_RESID)
+    for (int s = 0; s < bld.n_sm; ++s)
+      xrows = std::max<int64_t>(xrows, pk_split(d.rows, bld.n_sm, s + 1) - pk_split(d.rows, bld.n_sm, s));
+  const int64_t cap = kActBytes / 4 - 8;  // floats
+  auto fits_mma = [&](int atoms) { return N <= 4 && (int64_t)N * (atoms * 64 + 8 + xrows) <= cap; };
+  int pa = A;  // atoms per K part
+  if (!fits_mma(pa) && N <= 4 && d.out_kind == OUT_RESID) {
+    int parts = 2;
+    while (parts <= 16 && !fits_mma((A + parts - 1) / parts)) ++parts;
+    pa = (A + parts - 1) / parts;
+  }
+  if (!fits_mma(pa)) {
     d.mma = 2;
     d.ncols = round_up(2 * N, 16);
-    d.kc = 64 * (256 / d.ncols);  // inputs per K part
-    const int op = bld.add(d);
-    const int units = (d.rows + 7) / 8;
-    for (int s = 0; s < bld.n_sm; ++s) {
-      const int u0 = (int)((int64_t)units * s / bld.n_sm), u1 = (int)((int64_t)units * (s + 1) / bld.n_sm);
-      bld.place(op, s, std::min(8 * u0, d.rows), std::min(8 * u1, d.rows), 0);
-    }
+    place_all(bld.add(d));
     return;
   }
-  // a residual-add instruction also keeps its slice of x (N x its rows) in the staging area
-  const int64_t xrows = d.out_kind == OUT_RESID ? (d.rows + bld.n_sm - 1) / bld.n_sm : 0;
-  const int64_t cap = kActBytes / 4 - 8;  // floats
-  auto fits_mma = [&](int k) { return N <= 4 && k % 16 == 0 && (int64_t)N * (k + 8 + xrows) <= cap; };
-  auto fits_staged = [&](int k) { return N <= 2 && (int64_t)N * (k + xrows) <= cap; };
-  int parts = 1;
-  if (d.out_kind == OUT_RESID && N <= 4 && d.K % 16 == 0) {
-    while (!fits_mma(round_up((d.K + parts - 1) / parts, 16)) && parts < 16) ++parts;
-    if (!fits_mma(round_up((d.K + parts - 1) / parts, 16))) parts = 1;
-  }
-  const int kpart = round_up((d.K + parts - 1) / parts, 16);
+  const int parts = (A + pa - 1) / pa;
   const int ssq_out = d.ssq_out;
-  // mma.sync chunks: as many inputs per row as keep a chunk of the op's largest row group (plus the 16-byte row
-  // padding) within one ring slot, so SMs with few rows still move ~32 KB per chunk
-  int kc_mma = kMmaSlice;
-  {
-    const int glog = d.out_kind == OUT_SWIGLU ? 8 : 16;
-    int nl_max = 1;
-    for (int n : {d.rows / bld.n_sm, (d.rows + bld.n_sm - 1) / bld.n_sm}) {
-      if (n <= 0) continue;
-      const int ng = (n + glog - 1) / glog;
-      nl_max = std::max(nl_max, (n + ng - 1) / ng * (d.out_kind == OUT_SWIGLU ? 2 : 1));
-    }
-    kc_mma = std::max(kMmaSlice, ((kSlotBytes / nl_max - 16) / 2) / 16 * 16);
-  }
   for (int part = 0; part < parts; ++part) {
     OpDesc q = d;
-    q.k_begin = part * kpart;
-    q.K = std::min(kpart, d.ldw - q.k_begin);
+    q.mma = 1;
+    q.pa0 = part * pa;
+    q.k_begin = q.pa0 * kPackAtom;
+    q.K = std::min(pa * kPackAtom, d.ldw - q.k_begin);
     q.ssq_out = (part == parts - 1) ? ssq_out : -1;
-    q.mma = fits_mma(q.K) ? 1 : 0;
-    q.staged = (!q.mma && fits_staged(q.K)) ? 1 : 0;
-    q.kc = q.mma ? kc_mma : kChunkBytes / 2 / q.rg;
-    const int op = bld.add(q);
-    for (int s = 0; s < bld.n_sm; ++s) {
-      const int r0 = (int)((int64_t)q.rows * s / bld.n_sm);
-      const int r1 = (int)((int64_t)q.rows * (s + 1) / bld.n_sm);
-      bld.place(op, s, r0, r1, 0);
-    }
+    place_all(bld.add(q));
   }
 }
 
@@ -665,67 +677,14 @@ struct HostProgram {
   std::vector<OpDesc> ops;
   std::vector<Instr> flat;
   std::vector<int32_t> qoff;
-  std::vector<TmaDesc> tmaps;  // filled by encode_tmaps (needs the driver), not by construct_program
 };
-
-// cuTensorMapEncodeTiled, resolved once through the runtime (no link against the driver library)
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn tensor_map_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// Tensor maps of the program's tcgen05 GEMV ops: for each op (tm_base = its first map) and each of its weight
-// matrices, 16 maps with box heights 8, 16, .., 128 rows and a 64-input (128-byte) box width, 128-byte swizzle:
-// a box lands in shared memory as the K-major, 128B-swizzled tile tcgen05.mma reads. Heights above the
-// matrix's rows (rounded up to 8) are never used and stay zero. Rows and inputs past the matrix are filled
-// with zeros by the copy.
-mk_status encode_tmaps(mk_handle* h, HostProgram& hp) {
-  hp.tmaps.clear();
-  for (OpDesc& o : hp.ops) {
-    if (o.type != OP_GEMV || o.mma != 2) continue;
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return fail(h, MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    o.tm_base = (int)hp.tmaps.size();
-    for (int m = 0; m < o.n_mat; ++m) {
-      for (int hb = 1; hb <= 16; ++hb) {
-        TmaDesc d;
-        std::memset(&d, 0, sizeof(d));
-        if (8 * hb <= round_up(o.mat_rows[m], 8)) {
-          const cuuint64_t dims[2] = {(cuuint64_t)o.ldw, (cuuint64_t)o.mat_rows[m]};
-          const cuuint64_t strides[1] = {(cuuint64_t)o.ldw * 2};
-          const cuuint32_t box[2] = {64, (cuuint32_t)(8 * hb)};
-          const cuuint32_t es[2] = {1, 1};
-          const CUresult r = enc(reinterpret_cast<CUtensorMap*>(&d), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 const_cast<uint16_t*>(o.w[m]), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-          if (r != CUDA_SUCCESS)
-            return fail(h, MK_ERR_CUDA, "tensor map of a %d x %d weight matrix (box 64 x %d): error %d", o.mat_rows[m],
-                        o.ldw, 8 * hb, (int)r);
-        }
-        hp.tmaps.push_back(d);
-      }
-    }
-  }
-  return MK_OK;
-}
 
 mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& hp) {
   const mk_model_desc& D = h->desc;
   const int N = B * R;
   const int d = D.d_model;
-  Builder bld(h->n_sm);
+  h->pk.n_sm = h->n_sm;
+  Builder bld(h->n_sm, &h->pk);
 
   {  // embedding
     OpDesc e = blank(OP_EMBED);
@@ -889,13 +848,6 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
     bld.place(op, 0, 0, 0, 0);
   }
 
-  for (const OpDesc& o : bld.ops) {
-    if (o.type != OP_GEMV || o.out_kind != OUT_RESID) continue;
-    const int64_t xrows = (o.rows + h->n_sm - 1) / h->n_sm;
-    if ((int64_t)N * ((o.staged ? o.K : 0) + xrows) * 4 > kActBytes)
-      return fail(h, MK_ERR_UNSUPPORTED, "residual slice of %d rows x %lld outputs exceeds the staging area", N,
-                  (long long)xrows);
-  }
   if ((int)bld.ops.size() > h->max_ops)
     return fail(h, MK_ERR_UNSUPPORTED, "program has %d ops, more than the %d counters allocated",
                 (int)bld.ops.size(), h->max_ops);
@@ -918,7 +870,6 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
   HostProgram hp;
   *st = construct_program(h, B, R, head, hp);
   if (*st != MK_OK) return prog;
-  if ((*st = encode_tmaps(h, hp)) != MK_OK) return prog;
   const std::vector<Instr>& flat = hp.flat;
   const std::vector<int32_t>& qoff = hp.qoff;
   prog.n_ops = (int)hp.ops.size();
@@ -938,16 +889,7 @@ Program build_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     return prog;
   }
   h->bytes += (int64_t)(sizeof(OpDesc) * prog.n_ops + sizeof(Instr) * prog.n_instr + sizeof(int32_t) * (h->n_sm + 1));
-  prog.n_tmaps = (int)hp.tmaps.size();
-  if (prog.n_tmaps) {
-    if ((e = cudaMalloc(&prog.d_tmaps, sizeof(TmaDesc) * prog.n_tmaps)) != cudaSuccess ||
-        (e = cudaMemcpy(prog.d_tmaps, hp.tmaps.data(), sizeof(TmaDesc) * prog.n_tmaps, cudaMemcpyHostToDevice)) !=
-            cudaSuccess) {
-      *st = cuda_fail(h, e, "tensor map upload");
-      return prog;
-    }
-    h->bytes += (int64_t)(sizeof(TmaDesc) * prog.n_tmaps);
-  }
+  for (const OpDesc& o : hp.ops) prog.use_tc = prog.use_tc || (o.type == OP_GEMV && o.mma == 2);
   return prog;
 }
 
@@ -960,7 +902,6 @@ Program* get_program(mk_handle* h, int B, int R, bool head, mk_status* st) {
     cudaFree(p.d_ops);
     cudaFree(p.d_instr);
     cudaFree(p.d_qoff);
-    cudaFree(p.d_tmaps);
     return nullptr;
   }
   h->programs.push_back(p);
@@ -981,8 +922,7 @@ mk_status launch_program(mk_handle* h, const Program* prog, const int32_t* token
   p.status = h->status;
   p.abort_flag = h->abort_flag;
   p.timeout_ns = h->wait_limit_ns;
-  p.tmaps = prog->d_tmaps;
-  p.use_tc = prog->n_tmaps > 0 ? 1 : 0;
+  p.use_tc = prog->use_tc ? 1 : 0;
   p.spin_mask = h->wait_limit_ns < 1000000ull ? 0u : 63u;
   p.n_ops = prog->n_ops;
   p.n_sm = h->n_sm;
@@ -1053,12 +993,88 @@ mk_status launch_step(mk_handle* h, const int32_t* tokens, int tok_stride, const
                         accept_out);
 }
 
+// The packed GEMV weights of a handle: the groups are collected from the decode program of one row (every
+// step shape reads the same groups), then the caller's copy is taken, or one is made here.
+mk_status make_packed(mk_handle* h) {
+  HostProgram hp;
+  h->pk = PackTable();
+  mk_status st = construct_program(h, 1, 1, true, hp);
+  if (st != MK_OK) return st;
+  if (h->w.packed) {
+    if (reinterpret_cast<uintptr_t>(h->w.packed) & 1023u) return fail(h, MK_ERR_INVALID_ARG, "packed weights not 1024-byte aligned");
+    h->pk.base = static_cast<const uint8_t*>(h->w.packed);
+    return MK_OK;
+  }
+  cudaError_t e = cudaMalloc(&h->packed_own, std::max<size_t>(h->pk.total, 1024));
+  if (e != cudaSuccess) {
+    h->packed_own = nullptr;
+    return cuda_fail(h, e, "packed weights");
+  }
+  h->bytes += (int64_t)h->pk.total;
+  h->pk.base = static_cast<const uint8_t*>(h->packed_own);
+  for (const PackTable::Group& g : h->pk.groups)
+    if ((e = pack_gemv_launch(static_cast<uint8_t*>(h->packed_own) + g.offset, g.src, 0)) != cudaSuccess)
+      return cuda_fail(h, e, "weight packing");
+  return MK_OK;
+}
+
+// A shape-only handle for the calls that take a model without creating one (layout and packing).
+mk_status shape_handle(mk_handle& tmp, const mk_model_desc* desc, const mk_weights* weights, int device) {
+  tmp.desc = *desc;
+  tmp.w = *weights;
+  tmp.device = device;
+  mk_status st = check_desc(&tmp, tmp.desc, tmp.w);
+  if (st != MK_OK) return st;
+  if (cudaDeviceGetAttribute(&tmp.n_sm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || tmp.n_sm < 1)
+    return MK_ERR_CUDA;
+  derive_layout(&tmp);
+  HostProgram hp;
+  return construct_program(&tmp, 1, 1, true, hp);
+}
+
 }  // namespace
 
 // ==================================================================================================
 // C ABI
 // ==================================================================================================
 extern "C" {
+
+mk_status mk_packed_weight_bytes(const mk_model_desc* desc, const mk_weights* weights, int device, uint64_t* bytes) {
+  if (!desc || !weights || !bytes) return MK_ERR_INVALID_ARG;
+  mk_handle tmp;
+  const mk_status st = shape_handle(tmp, desc, weights, device);
+  if (st != MK_OK) {
+    if (!tmp.err.empty()) fprintf(stderr, "mk_packed_weight_bytes: %s\n", tmp.err.c_str());
+    return st;
+  }
+  *bytes = (uint64_t)tmp.pk.total;
+  return MK_OK;
+}
+
+mk_status mk_pack_weights(const mk_model_desc* desc, const mk_weights* weights, int device, void* packed,
+                          void* stream) {
+  if (!desc || !weights || !packed) return MK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(packed) & 1023u) return MK_ERR_INVALID_ARG;
+  mk_handle tmp;
+  const mk_status st = shape_handle(tmp, desc, weights, device);
+  if (st != MK_OK) {
+    if (!tmp.err.empty()) fprintf(stderr, "mk_pack_weights: %s\n", tmp.err.c_str());
+    return st;
+  }
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return MK_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  for (const PackTable::Group& g : tmp.pk.groups) {
+    e = pack_gemv_launch(static_cast<uint8_t*>(packed) + g.offset, g.src, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) break;
+  }
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "mk_pack_weights: %s\n", cudaGetErrorString(e));
+    return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
 
 mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int device, mk_handle** out) {
   if (!desc || !weights || !out) return MK_ERR_INVALID_ARG;
@@ -1154,6 +1170,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     ALLOC(trace, h->trace_cap * kTraceWords);
   }
 #undef ALLOC
+  if ((st = make_packed(h)) != MK_OK) goto fail_out;
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
     st = cuda_fail(h, e, "create");
     goto fail_out;
@@ -1347,6 +1364,10 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_weights* weights, int n_sm
     r.n_heads = o.n_heads;
     r.n_kv_heads = o.n_kv_heads;
     r.col_group = o.col_group;
+    r.ncols = o.ncols;
+    r.pa0 = o.pa0;
+    r.patoms = o.patoms;
+    r.pk_offset = o.type == OP_GEMV ? (int64_t)(o.wp - tmp.pk.base) : 0;
   }
   if (instrs) {
     int k = 0;
@@ -1463,8 +1484,8 @@ void mk_destroy(mk_handle* h) {
     cudaFree(p.d_ops);
     cudaFree(p.d_instr);
     cudaFree(p.d_qoff);
-    cudaFree(p.d_tmaps);
   }
+  if (h->packed_own) cudaFree(h->packed_own);
   for (void* p : h->allocs) cudaFree(p);
   if (h->stage_steps) cudaFree(h->stage_steps);
   delete h;
@@ -1600,19 +1621,19 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   tmp.epoch = state->epoch;
 
   const bool head = logits_out != nullptr || argmax_out != nullptr;
+  if (!weights->packed) {
+    fprintf(stderr, "mk_decode_step_static: mk_weights.packed is NULL (fill it once with mk_pack_weights)\n");
+    return MK_ERR_INVALID_ARG;
+  }
+  tmp.pk.base = static_cast<const uint8_t*>(weights->packed);
   HostProgram hp;
   if ((st = construct_program(&tmp, batch, rows, head, hp)) != MK_OK) {
-    fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
-    return st;
-  }
-  if ((st = encode_tmaps(&tmp, hp)) != MK_OK) {
     fprintf(stderr, "mk_decode_step_static: %s\n", tmp.err.c_str());
     return st;
   }
   const size_t o_ops = carve(off, sizeof(OpDesc) * hp.ops.size());
   const size_t o_instr = carve(off, sizeof(Instr) * hp.flat.size());
   const size_t o_qoff = carve(off, sizeof(int32_t) * hp.qoff.size());
-  const size_t o_tmaps = carve(off, sizeof(TmaDesc) * hp.tmaps.size());
   if (off > (size_t)MK_STATIC_SCRATCH_BYTES) {
     fprintf(stderr,
             "mk_decode_step_static: this step needs %zu bytes of working memory, more than the %u-byte static "
@@ -1629,15 +1650,9 @@ extern "C" mk_status mk_decode_step_static(const mk_model_desc* desc, const mk_w
   prog.d_qoff = reinterpret_cast<int32_t*>(base + o_qoff);
   prog.n_ops = (int)hp.ops.size();
   prog.n_instr = (int)hp.flat.size();
-  prog.n_tmaps = (int)hp.tmaps.size();
-  prog.d_tmaps = prog.n_tmaps ? reinterpret_cast<TmaDesc*>(base + o_tmaps) : nullptr;
+  for (const OpDesc& o : hp.ops) prog.use_tc = prog.use_tc || (o.type == OP_GEMV && o.mma == 2);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (prog.n_tmaps && (e = cudaMemcpyAsync(prog.d_tmaps, hp.tmaps.data(), sizeof(TmaDesc) * hp.tmaps.size(),
-                                           cudaMemcpyHostToDevice, s)) != cudaSuccess) {
-    fprintf(stderr, "mk_decode_step_static: %s\n", cudaGetErrorString(e));
-    return MK_ERR_CUDA;
-  }
   if ((e = cudaMemcpyAsync(prog.d_ops, hp.ops.data(), sizeof(OpDesc) * hp.ops.size(), cudaMemcpyHostToDevice, s)) !=
           cudaSuccess ||
       (e = cudaMemcpyAsync(prog.d_instr, hp.flat.data(), sizeof(Instr) * hp.flat.size(), cudaMemcpyHostToDevice,

@@ -64,17 +64,19 @@ struct OpDesc {
   // ---- GEMV ----
   int32_t K;                // input features
   int32_t rows;             // output rows (logical rows for SwiGLU)
-  int32_t rg;               // physical weight rows per row group (16 or 8)
-  int32_t ldw;              // elements between weight rows (the full input width)
+  int32_t rg;               // MoE: physical weight rows per row group (16 or 8)
+  int32_t ldw;              // the full input width of the weights (RMSNorm divides by it)
   int32_t k_begin;          // first input column of this op (an op may cover a K range of the matrix)
-  int32_t staged;           // 1: input rows staged in shared memory (fp32) for the whole instruction
-  int32_t mma;              // tensor cores: 1 = mma.sync (up to 4 rows; inputs staged whole as bf16 hi/lo
-                            // pairs, padded weight rows), 2 = tcgen05 with TMEM accumulators (5 and more rows;
-                            // weight tiles by TMA, inputs staged per K part), 0 = CUDA cores
-  int32_t tm_base;          // mma 2: first tensor map of this op (16 per matrix, box heights 8 .. 128 rows)
+  int32_t staged;           // MoE: 1 = input rows staged in shared memory (fp32) for the whole instruction
+  int32_t mma;              // GEMV tensor-core path: 1 = mma.sync (up to 4 rows; inputs staged whole as bf16
+                            // hi/lo pairs), 2 = tcgen05 with TMEM accumulators (inputs staged per K part)
   int32_t ncols;            // mma 2: TMEM columns per accumulator tile = bf16 hi / lo columns, 2 N rounded up to 16
-  int32_t kc;               // inputs per weight slice (chunk width)
-  int32_t passes;           // ceil(N / 8) when 8 activation rows are processed per pass, else 1
+  int32_t kc;               // MoE: inputs per weight slice (chunk width)
+  int32_t passes;           // MoE: ceil(N / 8) when 8 activation rows are processed per pass, else 1
+  // packed GEMV weights: the group's tiled copy, its atoms per row, and the first atom this op reads
+  const uint8_t* wp;
+  int32_t patoms;
+  int32_t pa0;
   int32_t n_mat;
   int32_t mat_rows[kMaxOpMats];
   const uint16_t* w[kMaxOpMats];
@@ -119,18 +121,57 @@ struct OpDesc {
   int32_t aux_stride;
 };
 
-// An opaque TMA tensor map (the driver's CUtensorMap: 128 bytes, 64-byte aligned), encoded on the host.
-struct alignas(64) TmaDesc {
-  uint64_t w[16];
-};
-static_assert(sizeof(TmaDesc) == 128, "tensor map size");
+// ---- packed GEMV weights -----------------------------------------------------------------------------
+// The matrices one GEMV op reads (stacked by rows: q, k, v of a projection; or the gate and up matrices of
+// a SwiGLU, paired row by row) are kept in a tiled copy made for the weight ring. Rows are shared out to the
+// SMs in whole 8-row units; each SM's share is cut into row blocks of at most 128 physical rows (SwiGLU: 64
+// logical rows, the block's gate rows then its up rows, each run rounded up to 8). A block stores its rows
+// atom by atom (64 inputs = 128 bytes of each row, inputs padded with zeros to whole atoms); inside an atom
+// row r's eight 16-byte pieces sit at positions (piece ^ (r & 7)). That is the K-major, 128-byte-swizzle
+// layout a tcgen05 descriptor reads (8-row groups 1024 bytes apart) and one ldmatrix reads without bank
+// conflicts; a ring chunk, one block over a run of atoms, is one contiguous copy. Every logical row before
+// a block's first row takes atoms x 128 bytes (x 2 for SwiGLU), so a block starting at logical row r
+// starts r x atoms x 128 (x 2) bytes into the copy.
+constexpr int kPackAtom = 64;       // inputs per atom
+constexpr int kPackBlockRows = 128; // physical rows per block at most
+#if defined(__CUDACC__)
+#define MK_HD __host__ __device__ __forceinline__
+#else
+#define MK_HD inline
+#endif
+MK_HD int pk_atoms(int K) { return (K + kPackAtom - 1) / kPackAtom; }
+// first logical row of SM s's share (s = n_sm gives the end)
+MK_HD int pk_split(int rows, int n_sm, int s) {
+  const long long units = (rows + 7) / 8;
+  const int r = 8 * (int)(units * s / n_sm);
+  return r < rows ? r : rows;
+}
+// the SM whose share holds logical row r
+MK_HD int pk_sm_of(int rows, int n_sm, int r) {
+  const long long units = (rows + 7) / 8;
+  return (int)(((long long)n_sm * (r / 8 + 1) - 1) / units);
+}
+MK_HD int pk_block_lrows(int swiglu) { return swiglu ? kPackBlockRows / 2 : kPackBlockRows; }
+// bytes of the packed copy of a group of `rows` logical rows over K inputs
+MK_HD long long pk_bytes(int rows, int K, int swiglu) {
+  return (long long)((rows + 7) & ~7) * pk_atoms(K) * 128 * (swiglu ? 2 : 1);
+}
 
-// tcgen05 GEMV geometry: accumulator tiles are 128 TMEM lanes (weight rows) x ncols columns; a row block
-// holds at most 128 physical weight rows (64 logical rows for SwiGLU: the gate and up tiles of the same
-// rows) split into segments at matrix boundaries; K is covered in K parts of 256 / ncols 64-wide atoms
-// (the staged activations of one part fill one 32 KB buffer); each ring chunk holds one row block's
-// weights over a run of atoms (at most 32 KB).
-constexpr int kTcMaxSeg = 4;      // segments (accumulator tiles) per row block
+// the caller's matrices of one GEMV weight group, as the packing kernel reads them (row-major bf16, K inputs
+// per row)
+struct PackSrc {
+  const uint16_t* w[kMaxOpMats];
+  int32_t mat_rows[kMaxOpMats];
+  int32_t n_mat;
+  int32_t rows;    // logical rows (SwiGLU: rows of each of the two matrices)
+  int32_t K;
+  int32_t swiglu;  // 1: w[0] gate and w[1] up, paired row by row
+  int32_t n_sm;
+};
+
+// tcgen05 GEMV geometry: accumulator tiles are 128 TMEM lanes (weight rows) x ncols columns; a packed row
+// block is one tile (two for SwiGLU: gate and up); K is covered in K parts of 256 / ncols atoms (the staged
+// activations of one part fill one 32 KB buffer).
 constexpr int kTcCols = 512;      // TMEM columns allocated per CTA
 constexpr int kTcBBytes = 32768;  // one staged-activation buffer (two are used)
 
@@ -154,7 +195,6 @@ struct KParams {
   int32_t* status;
   int32_t* abort_flag;
   unsigned long long timeout_ns;  // limit of every inter-SM / ring wait
-  const TmaDesc* tmaps;     // tensor maps of the program's tcgen05 GEMV ops
   int32_t use_tc;           // the program has tcgen05 ops: allocate TMEM
   uint32_t spin_mask;             // polls between clock reads, minus one (63, or 0 for limits below 1 ms)
   int32_t n_ops;

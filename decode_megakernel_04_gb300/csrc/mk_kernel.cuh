@@ -167,9 +167,7 @@ struct CSmem {
   int32_t pad[2];
   float mred[2 * kConsumerWarps * 128];  // tensor-core GEMV: two buffers of 8 warps x 16 rows x 8 cols
   int32_t uni_c[kMaxExperts + 4];        // MoE: the step's expert union, consumers' copy (count, ids)
-  // the producer warp's copy of the union during an expert op; during a tcgen05 GEMV op the same words hold
-  // the producer's current row block (a TcBlock, kept here so the producer's chunk cursor stays in registers)
-  int32_t uni_p[kMaxExperts + 4];
+  int32_t uni_p[kMaxExperts + 4];        // the producer warp's copy of the union during an expert op
   // tcgen05 GEMV: staged-activation buffer ready [2] / free [2], accumulators complete, drain at exit
   uint64_t tcbar[6];
   uint32_t tmem_base;
@@ -278,25 +276,61 @@ __device__ __forceinline__ void block_reduce(float* v, CSmem& cs, int warp, int 
 }
 
 // ------------------------------------------------------------------------------------------------
-// GEMV: out rows [a, b) of  act(in) @ W^T. Weight rows stream through the ring in chunks of
-// RG rows x KC inputs (32 KB of bf16). Thread t owns inputs [t*CPL, t*CPL + CPL) of each chunk and keeps
-// RG x NR partial sums in registers across the K slices of a row group; one block reduction per group.
+// GEMV: out rows [a, b) of  act(in) @ W^T, over the packed row blocks of the weights (mma.sync for up to
+// 4 activation rows, tcgen05 otherwise). The routed-expert GEMVs (MoE) stream plain weight rows instead.
 // ------------------------------------------------------------------------------------------------
-// first weight of physical row i of a row group, at the op's first input column
-__device__ __forceinline__ const uint16_t* gemv_row_src(const OpDesc& op, int g0, int i, int nl, bool swiglu) {
-  if (swiglu) {
-    return ((i < nl) ? op.w[0] + (size_t)(g0 + i) * op.ldw : op.w[1] + (size_t)(g0 + i - nl) * op.ldw) + op.k_begin;
-  }
-  int row = g0 + i;
-#pragma unroll 1
-  for (int m = 0; m < op.n_mat; ++m) {
-    if (row < op.mat_rows[m]) return op.w[m] + (size_t)row * op.ldw + op.k_begin;
-    row -= op.mat_rows[m];
-  }
-  return op.w[0];
+// A packed row block of a GEMV instruction: logical rows [start, end), rounded up to whole 8-row runs; P
+// physical rows per atom (SwiGLU: gate rows, then up rows); atoms per ring chunk (at most 32 KB).
+struct PkBlock {
+  int rows;   // logical rows
+  int rows8;  // rows rounded up to 8
+  int P;      // physical rows per atom: rows8, or 2 rows8 for SwiGLU
+  int atoms;  // atoms per ring chunk
+};
+
+// the row block that starts at logical row `start` of an instruction ending at `end`; returns its end
+__device__ __forceinline__ int pk_block(const OpDesc& op, int start, int end, PkBlock& blk) {
+  const int sw = op.out_kind == OUT_SWIGLU ? 1 : 0;
+  const int e = min(end, start + pk_block_lrows(sw));
+  blk.rows = e - start;
+  blk.rows8 = (blk.rows + 7) & ~7;
+  blk.P = blk.rows8 << sw;
+  blk.atoms = max(1, 256 / blk.P);
+  return e;
+}
+// the block's first byte in the packed copy: every earlier logical row takes patoms x 128 bytes (x 2 for
+// SwiGLU); plus the op's first atom
+__device__ __forceinline__ const uint8_t* pk_block_src(const OpDesc& op, int start, const PkBlock& blk) {
+  const size_t per_row = (size_t)op.patoms * 128 * (op.out_kind == OUT_SWIGLU ? 2 : 1);
+  return op.wp + (size_t)start * per_row + (size_t)op.pa0 * blk.P * 128;
 }
 
-// Row groups of a GEMV instruction: its rows are split into ceil(n / glog) groups of near-equal size (so no
+// end of the tcgen05 row group that starts at `start` (as many blocks as fit the TMEM columns)
+__device__ __forceinline__ int tc_group_end(const OpDesc& op, int start, int end) {
+  const int tiles = op.out_kind == OUT_SWIGLU ? 2 : 1;
+  const int blocks = max(1, kTcCols / (tiles * op.ncols));
+  return min(end, start + blocks * pk_block_lrows(tiles - 1));
+}
+
+__device__ __forceinline__ int tc_atoms(const OpDesc& op) { return (op.K + 63) >> 6; }
+__device__ __forceinline__ int tc_part(const OpDesc& op) { return 256 / op.ncols; }
+
+// ring chunks of one tcgen05 instruction (every consumer thread advances its chunk counter by this)
+__device__ __forceinline__ uint32_t tc_instr_chunks(const OpDesc& op, const Instr& in) {
+  const int nat = tc_atoms(op), KP = tc_part(op);
+  uint32_t n = 0;
+  for (int r = in.a; r < in.b;) {
+    PkBlock blk;
+    r = pk_block(op, r, in.b, blk);
+    for (int a0 = 0; a0 < nat; a0 += KP) {
+      const int a1 = min(nat, a0 + KP);
+      n += (uint32_t)((a1 - a0 + blk.atoms - 1) / blk.atoms);
+    }
+  }
+  return n;
+}
+
+// Row groups of an expert GEMV instruction: its rows are split into ceil(n / glog) groups of near-equal size (so no
 // group is left with a few rows and tiny chunks), and each group's K range into slices of KC inputs.
 __device__ __forceinline__ int gemv_ngroups(int n, int glog) { return (n + glog - 1) / glog; }
 __device__ __forceinline__ int gemv_group_row(int r0, int n, int ng, int g) {
@@ -365,12 +399,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // hi/lo bf16 columns of the staged activations: slot n (n < N) = hi of row n, slot N + n = lo of row n,
-// each K + 8 elements long (the 8 pad elements put successive slots in different banks)
+// each Kp + 8 elements long (Kp = K rounded up to whole atoms, zeros past K; the 8 pad elements put
+// successive slots in different banks)
 __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, CSmem& cs, uint16_t* cols, int ctid) {
   constexpr int kBatch = 8;  // loads of this many items are in flight before any of them is converted
   const bool norm = op.in_kind == IN_NORM;
-  const int K = op.K, N = p.N, cp = op.K + 8;
-  const int total4 = N * K / 4;
+  const int K = op.K, N = p.N, Kp = tc_atoms(op) * 64, cp = Kp + 8;
+  const int total4 = N * Kp / 4;
   for (int i0 = ctid; i0 < total4; i0 += kConsumerThreads * kBatch) {
     float4 v[kBatch];
     uint2 g[kBatch];
@@ -381,11 +416,13 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
       g[u] = make_uint2(0u, 0u);
       if (i < total4) {
         const int e = i * 4;
-        const int n = e / K, k = e % K;
-        const float* src =
-            norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
-        v[u] = __ldcg(reinterpret_cast<const float4*>(src));
-        if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+        const int n = e / Kp, k = e % Kp;
+        if (k < K) {
+          const float* src =
+              norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
+          v[u] = __ldcg(reinterpret_cast<const float4*>(src));
+          if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
+        }
       }
     }
 #pragma unroll
@@ -393,7 +430,7 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
       const int i = i0 + u * kConsumerThreads;
       if (i >= total4) break;
       const int e = i * 4;
-      const int n = e / K, k = e % K;
+      const int n = e / Kp, k = e % Kp;
       float4 x = v[u];
       if (norm) {
         const float s = cs.inv_rms[n];
@@ -417,15 +454,33 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
   }
 }
 
+// one m16n8k16 step of the mma.sync GEMV: A = 16 packed weight rows of one atom (ldmatrix through the
+// 128-byte swizzle), B = this lane's hi / lo activation column
+__device__ __forceinline__ void mma_kstep(float (&acc)[4], uint32_t arow, int rx, int lhi, int ks, uint32_t atom_bytes,
+                                          const uint16_t* bcol, int kbase, bool bvalid) {
+  const int a = ks >> 2, j = ks & 3;
+  uint32_t a0, a1, a2, a3;
+  ldmatrix_x4(arow + (uint32_t)a * atom_bytes + (uint32_t)(((2 * j + lhi) ^ rx) << 4), a0, a1, a2, a3);
+  uint32_t b0 = 0, b1 = 0;
+  if (bvalid) {
+    const uint16_t* bp = bcol + kbase + ks * 16;
+    b0 = *reinterpret_cast<const uint32_t*>(bp);
+    b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
+  }
+  mma_bf16_16816(acc, a0, a1, a2, a3, b0, b1);
+}
+
+// GEMV of up to 4 activation rows on mma.sync over packed row blocks. A block's P physical rows form
+// G16 = ceil(P / 16) m16 tiles; the 8 warps are split into G16 tiles x (8 / G16) K phases, each warp
+// accumulating its tile over every (8 / G16)-th k-step of each chunk, so a block needs one cross-warp sum.
 __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg, uint32_t& chunk,
                                  CSmem& cs, float* act, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int sm = blockIdx.x;
   const bool swiglu = op.out_kind == OUT_SWIGLU;
   const bool norm = op.in_kind == IN_NORM;
-  const int glog = swiglu ? 8 : 16;
-  const int K = op.K, N = p.N, KC = op.kc;
-  const int cpitch = K + 8;
+  const int N = p.N, nat = tc_atoms(op);
+  const int cpitch = nat * 64 + 8;
   uint16_t* cols = reinterpret_cast<uint16_t*>(act);
   // the residual slice follows the staged columns
   float* xres = act + (2 * N * cpitch + 1) / 2 + 4;
@@ -440,10 +495,10 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
   }
   consumer_sync();
   if (in.b > in.a) stage_hilo(p, op, cs, cols, ctid);
+  const int nrows = in.b - in.a;
   if (op.out_kind == OUT_RESID) {
-    const int nr_ = in.b - in.a;
-    for (int i = ctid; i < N * nr_; i += kConsumerThreads)
-      xres[i] = __ldcg(p.x + (size_t)(i / nr_) * p.d + in.a + i % nr_);
+    for (int i = ctid; i < N * nrows; i += kConsumerThreads)
+      xres[i] = __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows);
   }
   consumer_sync();
 
@@ -451,118 +506,113 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
   const int g = lane >> 2, t = lane & 3;
   const int bslot = (g < N) ? g : ((g >= 4 && g - 4 < N) ? N + (g - 4) : -1);
   const uint16_t* bcol = cols + (size_t)(bslot < 0 ? 0 : bslot) * cpitch + 2 * t;
-  // ldmatrix row / k offset of this lane inside a 16x16 tile
-  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int lk = ((lane >> 4) & 1) * 8;
+  // ldmatrix: this lane addresses tile row (lane & 7) + 8 ((lane >> 3) & 1), 16-byte piece parity lane >> 4
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lhi = lane >> 4;
   const uint32_t ring_s = smem_u32(rg.base);
 
-  // per-thread epilogue state: thread t < 16 * N owns (row i, activation row n), i = t / N, n = t % N
+  // epilogue state: thread ctid serves activation row n = ctid & 3 for logical rows (ctid >> 2) + 64 j
+  const int en = ctid & 3;
   float best_v = -CUDART_INF_F, ssq_acc = 0.f;
-  int best_i = 0;
-  float* red = cs.mred;  // [2][8 warps][16 rows][8 cols]
+  int best_i = 0x7fffffff;
 
-  const int nrows = in.b - in.a;
-  const int ng = gemv_ngroups(nrows, glog);
-  for (int grp = 0; grp < ng; ++grp) {
-    const int g0 = gemv_group_row(in.a, nrows, ng, grp);
-    const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
+  int bno = 0;
+  for (int r = in.a; r < in.b; ++bno) {
+    PkBlock blk;
+    const int r0 = r;
+    r = pk_block(op, r, in.b, blk);
+    const int G16 = (blk.P + 15) >> 4, np = kConsumerWarps / G16;
+    const int tile = warp % G16, ph = warp / G16;
+    const bool active = ph < np;
+    // rows past the block's last physical row read that row again (their sums are never used), so the tile
+    // never reaches past the chunk
+    const int prow = min(tile * 16 + lrow, blk.P - 1);
+    const int rx = prow & 7;
+    const uint32_t atom_bytes = (uint32_t)blk.P * 128u;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    // a group of fewer than 16 weight rows reads its last row again in the unused tile rows, so that the 16-row
-    // tile never reaches past the rows the chunk holds (a chunk of few rows is wider than one of 16)
-    const int lr = min(lrow, (swiglu ? 2 * nl : nl) - 1);
-    for (int k0 = 0; k0 < K; k0 += KC) {
-      const int kw = min(KC, K - k0);
-      const int pitch = kw * 2 + 16;
-      const int nsteps = kw >> 4;
+    for (int c0 = 0; c0 < nat; c0 += blk.atoms) {
+      const int na = min(blk.atoms, nat - c0);
       ring_wait_full(rg, chunk, p);
-      const uint32_t abase = ring_s + (chunk % kSlots) * kSlotBytes + lr * pitch + lk * 2;
-      int s = warp;
-      for (; s + kConsumerWarps < nsteps; s += 2 * kConsumerWarps) {
-        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-        ldmatrix_x4(abase + s * 32, a0, a1, a2, a3);
-        ldmatrix_x4(abase + (s + kConsumerWarps) * 32, c0, c1, c2, c3);
-        uint32_t b0 = 0, b1 = 0, e0 = 0, e1 = 0;
-        if (bslot >= 0) {
-          const uint16_t* bp = bcol + k0 + s * 16;
-          b0 = *reinterpret_cast<const uint32_t*>(bp);
-          b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
-          e0 = *reinterpret_cast<const uint32_t*>(bp + kConsumerWarps * 16);
-          e1 = *reinterpret_cast<const uint32_t*>(bp + kConsumerWarps * 16 + 8);
+      if (active) {
+        const uint32_t arow = ring_s + (chunk % kSlots) * kSlotBytes + (uint32_t)prow * 128u;
+        const int nks = 4 * na, kbase = c0 * 64;
+        int ks = ph;
+        for (; ks + np < nks; ks += 2 * np) {
+          mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
+          mma_kstep(acc1, arow, rx, lhi, ks + np, atom_bytes, bcol, kbase, bslot >= 0);
         }
-        mma_bf16_16816(acc0, a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(acc1, c0, c1, c2, c3, e0, e1);
-      }
-      if (s < nsteps) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(abase + s * 32, a0, a1, a2, a3);
-        uint32_t b0 = 0, b1 = 0;
-        if (bslot >= 0) {
-          const uint16_t* bp = bcol + k0 + s * 16;
-          b0 = *reinterpret_cast<const uint32_t*>(bp);
-          b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
-        }
-        mma_bf16_16816(acc0, a0, a1, a2, a3, b0, b1);
+        if (ks < nks) mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
       }
       ring_release(rg, chunk, lane);
       ++chunk;
     }
-    // cross-warp reduction: red[buf][warp][row][col]; fragment c0/c1 = (row g, cols 2t, 2t+1), c2/c3 = row g+8
-    float* rb = red + (grp & 1) * (kConsumerWarps * 128) + warp * 128;
-    rb[g * 8 + 2 * t] = acc0[0] + acc1[0];
-    rb[g * 8 + 2 * t + 1] = acc0[1] + acc1[1];
-    rb[(g + 8) * 8 + 2 * t] = acc0[2] + acc1[2];
-    rb[(g + 8) * 8 + 2 * t + 1] = acc0[3] + acc1[3];
+    // cross-warp sum: red[buf][warp][row][col]; fragment c0/c1 = (row g, cols 2t, 2t+1), c2/c3 = row g+8
+    float* rb = cs.mred + (bno & 1) * (kConsumerWarps * 128) + warp * 128;
+    if (active) {
+      rb[g * 8 + 2 * t] = acc0[0] + acc1[0];
+      rb[g * 8 + 2 * t + 1] = acc0[1] + acc1[1];
+      rb[(g + 8) * 8 + 2 * t] = acc0[2] + acc1[2];
+      rb[(g + 8) * 8 + 2 * t + 1] = acc0[3] + acc1[3];
+    }
     consumer_sync();
-    const float* rr = red + (grp & 1) * (kConsumerWarps * 128);
-    auto rowval = [&](int i, int n) -> float {
+    const float* rr = cs.mred + (bno & 1) * (kConsumerWarps * 128);
+    // physical row pr, activation row n: the hi and lo columns of every K phase of pr's tile
+    auto rowval = [&](int pr, int n) -> float {
+      const int tl = pr >> 4, i = pr & 15;
       float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += rr[w * 128 + i * 8 + n] + rr[w * 128 + i * 8 + 4 + n];
+      for (int q = 0; q < np; ++q) v += rr[(q * G16 + tl) * 128 + i * 8 + n] + rr[(q * G16 + tl) * 128 + i * 8 + 4 + n];
       return v;
     };
-    if (swiglu) {
-      if (ctid < nl * N) {
-        const int j = ctid / N, n = ctid % N;
-        const float gv = rowval(j, n), uv = rowval(nl + j, n);
-        op.out[(size_t)n * op.out_stride + g0 + j] = gv / (1.0f + expf(-gv)) * uv;
-      }
-    } else if (ctid < 16 * N) {
-      const int i = ctid / N, n = ctid % N;
-      if (i < nl) {
-        const float val = rowval(i, n);
-        if (op.out_kind == OUT_STORE) {
-          op.out[(size_t)n * op.out_stride + g0 + i] = val;
-        } else if (op.out_kind == OUT_RESID) {
-          const float xn = xres[n * nrows + (g0 - in.a) + i] + val;
-          __stcg(p.x + (size_t)n * p.d + g0 + i, xn);
-          ssq_acc += xn * xn;
+    if (en < N) {
+      for (int i = ctid >> 2; i < blk.rows; i += kConsumerThreads / 4) {
+        const int row = r0 + i;
+        if (swiglu) {
+          const float gv = rowval(i, en), uv = rowval(blk.rows8 + i, en);
+          op.out[(size_t)en * op.out_stride + row] = gv / (1.0f + expf(-gv)) * uv;
         } else {
-          if (p.logits) p.logits[(size_t)n * p.V + g0 + i] = val;
-          if (val > best_v) { best_v = val; best_i = g0 + i; }
+          const float val = rowval(i, en);
+          if (op.out_kind == OUT_STORE) {
+            op.out[(size_t)en * op.out_stride + row] = val;
+          } else if (op.out_kind == OUT_RESID) {
+            const float xn = xres[en * nrows + (row - in.a)] + val;
+            __stcg(p.x + (size_t)en * p.d + row, xn);
+            ssq_acc += xn * xn;
+          } else {
+            if (p.logits) p.logits[(size_t)en * p.V + row] = val;
+            if (val > best_v) { best_v = val; best_i = row; }
+          }
         }
       }
     }
-    // the other buffer is rewritten two groups later, after the next group's barrier
+    // the other buffer is rewritten two blocks later, after the next block's barrier
   }
   if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
-    // reduce the per-thread (row, n) state over the 16 rows of each n
+    // reduce the per-thread state over the threads of each activation row: lanes sharing (lane & 3), then warps
+    if (op.out_kind == OUT_RESID) {
+      for (int o = 4; o <= 16; o <<= 1) ssq_acc += __shfl_xor_sync(0xffffffffu, ssq_acc, o);
+    } else {
+      for (int o = 4; o <= 16; o <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+        if (ov > best_v || (ov == best_v && oi < best_i)) { best_v = ov; best_i = oi; }
+      }
+    }
     consumer_sync();
-    if (ctid < 16 * N) {
-      cs.sq[ctid] = (op.out_kind == OUT_RESID) ? ssq_acc : best_v;
-      cs.best_idx[ctid] = best_i;
+    if (lane < 4) {
+      cs.red[warp][lane] = op.out_kind == OUT_RESID ? ssq_acc : best_v;
+      cs.red[warp][4 + lane] = __int_as_float(best_i);
     }
     consumer_sync();
     if (ctid < N) {
       if (op.out_kind == OUT_RESID) {
         float s2 = 0.f;
-        for (int i = 0; i < 16; ++i) s2 += cs.sq[i * N + ctid];
+        for (int w = 0; w < kConsumerWarps; ++w) s2 += cs.red[w][ctid];
         if (op.ssq_out >= 0) __stcg(&p.ssq[ssq_index(p, op.ssq_out, ctid, sm)], s2);
       } else {
         float bv = -CUDART_INF_F;
         int bi = 0x7fffffff;
-        for (int i = 0; i < 16; ++i) {
-          const float v = cs.sq[i * N + ctid];
-          const int ix = cs.best_idx[i * N + ctid];
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float v = cs.red[w][ctid];
+          const int ix = __float_as_int(cs.red[w][4 + ctid]);
           if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
         }
         p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(bv, __int_as_float(bi));
@@ -576,100 +626,17 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
 // accumulators in tensor memory (TMEM). The weight rows are the M side of the MMA (128 TMEM lanes), the
 // activations the N side, split into a bf16 "hi" and "lo" column each (hi = bf16(v), lo = bf16(v - hi)) so
 // the product keeps ~16 mantissa bits of the fp32 activations; column 2n + 1 is added to column 2n at the end.
-//   * Weight tiles come from the ring, loaded by the producer warp with TMA (2D tensor maps of each weight
-//     matrix, 64-element boxes with 128-byte swizzle: the canonical K-major layout the MMA reads directly).
-//   * An instruction's rows are cut into row blocks of at most 128 physical rows, each split into segments
-//     at matrix boundaries (one TMA box per segment and atom). In shared memory a chunk is laid out atom by
-//     atom, each atom holding the block's segments stacked row after row, so one 128-row MMA per 16-input
-//     step covers the whole block, and the block accumulates in one TMEM tile of ncols columns (lane i = the
-//     block's row i). SwiGLU blocks take 64 logical rows: gate rows then up rows, two tiles. One row group
-//     (as many blocks as fit 512 columns) keeps all its accumulators in TMEM across the whole K loop, so no
-//     cross-warp reduction is needed.
+//   * Weight tiles come from the ring: packed row blocks (at most 128 physical rows; SwiGLU: 64 logical rows,
+//     gate rows then up rows), stored atom by atom in the canonical K-major 128-byte-swizzle layout the MMA
+//     reads directly, one contiguous bulk copy per chunk. One 128-row MMA per 16-input step covers a block
+//     (rows past its end read whatever follows and land in TMEM lanes that are never read), and the block
+//     accumulates in one TMEM tile of ncols columns (lane i = the block's row i; SwiGLU: a gate and an up
+//     tile). One row group (as many blocks as fit 512 columns) keeps all its accumulators in TMEM across the
+//     whole K loop, so no cross-warp reduction is needed.
 //   * K is covered in parts of 256 / ncols atoms (64 inputs each); the activations of a part are staged by
 //     warps 1..7 into one of two 32 KB buffers while lane 0 of warp 0 issues the MMAs of the previous part.
 // ------------------------------------------------------------------------------------------------
-struct TcSeg {
-  int m;      // matrix index in the op (SwiGLU: 0 gate, 1 up)
-  int row;    // first row inside that matrix
-  int h;      // rows
-  int out0;   // first output row (physical concatenated row; SwiGLU: logical row)
-  int roff;   // first row of the segment inside each stacked atom (a multiple of 8)
-};
-struct TcBlock {
-  int nseg;
-  int rows8;  // stacked rows of one atom: sum of the segments' box heights (rows rounded up to 8)
-  int atoms;  // 64-input atoms per ring chunk
-  int tiles;  // TMEM tiles of the block: 1, or 2 for SwiGLU (gate, up)
-  TcSeg seg[kTcMaxSeg];
-};
-
-static_assert(sizeof(TcBlock) <= sizeof(CSmem::uni_p), "the producer's row block must fit its shared-memory slot");
-
-__device__ __forceinline__ int tc_h8(int h) { return (h + 7) & ~7; }
-
-// the row block that starts at (concatenated / logical) row `start` of an instruction ending at `end`;
-// returns the next block's first row
-__device__ __forceinline__ int tc_block(const OpDesc& op, int start, int end, TcBlock& blk) {
-  if (op.out_kind == OUT_SWIGLU) {
-    const int h = min(64, end - start);
-    blk.nseg = 2;
-    blk.tiles = 2;
-    blk.seg[0] = {0, start, h, start, 0};
-    blk.seg[1] = {1, start, h, start, tc_h8(h)};
-    blk.rows8 = 2 * tc_h8(h);
-  } else {
-    int r = start, m = 0, base = 0;
-    while (m < op.n_mat - 1 && r >= base + op.mat_rows[m]) base += op.mat_rows[m++];
-    blk.nseg = 0;
-    blk.rows8 = 0;
-    blk.tiles = 1;
-    int left = 128;
-    while (r < end && left > 0 && blk.nseg < kTcMaxSeg) {
-      const int h = min(min(op.mat_rows[m] - (r - base), end - r), left);
-      blk.seg[blk.nseg++] = {m, r - base, h, r, blk.rows8};
-      blk.rows8 += tc_h8(h);
-      left -= tc_h8(h);
-      r += h;
-      if (r - base >= op.mat_rows[m] && m < op.n_mat - 1) base += op.mat_rows[m++];
-    }
-    start = r;
-  }
-  blk.atoms = max(1, min(16, 256 / blk.rows8));
-  return op.out_kind == OUT_SWIGLU ? start + blk.seg[0].h : start;
-}
-
-// end of the row group that starts at `start` (as many blocks as fit the TMEM columns)
-__device__ __forceinline__ int tc_group_end(const OpDesc& op, int start, int end) {
-  int cols = 0, r = start;
-  while (r < end) {
-    TcBlock blk;
-    const int nxt = tc_block(op, r, end, blk);
-    if (cols > 0 && cols + blk.tiles * op.ncols > kTcCols) break;
-    cols += blk.tiles * op.ncols;
-    r = nxt;
-  }
-  return r;
-}
-
-__device__ __forceinline__ int tc_atoms(const OpDesc& op) { return (op.K + 63) >> 6; }
-__device__ __forceinline__ int tc_part(const OpDesc& op) { return 256 / op.ncols; }
-
-// ring chunks of one instruction (every consumer thread advances its chunk counter by this)
-__device__ __forceinline__ uint32_t tc_instr_chunks(const OpDesc& op, const Instr& in) {
-  const int nat = tc_atoms(op), KP = tc_part(op);
-  uint32_t n = 0;
-  for (int r = in.a; r < in.b;) {
-    TcBlock blk;
-    r = tc_block(op, r, in.b, blk);
-    for (int a0 = 0; a0 < nat; a0 += KP) {
-      const int a1 = min(nat, a0 + KP);
-      n += (uint32_t)((a1 - a0 + blk.atoms - 1) / blk.atoms);
-    }
-  }
-  return n;
-}
-
-// --- tcgen05 / TMA primitives ---------------------------------------------------------------------
+// --- tcgen05 primitives ---------------------------------------------------------------------
 // shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
@@ -694,12 +661,6 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const TmaDesc* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
 }
 // 8 consecutive fp32 TMEM columns of this warp's 32 lanes
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
@@ -825,9 +786,10 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
         if (tr && g0 == in.a && a0 == 0) tr[5] = global_timer();
         const uint32_t bsa = smem_u32(bb);
         int col = 0;
+        const int tiles = swiglu ? 2 : 1;
         for (int r = g0; r < g1;) {
-          TcBlock blk;
-          r = tc_block(op, r, g1, blk);
+          PkBlock blk;
+          r = pk_block(op, r, g1, blk);
           for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
             const int na = min(blk.atoms, a1 - c0);
             const bool ok = ring_wait_full(rg, ck, p) && bok;
@@ -836,10 +798,10 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             if (ok) {
               const uint32_t slot = ring_s + (ck % kSlots) * kSlotBytes;
               for (int a = 0; a < na; ++a) {
-                const uint32_t atom = slot + (uint32_t)(a * blk.rows8 * 128);
+                const uint32_t atom = slot + (uint32_t)(a * blk.P * 128);
                 const uint32_t ba = bsa + (uint32_t)((c0 + a - a0) * nc * 128);
-                for (int t = 0; t < blk.tiles; ++t) {
-                  const uint32_t aa = atom + (uint32_t)(blk.seg[t].roff * 128);  // tile t starts at segment t
+                for (int t = 0; t < tiles; ++t) {
+                  const uint32_t aa = atom + (uint32_t)(t * blk.rows8 * 128);  // SwiGLU: the up rows follow the gate rows
                   const uint32_t d = ts.tmem + (uint32_t)(col + t * nc);
 #pragma unroll
                   for (int j = 0; j < 4; ++j)
@@ -853,7 +815,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             umma_commit(&rg.empty[ck % kSlots]);
             ++ck;
           }
-          col += blk.tiles * nc;
+          col += tiles * nc;
         }
         umma_commit(&bfree[buf]);
         if (tr) tr[7] = global_timer();
@@ -870,15 +832,15 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
     const int hc = nc >> 1;  // columns per half (hi / lo pairs: hc / 2 activation rows)
     int col = 0;
     for (int r = g0; r < g1;) {
-      TcBlock blk;
-      r = tc_block(op, r, g1, blk);
+      PkBlock blk;
+      const int r0 = r;
+      r = pk_block(op, r, g1, blk);
       {
-        // lane i of the tile is the block's row i (rows of consecutive segments follow each other)
+        // lane i of the tile is the block's row i
         const int s = 0;
         const int i = q * 32 + lane;
-        const int hrows = swiglu ? blk.seg[0].h : blk.seg[blk.nseg - 1].out0 + blk.seg[blk.nseg - 1].h - blk.seg[0].out0;
-        const bool valid = i < hrows;
-        const int row = blk.seg[0].out0 + i;
+        const bool valid = i < blk.rows;
+        const int row = r0 + i;
         for (int pc = 0; pc < hc; pc += 8) {
           const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + s * nc + half * hc + pc);
           float v[8];
@@ -922,7 +884,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
           }
         }
       }
-      col += blk.tiles * nc;
+      col += (swiglu ? 2 : 1) * nc;
     }
     tc_fence_before();
     consumer_sync();  // TMEM reads done before the next row group's MMAs overwrite the tiles
@@ -950,51 +912,6 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
   }
 }
 
-// The activation rows of a staged GEMV instruction: RMSNorm (when the op normalises its input) applied
-// once and kept in shared memory as fp32 for the whole instruction, so the inner loop reads only shared
-// memory. (Rounding them to bf16 instead costs up to ~5e-2 in the logits at full model width.)
-__device__ __forceinline__ void stage_activations(const KParams& p, const OpDesc& op, CSmem& cs, float* act,
-                                                  int ctid) {
-  constexpr int kBatch = 8;  // loads of this many items are in flight before any of them is stored
-  const bool norm = op.in_kind == IN_NORM;
-  const int K = op.K, N = p.N;
-  const int total4 = N * K / 4;
-  for (int i0 = ctid; i0 < total4; i0 += kConsumerThreads * kBatch) {
-    float4 v[kBatch];
-    uint2 g[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kConsumerThreads;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      g[u] = make_uint2(0u, 0u);
-      if (i < total4) {
-        const int e = i * 4;
-        const int n = e / K, k = e % K;
-        const float* src =
-            norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
-        v[u] = __ldcg(reinterpret_cast<const float4*>(src));
-        if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kConsumerThreads;
-      if (i >= total4) break;
-      const int e = i * 4;
-      const int n = e / K, k = e % K;
-      float4 x = v[u];
-      if (norm) {
-        const float s = cs.inv_rms[n];
-        x.x *= s * bf_lo(g[u].x);
-        x.y *= s * bf_hi(g[u].x);
-        x.z *= s * bf_lo(g[u].y);
-        x.w *= s * bf_hi(g[u].y);
-      }
-      *reinterpret_cast<float4*>(act + (size_t)n * K + k) = x;
-    }
-  }
-}
-
 template <int CPL>
 __device__ __forceinline__ void load_f32_smem(const float* src, float (&dst)[CPL]) {
 #pragma unroll
@@ -1017,175 +934,6 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // STAGED: activations from shared memory (fp32, N*K*4 <= kActBytes); otherwise each chunk loads
 // its activation slice from global memory (L2).
-template <int RG, int NR, bool STAGED>
-__device__ void gemv_consume(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                             uint32_t& chunk, CSmem& cs, float* act, int ctid) {
-  constexpr int CPL = kChunkBytes / 2 / RG / kConsumerThreads;  // 4 or 8 inputs per thread
-  constexpr int KC = CPL * kConsumerThreads;
-  constexpr int V = RG * NR;
-  const int warp = ctid >> 5, lane = ctid & 31;
-  const int sm = blockIdx.x;
-  const bool swiglu = op.out_kind == OUT_SWIGLU;
-  const bool norm = op.in_kind == IN_NORM;
-  const int glog = swiglu ? RG / 2 : RG;
-  const int K = op.K;
-  const int N = p.N;
-
-  if (norm) {
-    // 1/rms of each input row from the per-SM partial sums of squares: warp per row, lanes over SMs
-    for (int n = warp; n < N; n += kConsumerWarps) {
-      float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
-      s = warp_sum(s);
-      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
-    }
-  }
-  if (ctid < kMaxN) {
-    cs.ssq_acc[ctid] = 0.f;
-    cs.best_val[ctid] = -CUDART_INF_F;
-    cs.best_idx[ctid] = 0;
-  }
-  consumer_sync();
-  // residual-add ops read the x slice they update once, with the staging (this SM owns x[:, a:b))
-  float* xres = act + (STAGED ? N * K : 0);
-  if (STAGED && in.b > in.a) stage_activations(p, op, cs, act, ctid);
-  if (op.out_kind == OUT_RESID) {
-    const int nr_ = in.b - in.a;
-    for (int i = ctid; i < N * nr_; i += kConsumerThreads)
-      xres[i] = __ldcg(p.x + (size_t)(i / nr_) * p.d + in.a + i % nr_);
-  }
-  if ((STAGED && in.b > in.a) || op.out_kind == OUT_RESID) consumer_sync();
-
-  const int nrows = in.b - in.a;
-  const int ng = gemv_ngroups(nrows, glog);
-  for (int pass = 0; pass < op.passes; ++pass) {
-    const int nbase = pass * NR;
-    for (int grp = 0; grp < ng; ++grp) {
-      const int g0 = gemv_group_row(in.a, nrows, ng, grp);
-      const int nl = gemv_group_row(in.a, nrows, ng, grp + 1) - g0;
-      float acc[RG][NR];
-#pragma unroll
-      for (int i = 0; i < RG; ++i)
-#pragma unroll
-        for (int n = 0; n < NR; ++n) acc[i][n] = 0.f;
-
-      for (int k0 = 0; k0 < K; k0 += KC) {
-        const int kw = min(KC, K - k0);
-        const int col = ctid * CPL;
-        float a[NR][CPL];
-        if (col < kw) {
-          if (STAGED) {
-#pragma unroll
-            for (int n = 0; n < NR; ++n) {
-              if (n < N) load_f32_smem<CPL>(act + (size_t)n * K + k0 + col, a[n]);
-              else
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
-            }
-          } else {
-            float gsc[CPL];
-            if (norm) load_bf16_global<CPL>(op.gain + op.k_begin + k0 + col, gsc);
-#pragma unroll
-            for (int n = 0; n < NR; ++n) {
-              const int row = nbase + n;
-              if (row < N) {
-                if (norm) {
-                  load_f32<CPL>(p.x + (size_t)row * p.d + op.k_begin + k0 + col, a[n]);
-                  const float s = cs.inv_rms[row];
-#pragma unroll
-                  for (int c = 0; c < CPL; ++c) a[n][c] *= s * gsc[c];
-                } else {
-                  load_f32<CPL>(op.in + (size_t)row * op.in_stride + op.k_begin + k0 + col, a[n]);
-                }
-              } else {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) a[n][c] = 0.f;
-              }
-            }
-          }
-        }
-        ring_wait_full(rg, chunk, p);
-        if (col < kw) {
-          // all RG rows, branch-free, so the shared-memory loads of every row issue back to back; rows past
-          // nphys read stale bytes that still lie inside this slot and their sums are discarded below
-          const uint8_t* wbase = rg.slot_ptr(chunk) + col * 2;
-          float wf[RG][CPL];
-#pragma unroll
-          for (int i = 0; i < RG; ++i) load_bf16_row<CPL>(wbase + (size_t)i * kw * 2, wf[i]);
-#pragma unroll
-          for (int i = 0; i < RG; ++i)
-#pragma unroll
-            for (int c = 0; c < CPL; ++c)
-#pragma unroll
-              for (int n = 0; n < NR; ++n) acc[i][n] = fmaf(wf[i][c], a[n][c], acc[i][n]);
-        }
-        ring_release(rg, chunk, lane);
-        ++chunk;
-      }
-
-      float v[V];
-#pragma unroll
-      for (int i = 0; i < RG; ++i)
-#pragma unroll
-        for (int n = 0; n < NR; ++n) v[i * NR + n] = acc[i][n];
-      block_reduce<V>(v, cs, warp, lane, ctid);
-
-      // epilogue: cs.val[i * NR + n] is the dot product of physical row i with activation row nbase + n
-      if (swiglu) {
-        if (ctid < nl * NR) {
-          const int j = ctid / NR, n = ctid % NR, row = nbase + n;
-          if (row < N) {
-            const float g = cs.val[j * NR + n];
-            const float u = cs.val[(nl + j) * NR + n];
-            op.out[(size_t)row * op.out_stride + g0 + j] = g / (1.0f + expf(-g)) * u;
-          }
-        }
-      } else if (ctid < V) {
-        const int i = ctid / NR, n = ctid % NR, row = nbase + n;
-        const bool ok = (i < nl) && (row < N);
-        const float val = cs.val[ctid];
-        if (op.out_kind == OUT_STORE) {
-          if (ok) op.out[(size_t)row * op.out_stride + g0 + i] = val;
-        } else if (op.out_kind == OUT_RESID) {
-          float xn = 0.f;
-          if (ok) {
-            xn = xres[row * (in.b - in.a) + (g0 - in.a) + i] + val;
-            __stcg(p.x + (size_t)row * p.d + g0 + i, xn);
-          }
-          cs.sq[ctid] = xn * xn;
-        } else {  // OUT_LOGITS
-          if (ok && p.logits) p.logits[(size_t)row * p.V + g0 + i] = val;
-        }
-      }
-      if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
-        consumer_sync();
-        if (ctid < NR && nbase + ctid < N) {
-          const int row = nbase + ctid;
-          if (op.out_kind == OUT_RESID) {
-            float s = 0.f;
-            for (int i = 0; i < nl; ++i) s += cs.sq[i * NR + ctid];
-            cs.ssq_acc[row] += s;
-          } else {
-            float bv = cs.best_val[row];
-            int bi = cs.best_idx[row];
-            for (int i = 0; i < nl; ++i) {
-              const float vv = cs.val[i * NR + ctid];
-              if (vv > bv) { bv = vv; bi = g0 + i; }
-            }
-            cs.best_val[row] = bv;
-            cs.best_idx[row] = bi;
-          }
-        }
-      }
-      consumer_sync();
-    }
-  }
-  if (op.out_kind == OUT_RESID && op.ssq_out >= 0 && ctid < N)
-    __stcg(&p.ssq[ssq_index(p, op.ssq_out, ctid, sm)], cs.ssq_acc[ctid]);
-  if (op.out_kind == OUT_LOGITS && ctid < N)
-    p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(cs.best_val[ctid], __int_as_float(cs.best_idx[ctid]));
-}
-
 // ------------------------------------------------------------------------------------------------
 // embedding: x[n, a:b] = E[token_n, a:b] (fp32) and the RMS partial of this SM's columns
 // ------------------------------------------------------------------------------------------------
@@ -2277,52 +2025,46 @@ __device__ __noinline__ void mla_uv_consume(const KParams& p, const OpDesc& op, 
 
 // ------------------------------------------------------------------------------------------------
 // Producer: the chunks of an SM's queue, in the order its consumers read them. A cursor walks them and the
-// producer loads each chunk into the ring. Optionally (MK_PREFETCH_AHEAD > 0) a second cursor runs that
-// many chunks further and asks L2 to fetch those bytes early (cp.async.bulk.prefetch.L2); measured on the
-// hybrid stack this doubled HBM reads (prefetched lines were evicted before use), so it is off.
+// producer loads each chunk into the ring.
 // ------------------------------------------------------------------------------------------------
-#ifndef MK_PREFETCH_AHEAD
-#define MK_PREFETCH_AHEAD 0
-#endif
-constexpr int kPrefetchAhead = MK_PREFETCH_AHEAD;
-
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 struct ChunkCursor {
   int qi, q0, q1;
   int step;  // decode step of a multi-step launch: the queue is walked once per step
-  int kind;  // 0: load the next instruction, 1: GEMV chunks, 2: attention KV chunks
-  // the instruction's fields, cached in registers when it is loaded
-  int K, kc, pad, passes, ng, n, a, glog, swiglu;
+  int kind;  // 0: load the next instruction, 1: GEMV chunks, 2: attention KV chunks, 4: expert rows
   const OpDesc* op;
-  // GEMV walk: pass, row group, first input of the next slice; this lane's row pointer in the group
-  int pass, grp, k0, nphys;
-  const uint16_t* row;
+  // GEMV walk over packed row blocks, in the consumers' order (row groups, K parts, blocks, atoms): the
+  // instruction's end row, the row group [g0, g1), the K part (first atom a0, KP atoms; the whole K on the
+  // mma.sync path, whose row groups are single blocks), the block [r, rnext) with bP physical rows, bat atoms
+  // per chunk and its first byte; the next atom cc and the last chunk's atoms na (adv = 1: step past it)
+  int adv, rb, g0, g1, a0, r, rnext, cc, na, nat, KP, tc, bP, bat;
+  const uint8_t* bsrc;
   // attention walk: next position, end, positions per chunk, bytes per position, this lane's base,
   // number of copies per chunk (2: K and V of GQA; 1: the MLA latent)
   int t, t1, P, pos_bytes, ncopy;
   const uint16_t* kv;
-  // MoE walk: selected expert slot, count, format, this lane's weight row (codes) and scale row; the
-  // step's expert union, copied into shared memory when the walk reaches an expert op
+  // MoE walk: the instruction's rows (first row, count, group rows, groups), K and slice width, passes,
+  // selected expert slot, count, format, up / down; pass, row group, first input of the next slice, physical
+  // rows of the group; this lane's weight row (codes) and scale row; the step's expert union, copied into
+  // shared memory when the walk reaches an expert op
+  int a, n, glog, ng, K, kc, passes;
   int j, nsel, fp4, up;
+  int pass, grp, k0, nphys;
   int32_t* uni;
   const uint8_t* mw;
   const uint8_t* ms;
-  // tcgen05 GEMV walk: the instruction's row range, current row group, K part, row block and first atom
-  // of the current chunk, its atom count; tma = 1 when the chunk is a set of TMA tile copies
-  int tma, adv, rb, g0, g1, a0, r, rnext, cc, na, nat, KP;
-  TcBlock* blk;  // in shared memory (written by lane 0)
 };
 
-// the producer's row block: lane 0 computes it into shared memory, the warp reads it from there
-__device__ __forceinline__ int tc_cursor_block(const OpDesc& op, int start, int end, TcBlock* blk, int lane) {
-  int nxt = 0;
-  __syncwarp();
-  if (lane == 0) nxt = tc_block(op, start, end, *blk);
-  __syncwarp();
-  return __shfl_sync(0xffffffffu, nxt, 0);
+// the GEMV walk's current block: rows [c.r, ...) of the current row group
+__device__ __forceinline__ void cursor_block(ChunkCursor& c) {
+  PkBlock blk;
+  c.rnext = pk_block(*c.op, c.r, c.g1, blk);
+  c.bP = blk.P;
+  c.bat = blk.atoms;
+  c.bsrc = pk_block_src(*c.op, c.r, blk);
+}
+// end of the GEMV walk's row group starting at g0: TMEM-sized on the tcgen05 path, one block on mma.sync
+__device__ __forceinline__ int cursor_group_end(const ChunkCursor& c) {
+  return c.tc ? tc_group_end(*c.op, c.g0, c.rb) : min(c.rb, c.g0 + pk_block_lrows(c.op->out_kind == OUT_SWIGLU));
 }
 
 __device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& c, int lane) {
@@ -2341,13 +2083,6 @@ __device__ __forceinline__ void cursor_moe_group(const KParams& p, ChunkCursor& 
   }
 }
 
-__device__ __forceinline__ void cursor_group(ChunkCursor& c, int lane) {
-  const int g0 = gemv_group_row(c.a, c.n, c.ng, c.grp);
-  const int nl = gemv_group_row(c.a, c.n, c.ng, c.grp + 1) - g0;
-  c.nphys = c.swiglu ? 2 * nl : nl;
-  c.row = (lane < c.nphys) ? gemv_row_src(*c.op, g0, lane, nl, c.swiglu != 0) : nullptr;
-}
-
 // This lane's copy of the next chunk (bytes = 0: none) and the chunk's total bytes; false at the end.
 __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, int lane, const void*& src,
                                             uint32_t& bytes, uint32_t& dst, uint32_t& total) {
@@ -2363,39 +2098,22 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
       const OpDesc& op = p.ops[in.op];
       c.op = &op;
       const int type = op.type;
-      if (type == OP_GEMV && op.mma == 2) {
+      if (type == OP_GEMV) {
         if (in.b <= in.a) {
           ++c.qi;
           continue;
         }
-        c.a = in.a;
         c.rb = in.b;
+        c.tc = op.mma == 2 ? 1 : 0;
         c.nat = tc_atoms(op);
-        c.KP = tc_part(op);
+        c.KP = c.tc ? tc_part(op) : c.nat;
         c.g0 = in.a;
-        c.g1 = tc_group_end(op, in.a, in.b);
+        c.g1 = cursor_group_end(c);
         c.a0 = 0;
         c.r = in.a;
-        c.rnext = tc_cursor_block(op, c.r, c.g1, c.blk, lane);
+        cursor_block(c);
         c.cc = 0;
         c.adv = 0;
-        c.kind = 5;
-      } else if (type == OP_GEMV) {
-        c.swiglu = op.out_kind == OUT_SWIGLU;
-        c.glog = c.swiglu ? op.rg / 2 : op.rg;
-        c.a = in.a;
-        c.n = in.b - in.a;
-        c.ng = gemv_ngroups(c.n, c.glog);
-        c.K = op.K;
-        c.kc = op.kc;
-        c.pad = op.mma ? 16 : 0;  // the tensor-core path pads rows for ldmatrix
-        c.passes = op.passes;
-        c.pass = c.grp = c.k0 = 0;
-        if (c.ng == 0) {
-          ++c.qi;
-          continue;
-        }
-        cursor_group(c, lane);
         c.kind = 1;
       } else if (type == OP_ATTN) {
         const int hkv = op.n_kv_heads, hd = op.head_dim;
@@ -2447,11 +2165,10 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
         continue;
       }
     }
-    c.tma = 0;
-    if (c.kind == 5) {
-      if (c.adv) {  // step past the chunk returned last time, in the consumer's order: atoms, blocks, parts, groups
+    if (c.kind == 1) {
+      if (c.adv) {  // step past the chunk returned last time: atoms, blocks, K parts, row groups
         c.adv = 0;
-        c.cc += c.blk->atoms;
+        c.cc += c.na;
         if (c.cc >= min(c.nat, c.a0 + c.KP)) {
           c.r = c.rnext;
           if (c.r >= c.g1) {
@@ -2464,44 +2181,21 @@ __device__ __forceinline__ bool cursor_next(const KParams& p, ChunkCursor& c, in
                 ++c.qi;
                 continue;
               }
-              c.g1 = tc_group_end(*c.op, c.g0, c.rb);
+              c.g1 = cursor_group_end(c);
             }
             c.r = c.g0;
           }
-          c.rnext = tc_cursor_block(*c.op, c.r, c.g1, c.blk, lane);
+          cursor_block(c);
           c.cc = c.a0;
         }
       }
-      c.na = min(c.blk->atoms, min(c.nat, c.a0 + c.KP) - c.cc);
-      total = (uint32_t)(c.blk->rows8 * c.na * 128);
-      bytes = 0;
-      c.tma = 1;
+      // one contiguous copy of the block's atoms [cc, cc + na)
+      c.na = min(c.bat, min(c.nat, c.a0 + c.KP) - c.cc);
+      total = (uint32_t)(c.na * c.bP * 128);
+      src = c.bsrc + (size_t)c.cc * c.bP * 128;
+      bytes = lane == 0 ? total : 0u;
+      dst = 0;
       c.adv = 1;
-      return true;
-    }
-    if (c.kind == 1) {
-      const int kw = min(c.kc, c.K - c.k0);
-      total = (uint32_t)(c.nphys * kw * 2);
-      if (lane < c.nphys) {
-        src = c.row + c.k0;
-        bytes = (uint32_t)(kw * 2);
-        dst = (uint32_t)(lane * (kw * 2 + c.pad));
-      } else {
-        bytes = 0;
-      }
-      c.k0 += c.kc;
-      if (c.k0 >= c.K) {
-        c.k0 = 0;
-        if (++c.grp >= c.ng) {
-          c.grp = 0;
-          if (++c.pass >= c.passes) {
-            c.kind = 0;
-            ++c.qi;
-            return true;
-          }
-        }
-        cursor_group(c, lane);
-      }
       return true;
     }
     if (kFull && c.kind == 4) {
@@ -2621,26 +2315,19 @@ __device__ MK_OUTLINE void final_consume(const KParams& p, CSmem& cs, int step, 
 // ------------------------------------------------------------------------------------------------
 // the two roles
 // ------------------------------------------------------------------------------------------------
-__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, int32_t* uni, TcBlock* tc_blk) {
+__device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, int32_t* uni) {
   const int lane = threadIdx.x & 31;
   uint32_t chunk = 0;
   const uint32_t ring_base = smem_u32(rg.base);
-  ChunkCursor mc, pc;
-  mc.qi = pc.qi = q0;
-  mc.q0 = pc.q0 = q0;
-  mc.q1 = pc.q1 = q1;
-  mc.step = pc.step = 0;
-  mc.blk = pc.blk = tc_blk;
-  mc.kind = pc.kind = 0;
-  mc.uni = pc.uni = uni;
+  ChunkCursor mc;
+  mc.qi = q0;
+  mc.q0 = q0;
+  mc.q1 = q1;
+  mc.step = 0;
+  mc.kind = 0;
+  mc.uni = uni;
   const void* src = nullptr;
   uint32_t bytes = 0, dst = 0, total = 0;
-  if (kPrefetchAhead > 0) {
-    for (int i = 0; i < kPrefetchAhead; ++i) {
-      if (!cursor_next(p, pc, lane, src, bytes, dst, total)) break;
-      if (bytes) prefetch_l2(src, bytes);
-    }
-  }
   int last_qi = -1;
   while (cursor_next(p, mc, lane, src, bytes, dst, total)) {
     if (p.trace && lane == 0 && mc.step == 0 && mc.qi != last_qi) {
@@ -2648,26 +2335,8 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
       last_qi = mc.qi;
     }
     if (!ring_acquire(rg, chunk, total, p, lane)) break;
-    if (mc.tma) {
-      // one 2D TMA box per (segment, atom): segment s's atom a lands at its tile offset in the slot
-      const uint32_t slot = ring_base + (chunk % kSlots) * kSlotBytes;
-      const TcBlock& blk = *mc.blk;
-      const int na = mc.na, n = blk.nseg * na;
-      for (int idx = lane; idx < n; idx += 32) {
-        const int s = idx / na, a = idx - s * na;
-        const int h8 = tc_h8(blk.seg[s].h);
-        const TmaDesc* map = p.tmaps + mc.op->tm_base + blk.seg[s].m * 16 + (h8 / 8 - 1);
-        tma_load_2d(slot + (uint32_t)((a * blk.rows8 + blk.seg[s].roff) * 128), map, (mc.cc + a) * 64, blk.seg[s].row,
-                    &rg.full[chunk % kSlots]);
-      }
-    } else if (bytes) {
-      bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + dst, src, bytes, &rg.full[chunk % kSlots]);
-    }
+    if (bytes) bulk_g2s(ring_base + (chunk % kSlots) * kSlotBytes + dst, src, bytes, &rg.full[chunk % kSlots]);
     ++chunk;
-    const void* psrc = nullptr;
-    uint32_t pbytes = 0, pdst = 0, ptotal = 0;
-    if (kPrefetchAhead > 0 && cursor_next(p, pc, lane, psrc, pbytes, pdst, ptotal) && pbytes)
-      prefetch_l2(psrc, pbytes);
   }
   // every issued copy must land before the CTA may exit
   if (lane == 0) {
@@ -2682,11 +2351,6 @@ __device__ void run_producer(const KParams& p, const Ring& rg, int q0, int q1, i
   __syncwarp();
 }
 
-template <int RG, int NR, bool STAGED>
-__device__ MK_OUTLINE void gemv_dispatch(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
-                                           uint32_t& chunk, CSmem& cs, float* act, int ctid) {
-  gemv_consume<RG, NR, STAGED>(p, op, in, rg, chunk, cs, act, ctid);
-}
 
 // The MLA and MoE ops (full variant only).
 __device__ __forceinline__ void run_full_op(const KParams& p, const OpDesc& op, const Instr& in, const Ring& rg,
@@ -2760,16 +2424,8 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
         if (op.mma == 2) {
           gemv_tc_consume(p, op, in, rg, chunk, cs, reinterpret_cast<uint8_t*>(act), ts,
                           (trace && step == 0) ? p.trace + (size_t)qi * kTraceWords : nullptr, ctid);
-        } else if (op.mma) {
-          gemv_mma_consume(p, op, in, rg, chunk, cs, actf, ctid);
-        } else if (op.staged) {
-          if (nr == 1) gemv_dispatch<16, 1, true>(p, op, in, rg, chunk, cs, actf, ctid);
-          else gemv_dispatch<16, 2, true>(p, op, in, rg, chunk, cs, actf, ctid);
         } else {
-          if (nr == 1) gemv_dispatch<16, 1, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 2) gemv_dispatch<16, 2, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else if (nr == 4) gemv_dispatch<16, 4, false>(p, op, in, rg, chunk, cs, actf, ctid);
-          else gemv_dispatch<8, 8, false>(p, op, in, rg, chunk, cs, actf, ctid);
+          gemv_mma_consume(p, op, in, rg, chunk, cs, actf, ctid);
         }
         break;
       case OP_ROPE_APPEND: rope_append_consume(p, op, step, ctid); break;
@@ -2879,7 +2535,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   tc_fence_after();
   const int q0 = p.qoff[blockIdx.x], q1 = p.qoff[blockIdx.x + 1];
   if (tid >= kConsumerThreads) {
-    run_producer(p, rg, q0, q1, cs.uni_p, reinterpret_cast<TcBlock*>(cs.uni_p));
+    run_producer(p, rg, q0, q1, cs.uni_p);
   } else {
     TcState ts;
     ts.tmem = p.use_tc ? cs.tmem_base : 0u;
@@ -2921,6 +2577,51 @@ __global__ void rope_table_kernel(float2* tab, int max_ctx, int rot_dim, double 
   tab[i] = make_float2((float)c, (float)s);
 }
 
+// The tiled copy of one GEMV weight group (layout in mk_internal.h): one thread per 16-byte piece, read from
+// the caller's row-major matrices; zeros past K and past the group's last row.
+__global__ void pack_gemv_kernel(uint8_t* dst, PackSrc s, long long pieces) {
+  const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (id >= pieces) return;
+  const int A = pk_atoms(s.K), mc = s.swiglu ? 2 : 1;
+  const int c = (int)(id & 7);
+  long long rest = id >> 3;
+  const int a = (int)(rest % A);
+  rest /= A;
+  const int m = (int)(rest % mc);
+  const int r = (int)(rest / mc);
+  // the block holding logical row r: its SM's share is cut into blocks from the share's first row
+  const int sm = pk_sm_of(s.rows, s.n_sm, r);
+  const int a_s = pk_split(s.rows, s.n_sm, sm), b_s = pk_split(s.rows, s.n_sm, sm + 1);
+  const int br = pk_block_lrows(s.swiglu);
+  const int bs = a_s + (r - a_s) / br * br;
+  const int be = min(b_s, bs + br);
+  const int rows8 = (be - bs + 7) & ~7;
+  const int P = rows8 * mc;
+  const int prow = m * rows8 + (r - bs);
+  const size_t off = (size_t)bs * A * 128 * mc + (size_t)a * P * 128 + (size_t)prow * 128 + (size_t)((c ^ (prow & 7)) << 4);
+  uint16_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int k = a * 64 + c * 8;
+  if (r < s.rows && k < s.K) {
+    const uint16_t* row;
+    if (s.swiglu) {
+      row = s.w[m] + (size_t)r * s.K;
+    } else {
+      int rr = r, mm = 0;
+      while (mm < s.n_mat - 1 && rr >= s.mat_rows[mm]) rr -= s.mat_rows[mm++];
+      row = s.w[mm] + (size_t)rr * s.K;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (k + j < s.K) v[j] = row[k + j];
+  }
+  uint4 o;
+  o.x = v[0] | ((uint32_t)v[1] << 16);
+  o.y = v[2] | ((uint32_t)v[3] << 16);
+  o.z = v[4] | ((uint32_t)v[5] << 16);
+  o.w = v[6] | ((uint32_t)v[7] << 16);
+  *reinterpret_cast<uint4*>(dst + off) = o;
+}
+
 __global__ void fill_i32_kernel(int32_t* dst, int n, int32_t value) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = value;
@@ -2951,6 +2652,13 @@ cudaError_t kernel_launch(const KParams& p, int n_sm, cudaStream_t stream) {
 cudaError_t rope_table_launch(float2* tab, int max_ctx, int rot_dim, double theta, cudaStream_t stream) {
   const int n = max_ctx * (rot_dim / 2);
   rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(tab, max_ctx, rot_dim, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_gemv_launch(uint8_t* dst, const PackSrc& src, cudaStream_t stream) {
+  const long long pieces = pk_bytes(src.rows, src.K, src.swiglu) / 16;
+  if (pieces == 0) return cudaSuccess;
+  pack_gemv_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(dst, src, pieces);
   return cudaGetLastError();
 }
 

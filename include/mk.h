@@ -120,6 +120,11 @@ typedef struct mk_weights {
   const void* final_norm;  /* bf16 [d]                                                     */
   const void* lm_head;     /* bf16 [vocab, d]; NULL when tied_embedding                    */
   mk_layer_weights layers[MK_MAX_LAYERS];
+  /* The dense projection matrices (every matrix above except the embedding table, the norms, the
+   * routed / shared experts and w_uk / w_uv) in the kernel's tiled layout, written by mk_pack_weights
+   * for this model and device; or NULL, and mk_create makes its own copy (mk_decode_step_static needs
+   * it). Device memory owned by the caller, 1024-byte aligned, kept alive and unchanged while used. */
+  const void* packed;
 } mk_weights;
 
 typedef struct mk_handle mk_handle;
@@ -138,7 +143,9 @@ typedef struct mk_info {
 /* Creates a handle on `device`. The caller keeps ownership of every weight buffer and must keep
  * them alive and unchanged until mk_destroy. The handle allocates (cudaMalloc) and owns the KV /
  * latent caches, the recurrent states, activation scratch, instruction queues, counters and the
- * status word. Synchronous. Errors: MK_ERR_INVALID_ARG (inconsistent shape, missing weight,
+ * status word; and, when weights->packed is NULL, a tiled copy of the dense projection matrices
+ * (mk_pack_weights' layout; as large as those matrices), made here, which the decode path reads
+ * instead of the caller's matrices. Synchronous. Errors: MK_ERR_INVALID_ARG (inconsistent shape, missing weight,
  * alignment: every weight must be 16-byte aligned and every inner dimension a multiple of 8),
  * MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA.
  * Passage: the pages define no API for the kernel (their interface is a CLI and an HTTP server); this
@@ -269,6 +276,9 @@ typedef struct mk_plan_op {
                           chunk, weight rows per group, activation passes                              */
   int32_t out_kind;    /* GEMV epilogue: store 0, residual 1, SwiGLU 2, logits 3                        */
   int32_t nchunk, groups, head_dim, n_heads, n_kv_heads, col_group;  /* attention / delta / MLA       */
+  int32_t ncols;       /* GEMV, tcgen05: TMEM columns per accumulator tile                             */
+  int32_t pa0, patoms; /* GEMV: first packed atom (64 inputs) this op reads, atoms per packed row       */
+  int64_t pk_offset;   /* GEMV: byte offset of the op's weight group in the packed copy                */
 } mk_plan_op;
 
 typedef struct mk_plan_instr {
@@ -312,13 +322,33 @@ mk_status mk_get_info(const mk_handle* h, mk_info* out);
  * Passage: none; the pages define no API. */
 void mk_destroy(mk_handle* h);
 
+/* ---- Packed projection weights -------------------------------------------------------------------
+ * Every GEMV of the step (projections, output projections, dense FFN, router, LM head) reads its
+ * matrices from a tiled copy laid out for the weight ring: each SM's share of the rows (whole 8-row
+ * units) is cut into row blocks of at most 128 rows (SwiGLU: 64 gate rows and their 64 up rows), and a
+ * block stores 64 inputs of all its rows at a time, each 128-byte row piece swizzled in 16-byte units,
+ * so that one contiguous copy fills a ring slot with exactly what the tensor cores read. The layout
+ * depends on the model and on the device's SM count only.
+ *
+ * mk_packed_weight_bytes: size of that copy for `desc` / `weights` on `device`. mk_pack_weights fills
+ * `packed` (device memory of that size, 1024-byte aligned, owned by the caller) from the caller's
+ * matrices on `stream` (asynchronous; allocates nothing); pass it as weights->packed to mk_create (no
+ * second copy is made) or to mk_decode_step_static (which needs it). Errors: MK_ERR_INVALID_ARG
+ * (as mk_create, or a misaligned `packed`), MK_ERR_CUDA.
+ * Passage: none; the pages read each weight from HBM in its own layout, and this is this library's
+ * layout of the same values. */
+mk_status mk_packed_weight_bytes(const mk_model_desc* desc, const mk_weights* weights, int device, uint64_t* bytes);
+mk_status mk_pack_weights(const mk_model_desc* desc, const mk_weights* weights, int device, void* packed,
+                          void* stream);
+
 /* ---- A decode step that allocates no device memory ---------------------------------------------
  * The source pages have no counterpart for this call; it is a convenience of this library.
  * Some callers cannot call cudaMalloc at decode time: a serving process that hands all free HBM to its
  * own pool up front (so a later cudaMalloc fails or breaks the pool's accounting), a plug-in that runs
  * inside a host framework which owns device memory, or a latency-critical loop that cannot afford
  * cudaMalloc's implicit device synchronisation. mk_decode_step_static runs the same kernel as
- * mk_decode_step without a handle: the caller passes the model, the weights, its own persistent buffers
+ * mk_decode_step without a handle: the caller passes the model, the weights (with weights->packed
+ * filled by mk_pack_weights), its own persistent buffers
  * (below) and the step's inputs and outputs, and the step's working memory (activations, partial
  * results, inter-SM counters, the instruction queues, the RoPE table) lives in one statically sized
  * device array inside libmk, MK_STATIC_SCRATCH_BYTES long, which every GPU that loads the library keeps
@@ -340,7 +370,7 @@ void mk_destroy(mk_handle* h);
  * work overlaps (two host threads, or two streams that are not ordered) race on the array and give
  * wrong results. The call waits for `stream` and returns the device status of the step (as
  * mk_get_status would). Errors: MK_ERR_INVALID_ARG (as mk_create / mk_decode_step, or a missing
- * persistent buffer), MK_ERR_UNSUPPORTED when the step needs more working memory than
+ * persistent buffer or weights->packed), MK_ERR_UNSUPPORTED when the step needs more working memory than
  * MK_STATIC_SCRATCH_BYTES (a message on stderr gives both sizes), MK_ERR_CUDA, MK_ERR_DEVICE,
  * MK_ERR_TIMEOUT. MLA and MoE models are refused with MK_ERR_UNSUPPORTED: their latent cache and routing
  * buffers are not among the persistent buffers below. */

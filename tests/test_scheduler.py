@@ -49,6 +49,51 @@ def make_plan(cfg, n_sm, B, R, head=True, max_batch=8, max_rows=8, max_ctx=4096)
     return binding.plan(desc, fake_weights(cfg), n_sm, B, R, head)
 
 
+def pk_split(rows, n_sm, s):
+    """first logical row of SM s's share of a GEMV: whole 8-row units, balanced"""
+    units = -(-rows // 8)
+    return min(rows, 8 * (units * s // n_sm))
+
+
+def walk_chunks(o, instrs, packed_groups):
+    """The ring chunks of a GEMV op, in the producer's (= the consumers') order: per instruction, row groups
+    (one packed block on mma.sync; as many blocks as fit 512 TMEM columns on tcgen05), K parts (the whole K on
+    mma.sync; 256 / ncols atoms on tcgen05), blocks of at most 128 physical rows (64 logical rows for SwiGLU),
+    runs of at most 32 KB of atoms. Each chunk is one contiguous range of the group's packed copy; the ranges
+    are recorded per group so that the op (or its K parts together) can be checked to read every byte once."""
+    sw = 1 if o["out_kind"] == SWIGLU else 0
+    br = 64 if sw else 128
+    A, nat = o["patoms"], -(-o["K"] // 64)
+    tc = o["mma"] == 2
+    KP = 256 // o["ncols"] if tc else nat
+    per_group = packed_groups.setdefault(o["pk_offset"], {"bytes": (-(-o["rows"] // 8) * 8) * A * 128 * (1 + sw),
+                                                          "ranges": []})
+    for x in instrs:
+        a, b = x["a"], x["b"]
+        if b <= a:
+            continue
+        g0 = a
+        while g0 < b:
+            g1 = min(b, g0 + (max(1, 512 // ((1 + sw) * o["ncols"])) if tc else 1) * br)
+            for a0 in range(0, nat, KP):
+                r = g0
+                while r < g1:
+                    e = min(g1, r + br)
+                    rows8 = -(-(e - r) // 8) * 8
+                    P = rows8 << sw
+                    bat = max(1, 256 // P)
+                    base = r * A * 128 * (1 + sw) + (o["pa0"]) * P * 128
+                    cc = a0
+                    while cc < min(nat, a0 + KP):
+                        na = min(bat, min(nat, a0 + KP) - cc)
+                        off, nb = base + cc * P * 128, na * P * 128
+                        assert 0 < nb <= 32768 and off % 1024 == 0 and off + nb <= per_group["bytes"]
+                        per_group["ranges"].append((off, nb))
+                        cc += na
+                    r = e
+            g0 = g1
+
+
 def check_program(cfg, n_sm, B, R, head=True):
     ops, ins = make_plan(cfg, n_sm, B, R, head)
     N = B * R
@@ -79,6 +124,7 @@ def check_program(cfg, n_sm, B, R, head=True):
     d = cfg.d_model
     k = 0
     splits = []
+    packed_groups = {}
     for k, o in enumerate(ops):
         t = o["type"]
         if t == EMBED:
@@ -86,26 +132,18 @@ def check_program(cfg, n_sm, B, R, head=True):
         elif t == GEMV:
             partition(k, o["rows"])
             assert 0 <= o["k_begin"] and o["k_begin"] + o["K"] <= o["ldw"]
+            for x in by_op[k]:
+                assert x["a"] == pk_split(o["rows"], n_sm, x["sm"]), "shares of whole 8-row units"
             if o["mma"] == 1:
-                # chunks of up to one 33 KB ring slot: the largest row group x (kc inputs + 8 pad) x 2 bytes
-                assert N <= 4 and o["K"] % 16 == 0 and o["kc"] >= 1024 and o["kc"] % 16 == 0 and o["rg"] == 16
-                rows_max = -(-o["rows"] // n_sm)
-                glog = 8 if o["out_kind"] == 2 else 16
-                ng = -(-rows_max // glog)
-                nl = -(-rows_max // ng) * (2 if o["out_kind"] == 2 else 1)
-                assert nl * (o["kc"] * 2 + 16) <= 33 * 1024 or o["kc"] == 1024
-            elif o["mma"] == 2:
-                # tcgen05: 5 to 64 rows, rows cut in 8-row units (the TMA box heights), K parts of 256 / ncols atoms
-                ncols = -(-2 * N // 16) * 16
-                assert 5 <= N <= 64 and o["kc"] == 64 * (256 // ncols)
-                assert o["k_begin"] == 0 and o["K"] == o["ldw"], "no K split on the tcgen05 path"
-                for x in by_op[k]:
-                    assert x["a"] % 8 == 0 and (x["b"] % 8 == 0 or x["b"] == o["rows"])
+                # mma.sync: up to 4 rows, hi / lo columns of whole atoms (and the residual slice) staged
+                assert N <= 4 and o["k_begin"] == 64 * o["pa0"]
+                xrows = max(x["b"] - x["a"] for x in by_op[k]) if o["out_kind"] == RESID else 0
+                assert N * (64 * -(-o["K"] // 64) + 8 + xrows) * 4 <= 82176 - 32
             else:
-                assert o["kc"] * o["rg"] == 16384
-                if o["staged"]:
-                    assert N <= 2
-            assert o["passes"] == (1 if N <= 8 else (N + 7) // 8)
+                assert o["mma"] == 2 and o["ncols"] == -(-2 * N // 16) * 16
+                assert o["k_begin"] == 0 and o["K"] == o["ldw"] and o["pa0"] == 0, "no K split on the tcgen05 path"
+            assert o["patoms"] == -(-o["ldw"] // 64)
+            walk_chunks(o, by_op[k], packed_groups)
             if o["k_begin"] > 0 or o["K"] < o["ldw"]:
                 splits.append(k)
         elif t == ROPE:
@@ -168,6 +206,14 @@ def check_program(cfg, n_sm, B, R, head=True):
         for a, b in zip(g, g[1:]):
             assert ops[b]["k_begin"] == ops[a]["k_begin"] + ops[a]["K"]
         assert ops[g[-1]]["k_begin"] + ops[g[-1]]["K"] == ops[g[-1]]["ldw"]
+    # every GEMV weight group is read exactly once per step: its ops' chunks tile its packed copy
+    assert packed_groups
+    for g in packed_groups.values():
+        pos = 0
+        for off, nb in sorted(g["ranges"]):
+            assert off == pos, "chunks of a packed group must not overlap or leave gaps"
+            pos = off + nb
+        assert pos == g["bytes"]
     # one LM head when asked for, none otherwise
     assert sum(o["type"] == GEMV and o["out_kind"] == LOGITS for o in ops) == (1 if head else 0)
     return ops, ins
@@ -242,11 +288,15 @@ def test_plan_rejects_bad_shapes():
         make_plan(dataclasses.replace(nv, expert_dim=2000), 152, 1, 1)  # NVFP4 rows need multiples of 256
 
 
-def test_plan_refuses_what_one_sm_cannot_stage():
-    """With one SM a 16-row residual GEMV would have to keep all 5120 x 16 outputs in shared memory: the
-    scheduler refuses instead of overflowing the staging area."""
-    with pytest.raises(binding.MKError):
-        make_plan(config("hybrid_gdn_gqa", n_layers=4), 1, 2, 8)
+def test_one_sm_residual_gemv_takes_tcgen05():
+    """With one SM a residual GEMV's share is all 5120 rows: for 4 activation rows their slice of x no longer
+    fits beside any K part of the staged inputs, so those GEMVs take the tcgen05 path (whose epilogue reads x
+    from HBM), and the program still covers every row and reads every packed byte once."""
+    cfg = config("hybrid_gdn_gqa", n_layers=4)
+    ops, _ = check_program(cfg, 1, 4, 1)
+    resid = [o for o in ops if o["type"] == GEMV and o["out_kind"] == RESID]
+    assert resid and all(o["mma"] == 2 for o in resid)
+    check_program(cfg, 1, 2, 8)
 
 
 def test_batch_above_eight_rows_per_call():
@@ -256,7 +306,7 @@ def test_batch_above_eight_rows_per_call():
     cfg = config("hybrid_gdn_gqa", n_layers=4)
     ops, ins = make_plan(cfg, 152, 64, 1, max_batch=64)
     gemvs = [o for o in ops if o["type"] == GEMV]
-    assert gemvs and all(o["mma"] == 2 and o["kc"] == 64 * (256 // 128) for o in gemvs)
+    assert gemvs and all(o["mma"] == 2 and o["ncols"] == 128 for o in gemvs)
     ops, _ = make_plan(cfg, 152, 8, 8, max_batch=64)
     assert all(o["mma"] == 2 for o in ops if o["type"] == GEMV)
     with pytest.raises(binding.MKError):

@@ -44,11 +44,27 @@ def _state_buffers(cfg, desc, dev):
     return keep, sb
 
 
+def _packed_weights(mk, dev):
+    """The caller's tiled copy of the projection matrices (mk_pack_weights into a 1024-byte aligned buffer
+    the caller owns) and a weight table that points to it, as mk_decode_step_static requires."""
+    from decode_megakernel_04_gb300 import binding
+    n = binding.packed_weight_bytes(mk.desc, mk.wtab, dev.index or 0)
+    buf = torch.empty(n + 1024, dtype=torch.uint8, device=dev)
+    ptr = (buf.data_ptr() + 1023) // 1024 * 1024
+    binding.pack_weights(mk.desc, mk.wtab, ptr, dev.index or 0)
+    torch.cuda.synchronize()
+    wt = binding.Weights()
+    C.memmove(C.byref(wt), C.byref(mk.wtab), C.sizeof(wt))
+    wt.packed = ptr
+    return buf, wt
+
+
 def _compare_calls(lib, mk, sb, cfg, calls, dev):
     """Runs each (tokens, positions) call through mk_decode_step on the handle and through
     mk_decode_step_static on the caller's buffers; logits within TOL, greedy tokens equal, and the
     caller's call counter advanced by one per call."""
     from decode_megakernel_04_gb300 import binding
+    packed_buf, wt = _packed_weights(mk, dev)
     for i, (toks, pos) in enumerate(calls):
         toks = toks.contiguous()
         B, R = toks.shape
@@ -60,7 +76,7 @@ def _compare_calls(lib, mk, sb, cfg, calls, dev):
         assert mk.status() == 0
         lb = torch.full((n, cfg.vocab), float("nan"), device=dev)
         ab = torch.full((n,), -1, dtype=torch.int32, device=dev)
-        rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(mk.wtab), C.byref(sb), toks.data_ptr(),
+        rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(wt), C.byref(sb), toks.data_ptr(),
                                        pos_t.data_ptr(), B, R, lb.data_ptr(), ab.data_ptr(), None)
         assert rc == 0, binding.STATUS.get(rc, rc)
         err = float((la - lb).abs().max())
@@ -84,6 +100,32 @@ def test_static_entry_point_matches_handle_entry_point():
              (make_tokens(4, "b", (B, 1), cfg.vocab, device=dev), [R, R])]
     _compare_calls(lib, mk, sb, cfg, calls, dev)
     mk.close()
+
+
+def test_handle_on_caller_packed_weights():
+    """mk_create with weights->packed set reads the caller's tiled copy (mk_pack_weights) instead of making its
+    own: the same step gives the same logits, bit for bit, and the handle owns less device memory."""
+    from decode_megakernel_04_gb300 import Megakernel, binding
+    cfg = config("hybrid_gdn_gqa", n_layers=2, d_model=256, ffn_dim=512, vocab=2048, n_q_heads=4, n_kv_heads=2,
+                 head_dim=64, lin_heads=4, lin_dk=64, lin_dv=32)
+    dev = torch.device("cuda")
+    w = make_weights(cfg, seed=7, device=dev)
+    a = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64)
+    buf, wt = _packed_weights(a, dev)
+    b = Megakernel(cfg, w, max_batch=2, max_rows=8, max_ctx=64, packed=wt.packed)
+    ia, ib = binding.Info(), binding.Info()
+    assert a.lib.mk_get_info(a.h, C.byref(ia)) == 0 and b.lib.mk_get_info(b.h, C.byref(ib)) == 0
+    n = binding.packed_weight_bytes(a.desc, a.wtab, dev.index or 0)
+    assert ia.device_bytes - ib.device_bytes == n
+    toks = make_tokens(7, "p", (2, 8), cfg.vocab, device=dev).contiguous()
+    pos = torch.zeros(2, dtype=torch.int32, device=dev)
+    la, lb = torch.empty((16, cfg.vocab), device=dev), torch.empty((16, cfg.vocab), device=dev)
+    a.step(toks, pos, la)
+    b.step(toks, pos, lb)
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(la, lb)
+    a.close()
+    b.close()
 
 
 def test_static_entry_point_hybrid_state_and_pending_rows():
@@ -124,13 +166,18 @@ def test_static_entry_point_rejects_oversized_step():
     toks = torch.zeros((1, 8), dtype=torch.int32, device=dev)
     pos = torch.zeros((1,), dtype=torch.int32, device=dev)
     lg = torch.empty((8, cfg.vocab), device=dev)
+    # without the caller's packed weights the call is refused
     rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(mk.wtab), C.byref(sb), toks.data_ptr(),
+                                   pos.data_ptr(), 1, 1, lg.data_ptr(), None, None)
+    assert rc == 1  # MK_ERR_INVALID_ARG
+    packed_buf, wt = _packed_weights(mk, dev)
+    rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(wt), C.byref(sb), toks.data_ptr(),
                                    pos.data_ptr(), 1, 8, lg.data_ptr(), None, None)
     assert rc == 2  # MK_ERR_UNSUPPORTED
     assert sb.epoch == 0
     # a single row fits and runs
     lg1 = torch.empty((1, cfg.vocab), device=dev)
-    rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(mk.wtab), C.byref(sb), toks.data_ptr(),
+    rc = lib.mk_decode_step_static(C.byref(mk.desc), C.byref(wt), C.byref(sb), toks.data_ptr(),
                                    pos.data_ptr(), 1, 1, lg1.data_ptr(), None, None)
     assert rc == 0
     assert torch.isfinite(lg1).all()
