@@ -124,8 +124,8 @@ struct OpDesc {
 // ---- packed GEMV weights -----------------------------------------------------------------------------
 // The matrices one GEMV op reads (stacked by rows: q, k, v of a projection; or the gate and up matrices of
 // a SwiGLU, paired row by row) are kept in a tiled copy made for the weight ring. Rows are shared out to the
-// SMs in whole 8-row units; each SM's share is cut into row blocks of at most 128 physical rows (SwiGLU: 64
-// logical rows, the block's gate rows then its up rows, each run rounded up to 8). A block stores its rows
+// SMs in whole 8-row units; each SM's share is cut into row blocks of at most 128 logical rows, rounded up to
+// whole 8-row runs (SwiGLU: the block's gate rows then its up rows, up to 256 physical rows). A block stores its rows
 // atom by atom (64 inputs = 128 bytes of each row, inputs padded with zeros to whole atoms); inside an atom
 // row r's eight 16-byte pieces sit at positions (piece ^ (r & 7)). That is the K-major, 128-byte-swizzle
 // layout a tcgen05 descriptor reads (8-row groups 1024 bytes apart) and one ldmatrix reads without bank
@@ -133,7 +133,7 @@ struct OpDesc {
 // a block's first row takes atoms x 128 bytes (x 2 for SwiGLU), so a block starting at logical row r
 // starts r x atoms x 128 (x 2) bytes into the copy.
 constexpr int kPackAtom = 64;       // inputs per atom
-constexpr int kPackBlockRows = 128; // physical rows per block at most
+constexpr int kPackBlockRows = 128; // logical rows per block at most
 #if defined(__CUDACC__)
 #define MK_HD __host__ __device__ __forceinline__
 #else
@@ -151,7 +151,7 @@ MK_HD int pk_sm_of(int rows, int n_sm, int r) {
   const long long units = (rows + 7) / 8;
   return (int)(((long long)n_sm * (r / 8 + 1) - 1) / units);
 }
-MK_HD int pk_block_lrows(int swiglu) { return swiglu ? kPackBlockRows / 2 : kPackBlockRows; }
+MK_HD int pk_block_lrows(int) { return kPackBlockRows; }
 // bytes of the packed copy of a group of `rows` logical rows over K inputs
 MK_HD long long pk_bytes(int rows, int K, int swiglu) {
   return (long long)((rows + 7) & ~7) * pk_atoms(K) * 128 * (swiglu ? 2 : 1);

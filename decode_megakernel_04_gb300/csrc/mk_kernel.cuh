@@ -398,15 +398,35 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 1/rms of activation rows n = warp, warp + 8, .. from the per-SM partial sums of squares of norm point `slot`
+// (sum over `width` columns): every partial of a row is loaded at once (8 per lane), so this costs one L2 round
+// trip. Writes cs.inv_rms; the caller synchronises.
+__device__ __forceinline__ void inv_rms_rows(const KParams& p, int slot, int width, CSmem& cs, int warp, int lane,
+                                             int nwarps = kConsumerWarps) {
+  for (int n = warp; n < p.N; n += nwarps) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = lane + 32 * i;
+      v[i] = q < p.n_sm ? __ldcg(&p.ssq[ssq_index(p, slot, n, q)]) : 0.f;
+    }
+    float s = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    s = warp_sum(s);
+    if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)width + p.eps);
+  }
+}
+
 // hi/lo bf16 columns of the staged activations: slot n (n < N) = hi of row n, slot N + n = lo of row n,
 // each Kp + 8 elements long (Kp = K rounded up to whole atoms, zeros past K; the 8 pad elements put
-// successive slots in different banks)
+// successive slots in different banks). With RMSNorm the 1/rms of each row is computed while the first round
+// of input loads is in flight, so the staging costs one L2 round trip per 16 loads a thread issues.
+template <int kBatch, bool norm>  // kBatch: loads in flight per thread before any of them is converted
 __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, CSmem& cs, uint16_t* cols, int ctid) {
-  constexpr int kBatch = 8;  // loads of this many items are in flight before any of them is converted
-  const bool norm = op.in_kind == IN_NORM;
   const int K = op.K, N = p.N, Kp = tc_atoms(op) * 64, cp = Kp + 8;
   const int total4 = N * Kp / 4;
-  for (int i0 = ctid; i0 < total4; i0 += kConsumerThreads * kBatch) {
+  const int rounds = (total4 + kConsumerThreads * kBatch - 1) / (kConsumerThreads * kBatch);
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int i0 = rd * kConsumerThreads * kBatch + ctid;
     float4 v[kBatch];
     uint2 g[kBatch];
 #pragma unroll
@@ -424,6 +444,10 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
           if (norm) g[u] = __ldg(reinterpret_cast<const uint2*>(op.gain + op.k_begin + k));
         }
       }
+    }
+    if (norm && rd == 0) {
+      inv_rms_rows(p, op.ssq_in, op.ldw, cs, ctid >> 5, ctid & 31);
+      consumer_sync();
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -485,21 +509,25 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
   // the residual slice follows the staged columns
   float* xres = act + (2 * N * cpitch + 1) / 2 + 4;
 
-  if (norm) {
-    for (int n = warp; n < N; n += kConsumerWarps) {
-      float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
-      s = warp_sum(s);
-      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
-    }
-  }
-  consumer_sync();
-  if (in.b > in.a) stage_hilo(p, op, cs, cols, ctid);
+  // a residual add also stages this SM's slice of x: its first 2 x 256 values load with the inputs' first round
   const int nrows = in.b - in.a;
-  if (op.out_kind == OUT_RESID) {
-    for (int i = ctid; i < N * nrows; i += kConsumerThreads)
-      xres[i] = __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows);
+  const int nx = op.out_kind == OUT_RESID ? N * nrows : 0;
+  float xr[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = ctid + u * kConsumerThreads;
+    xr[u] = i < nx ? __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows) : 0.f;
   }
+  if (in.b > in.a) {
+    // (the full build's handlers get fewer registers: it keeps the shallower batch there)
+    if (norm) stage_hilo<kFull ? 8 : 12, true>(p, op, cs, cols, ctid);
+    else stage_hilo<kFull ? 8 : 20, false>(p, op, cs, cols, ctid);
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+    if (ctid + u * kConsumerThreads < nx) xres[ctid + u * kConsumerThreads] = xr[u];
+  for (int i = ctid + 2 * kConsumerThreads; i < nx; i += kConsumerThreads)
+    xres[i] = __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows);
   consumer_sync();
 
   // this lane's B column: hi of row g, lo of row g - 4, or zero
@@ -520,41 +548,63 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
     PkBlock blk;
     const int r0 = r;
     r = pk_block(op, r, in.b, blk);
-    const int G16 = (blk.P + 15) >> 4, np = kConsumerWarps / G16;
-    const int tile = warp % G16, ph = warp / G16;
-    const bool active = ph < np;
+    // m16 tiles of the block: up to 8 take one warp each (or 8 / G16 warps splitting the K steps); 9 to 16
+    // (SwiGLU blocks over 64 rows) take two per warp, tiles w and w + 8
+    const int G16 = (blk.P + 15) >> 4;
+    const bool two = G16 > kConsumerWarps;
+    const int np = two ? 1 : kConsumerWarps / G16;
+    const int tile = two ? warp : warp % G16, ph = two ? 0 : warp / G16;
+    const bool active = ph < np, active2 = two && warp + kConsumerWarps < G16;
     // rows past the block's last physical row read that row again (their sums are never used), so the tile
     // never reaches past the chunk
     const int prow = min(tile * 16 + lrow, blk.P - 1);
-    const int rx = prow & 7;
+    const int prow2 = min((tile + kConsumerWarps) * 16 + lrow, blk.P - 1);
+    const int rx = prow & 7, rx2 = prow2 & 7;
     const uint32_t atom_bytes = (uint32_t)blk.P * 128u;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c0 = 0; c0 < nat; c0 += blk.atoms) {
       const int na = min(blk.atoms, nat - c0);
       ring_wait_full(rg, chunk, p);
       if (active) {
-        const uint32_t arow = ring_s + (chunk % kSlots) * kSlotBytes + (uint32_t)prow * 128u;
+        const uint32_t sbase = ring_s + (chunk % kSlots) * kSlotBytes;
+        const uint32_t arow = sbase + (uint32_t)prow * 128u;
         const int nks = 4 * na, kbase = c0 * 64;
-        int ks = ph;
-        for (; ks + np < nks; ks += 2 * np) {
-          mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
-          mma_kstep(acc1, arow, rx, lhi, ks + np, atom_bytes, bcol, kbase, bslot >= 0);
+        if (two) {
+          const uint32_t arow2 = sbase + (uint32_t)prow2 * 128u;
+          for (int ks = 0; ks < nks; ++ks) {
+            mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
+            if (active2) mma_kstep(acc1, arow2, rx2, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
+          }
+        } else {
+          int ks = ph;
+          for (; ks + np < nks; ks += 2 * np) {
+            mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
+            mma_kstep(acc1, arow, rx, lhi, ks + np, atom_bytes, bcol, kbase, bslot >= 0);
+          }
+          if (ks < nks) mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
         }
-        if (ks < nks) mma_kstep(acc0, arow, rx, lhi, ks, atom_bytes, bcol, kbase, bslot >= 0);
       }
       ring_release(rg, chunk, lane);
       ++chunk;
     }
-    // cross-warp sum: red[buf][warp][row][col]; fragment c0/c1 = (row g, cols 2t, 2t+1), c2/c3 = row g+8
-    float* rb = cs.mred + (bno & 1) * (kConsumerWarps * 128) + warp * 128;
-    if (active) {
-      rb[g * 8 + 2 * t] = acc0[0] + acc1[0];
-      rb[g * 8 + 2 * t + 1] = acc0[1] + acc1[1];
-      rb[(g + 8) * 8 + 2 * t] = acc0[2] + acc1[2];
-      rb[(g + 8) * 8 + 2 * t + 1] = acc0[3] + acc1[3];
+    // cross-warp sum: red[buf][warp][row][col] (two tiles a warp: red[tile][row][col] over both buffers);
+    // fragment c0/c1 = (row g, cols 2t, 2t+1), c2/c3 = row g+8
+    if (two) consumer_sync();  // the whole buffer is rewritten: the previous block's epilogue must be done
+    auto put = [&](float* rb, const float (&x)[4], const float (&y)[4]) {
+      rb[g * 8 + 2 * t] = x[0] + y[0];
+      rb[g * 8 + 2 * t + 1] = x[1] + y[1];
+      rb[(g + 8) * 8 + 2 * t] = x[2] + y[2];
+      rb[(g + 8) * 8 + 2 * t + 1] = x[3] + y[3];
+    };
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (two) {
+      if (active) put(cs.mred + tile * 128, acc0, zero4);
+      if (active2) put(cs.mred + (tile + kConsumerWarps) * 128, acc1, zero4);
+    } else if (active) {
+      put(cs.mred + (bno & 1) * (kConsumerWarps * 128) + warp * 128, acc0, acc1);
     }
     consumer_sync();
-    const float* rr = cs.mred + (bno & 1) * (kConsumerWarps * 128);
+    const float* rr = two ? cs.mred : cs.mred + (bno & 1) * (kConsumerWarps * 128);
     // physical row pr, activation row n: the hi and lo columns of every K phase of pr's tile
     auto rowval = [&](int pr, int n) -> float {
       const int tl = pr >> 4, i = pr & 15;
@@ -584,6 +634,7 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
       }
     }
     // the other buffer is rewritten two blocks later, after the next block's barrier
+    if (two) consumer_sync();
   }
   if (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS) {
     // reduce the per-thread state over the threads of each activation row: lanes sharing (lane & 3), then warps
@@ -626,8 +677,8 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
 // accumulators in tensor memory (TMEM). The weight rows are the M side of the MMA (128 TMEM lanes), the
 // activations the N side, split into a bf16 "hi" and "lo" column each (hi = bf16(v), lo = bf16(v - hi)) so
 // the product keeps ~16 mantissa bits of the fp32 activations; column 2n + 1 is added to column 2n at the end.
-//   * Weight tiles come from the ring: packed row blocks (at most 128 physical rows; SwiGLU: 64 logical rows,
-//     gate rows then up rows), stored atom by atom in the canonical K-major 128-byte-swizzle layout the MMA
+//   * Weight tiles come from the ring: packed row blocks (at most 128 logical rows; SwiGLU: 128 gate rows then
+//     128 up rows), stored atom by atom in the canonical K-major 128-byte-swizzle layout the MMA
 //     reads directly, one contiguous bulk copy per chunk. One 128-row MMA per 16-input step covers a block
 //     (rows past its end read whatever follows and land in TMEM lanes that are never read), and the block
 //     accumulates in one TMEM tile of ncols columns (lane i = the block's row i; SwiGLU: a gate and an up
@@ -676,15 +727,22 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 // Activations of atoms [a0, a1) as bf16 hi / lo rows (row 2n = hi of activation row n, 2n + 1 = lo; rows
 // from 2N to ncols are zero) in the swizzled K-major layout: atom a at buf + (a - a0) * ncols * 128, row r at
 // + r * 128, its 16-byte chunk c at + ((c ^ (r & 7)) << 4). Warps 1..7 do this; inputs past K are zero.
-__device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, const CSmem& cs, uint8_t* buf, int a0,
-                                         int a1, int stid, int nthr) {
+// With rms = true (the first K part of an instruction that normalises its input) the staging warps also compute
+// 1/rms of every row from the RMS partials while their first loads are in flight, and meet at a barrier of their
+// own before converting.
+// With ok = false (this warp's wait for the buffer gave up) nothing is staged, but the rms barrier is still
+// met, so the staging warps never wait on one another without a limit.
+__device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, CSmem& cs, uint8_t* buf, int a0,
+                                         int a1, int stid, int nthr, bool rms, bool ok) {
   constexpr int kBatch = 8;  // items whose loads are all in flight before any of them is converted
   const bool norm = op.in_kind == IN_NORM;
   const int N = p.N, K = op.K, nc = op.ncols;
   const int pairs = nc >> 1;                 // activation rows incl. the zero padding
   const int na = a1 - a0;
-  const int items = pairs * na * 8;          // (activation row, atom, 16-byte chunk)
-  for (int it0 = stid; it0 < items; it0 += nthr * kBatch) {
+  const int items = ok ? pairs * na * 8 : 0;  // (activation row, atom, 16-byte chunk)
+  const int rounds = max(rms ? 1 : 0, (items + nthr * kBatch - 1) / (nthr * kBatch));
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int it0 = rd * nthr * kBatch + stid;
     float4 x0[kBatch], x1[kBatch];
     uint4 g[kBatch];
 #pragma unroll
@@ -701,6 +759,10 @@ __device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, con
         x1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
         if (norm) g[u] = __ldg(reinterpret_cast<const uint4*>(op.gain + k));
       }
+    }
+    if (rms && rd == 0) {
+      inv_rms_rows(p, op.ssq_in, op.ldw, cs, stid >> 5, stid & 31, nthr >> 5);
+      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");  // the staging warps only
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -751,14 +813,6 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
   float* pred = &cs.red[0][0];                                 // [8 warps][64]: ssq or argmax value partials
   int32_t* pidx = reinterpret_cast<int32_t*>(cs.mred);         // [8 warps][64]: argmax index partials
 
-  if (norm) {
-    for (int n = warp; n < N; n += kConsumerWarps) {
-      float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
-      s = warp_sum(s);
-      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)op.ldw + p.eps);
-    }
-  }
   for (int i = ctid; i < kConsumerWarps * 64; i += kConsumerThreads) {
     pred[i] = op.out_kind == OUT_LOGITS ? -CUDART_INF_F : 0.f;
     pidx[i] = 0x7fffffff;
@@ -777,37 +831,48 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
       if (warp >= 1) {
         bool ok = true;
         if (use > 0) ok = wait_bar(&bfree[buf], (use - 1) & 1u, p);
-        if (ok) tc_stage(p, op, cs, bb, a0, a1, ctid - 32, kConsumerThreads - 32);
+        tc_stage(p, op, cs, bb, a0, a1, ctid - 32, kConsumerThreads - 32, norm && g0 == in.a && a0 == 0, ok);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&bready[buf]);
         if (tr && ctid == 32) tr[8] = global_timer();
       } else if (lane == 0) {
         const bool bok = wait_bar(&bready[buf], use & 1u, p);
         if (tr && g0 == in.a && a0 == 0) tr[5] = global_timer();
-        const uint32_t bsa = smem_u32(bb);
+        // The issuing thread's own work bounds this loop (an M = 128, K = 16 MMA is issued in ~45 cycles when its
+        // operands are ready; computing each descriptor from scratch tripled that): descriptors are built once per
+        // chunk and stepped by constants (the start address sits in the low bits, in 16-byte units).
+        const uint64_t bd0 = umma_desc(smem_u32(bb));
+        const uint64_t b_atom = (uint64_t)((nc * 128) >> 4);
         int col = 0;
         const int tiles = swiglu ? 2 : 1;
         for (int r = g0; r < g1;) {
           PkBlock blk;
           r = pk_block(op, r, g1, blk);
+          const uint64_t a_atom = (uint64_t)((blk.P * 128) >> 4);
+          const uint64_t a_up = (uint64_t)((blk.rows8 * 128) >> 4);  // SwiGLU: the up rows follow the gate rows
+          const uint32_t dg = ts.tmem + (uint32_t)col, du = dg + (uint32_t)nc;
           for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
             const int na = min(blk.atoms, a1 - c0);
             const bool ok = ring_wait_full(rg, ck, p) && bok;
             if (tr && ck == chunk) tr[6] = global_timer();
             tc_fence_after();
             if (ok) {
-              const uint32_t slot = ring_s + (ck % kSlots) * kSlotBytes;
-              for (int a = 0; a < na; ++a) {
-                const uint32_t atom = slot + (uint32_t)(a * blk.P * 128);
-                const uint32_t ba = bsa + (uint32_t)((c0 + a - a0) * nc * 128);
-                for (int t = 0; t < tiles; ++t) {
-                  const uint32_t aa = atom + (uint32_t)(t * blk.rows8 * 128);  // SwiGLU: the up rows follow the gate rows
-                  const uint32_t d = ts.tmem + (uint32_t)(col + t * nc);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    umma_bf16(d, umma_desc(aa + j * 32), umma_desc(ba + j * 32), idesc,
-                              (c0 + a > 0 || j > 0) ? 1u : 0u);
+              uint64_t ad = umma_desc(ring_s + (ck % kSlots) * kSlotBytes);
+              uint64_t bd = bd0 + (uint64_t)(c0 - a0) * b_atom;
+              uint32_t acc = c0 > 0 ? 1u : 0u;  // the group's first MMA starts its accumulators
+              for (int a = 0; a < na; ++a, ad += a_atom, bd += b_atom) {
+                umma_bf16(dg, ad, bd, idesc, acc);
+                umma_bf16(dg, ad + 2, bd + 2, idesc, 1u);
+                umma_bf16(dg, ad + 4, bd + 4, idesc, 1u);
+                umma_bf16(dg, ad + 6, bd + 6, idesc, 1u);
+                if (tiles == 2) {
+                  const uint64_t au = ad + a_up;
+                  umma_bf16(du, au, bd, idesc, acc);
+                  umma_bf16(du, au + 2, bd + 2, idesc, 1u);
+                  umma_bf16(du, au + 4, bd + 4, idesc, 1u);
+                  umma_bf16(du, au + 6, bd + 6, idesc, 1u);
                 }
+                acc = 1u;
               }
             }
             // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
@@ -843,9 +908,8 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
         const int row = r0 + i;
         for (int pc = 0; pc < hc; pc += 8) {
           const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + s * nc + half * hc + pc);
-          float v[8];
+          float v[8], u[8];
           tmem_ld8(ta, v);
-          float u[8];
           if (swiglu) tmem_ld8(ta + (uint32_t)nc, u);
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
@@ -1272,15 +1336,14 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
   float* pb_ = pa_ + a * na;          // [a]     accepted beta
   float* pv_ = pb_ + a;               // [a][C]  accepted v
 
-  // the state columns this warp owns (independent of the staging)
+  // the state columns this warp owns (independent of the staging); column c at Sp + c * dk
   float S[CW][4];
-  float* Sp[CW];
+  float* const Sp = p.state + ((((size_t)op.slot * p.max_batch + b) * H + h) * dv + j0 + warp * CW) * dk + lane * E;
 #pragma unroll
   for (int c = 0; c < CW; ++c) {
     const int j = j0 + warp * CW + c;
-    Sp[c] = p.state + ((((size_t)op.slot * p.max_batch + b) * H + h) * dv + j) * dk + lane * E;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp[c] + e) : 0.f;
+    for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp + c * dk + e) : 0.f;
   }
   for (int i = ctid; i < R * dk; i += kConsumerThreads) {
     const int r = i / dk, e = i % dk;
@@ -1343,7 +1406,7 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
 #pragma unroll
     for (int c = 0; c < CW; ++c)
       if (jw + c < dv)
-        for (int e = 0; e < E; ++e) __stcg(Sp[c] + e, S[c][e]);
+        for (int e = 0; e < E; ++e) __stcg(Sp + c * dk + e, S[c][e]);
   }
 
   const float qs = rsqrtf((float)dk);
@@ -1580,12 +1643,7 @@ __device__ __noinline__ void moe_consume(const KParams& p, const OpDesc& op, con
   // staged inputs: UP [N][K] at act; DOWN two [N][F] buffers after xres
   float* hst = act + 2 * rt + ((N * nrows + 3) & ~3);
   if (up) {
-    for (int n = warp; n < N; n += kConsumerWarps) {
-      float s = 0.f;
-      for (int q = lane; q < p.n_sm; q += 32) s += __ldcg(&p.ssq[ssq_index(p, op.ssq_in, n, q)]);
-      s = warp_sum(s);
-      if (lane == 0) cs.inv_rms[n] = rsqrtf(s / (float)p.d + p.eps);
-    }
+    inv_rms_rows(p, op.ssq_in, p.d, cs, warp, lane);
     if constexpr (STG) {
       consumer_sync();
       for (int i = ctid * 4; i < N * K; i += kConsumerThreads * 4) {
@@ -2465,7 +2523,9 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
       case OP_DELTA:
         if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-        else delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else if (op.col_group == 32) delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else if (op.col_group == 64) delta_consume<8>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else delta_consume<16>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         break;
       case OP_FINAL: final_consume(p, cs, step, ctid); break;
       default: break;

@@ -62,7 +62,7 @@ def walk_chunks(o, instrs, packed_groups):
     runs of at most 32 KB of atoms. Each chunk is one contiguous range of the group's packed copy; the ranges
     are recorded per group so that the op (or its K parts together) can be checked to read every byte once."""
     sw = 1 if o["out_kind"] == SWIGLU else 0
-    br = 64 if sw else 128
+    br = 128
     A, nat = o["patoms"], -(-o["K"] // 64)
     tc = o["mma"] == 2
     KP = 256 // o["ncols"] if tc else nat
@@ -175,7 +175,7 @@ def check_program(cfg, n_sm, B, R, head=True):
             ng = -(-cfg.lin_dv // o["col_group"])
             got = sorted((x["a"], x["b"], x["c"]) for x in by_op[k])
             assert got == sorted((b, h, j) for b in range(B) for h in range(cfg.lin_heads) for j in range(ng))
-            assert o["col_group"] in (8, 16, 32)
+            assert o["col_group"] in (8, 16, 32, 64, 128)
         elif t == MLA_PREP:
             sms = sorted(x["sm"] for x in by_op[k])
             assert sms == list(range(len(sms))) and 8 * len(sms) >= 2 * N
