@@ -835,12 +835,14 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&bready[buf]);
         if (tr && ctid == 32) tr[8] = global_timer();
-      } else if (lane == 0) {
+      } else {
+        // Warp 0 walks the chunks together and lane 0 issues the MMAs: the other lanes must not run ahead into a
+        // barrier poll, which would stall the warp and with it the issuing lane. The issuing lane's own work bounds
+        // this loop (an M = 128, K = 16 MMA takes ~30-45 cycles when its operands are ready; computing each
+        // descriptor from scratch tripled that): descriptors are built once per chunk and stepped by constants
+        // (the start address sits in the low bits, in 16-byte units).
         const bool bok = wait_bar(&bready[buf], use & 1u, p);
-        if (tr && g0 == in.a && a0 == 0) tr[5] = global_timer();
-        // The issuing thread's own work bounds this loop (an M = 128, K = 16 MMA is issued in ~45 cycles when its
-        // operands are ready; computing each descriptor from scratch tripled that): descriptors are built once per
-        // chunk and stepped by constants (the start address sits in the low bits, in 16-byte units).
+        if (tr && lane == 0 && g0 == in.a && a0 == 0) tr[5] = global_timer();
         const uint64_t bd0 = umma_desc(smem_u32(bb));
         const uint64_t b_atom = (uint64_t)((nc * 128) >> 4);
         int col = 0;
@@ -854,9 +856,9 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
           for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
             const int na = min(blk.atoms, a1 - c0);
             const bool ok = ring_wait_full(rg, ck, p) && bok;
-            if (tr && ck == chunk) tr[6] = global_timer();
+            if (tr && lane == 0 && ck == chunk) tr[6] = global_timer();
             tc_fence_after();
-            if (ok) {
+            if (ok && lane == 0) {
               uint64_t ad = umma_desc(ring_s + (ck % kSlots) * kSlotBytes);
               uint64_t bd = bd0 + (uint64_t)(c0 - a0) * b_atom;
               uint32_t acc = c0 > 0 ? 1u : 0u;  // the group's first MMA starts its accumulators
@@ -876,14 +878,18 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
               }
             }
             // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
-            mbar_arrive_n(&rg.empty[ck % kSlots], kConsumerWarps - 1);
-            umma_commit(&rg.empty[ck % kSlots]);
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive_n(&rg.empty[ck % kSlots], kConsumerWarps - 1);
+              umma_commit(&rg.empty[ck % kSlots]);
+            }
             ++ck;
           }
           col += tiles * nc;
         }
-        umma_commit(&bfree[buf]);
-        if (tr) tr[7] = global_timer();
+        if (lane == 0) umma_commit(&bfree[buf]);
+        if (tr && lane == 0) tr[7] = global_timer();
+        __syncwarp();
       }
       ++ts.kp;
     }
