@@ -70,6 +70,14 @@ __device__ __forceinline__ void red_release_add(uint32_t* ptr, uint32_t v) {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
+// V independent warp sums, their butterfly rounds interleaved; every lane gets every total
+template <int V>
+__device__ __forceinline__ void warp_sum_n(float (&v)[V]) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -1348,8 +1356,16 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
 #pragma unroll
   for (int c = 0; c < CW; ++c) {
     const int j = j0 + warp * CW + c;
+    if (E == 4) {  // this lane's 4 key rows of the column in one 16-byte load
+      const float4 v4 = j < dv ? __ldcg(reinterpret_cast<const float4*>(Sp + c * dk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      S[c][0] = v4.x;
+      S[c][1] = v4.y;
+      S[c][2] = v4.z;
+      S[c][3] = v4.w;
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp + c * dk + e) : 0.f;
+      for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp + c * dk + e) : 0.f;
+    }
   }
   for (int i = ctid; i < R * dk; i += kConsumerThreads) {
     const int r = i / dk, e = i % dk;
@@ -1395,15 +1411,20 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
       al[e] = e < E ? (kda ? pa_[r * dk + lane * E + e] : pa_[r]) : 1.f;
     }
     const float beta = pb_[r];
+    float dot[CW];
 #pragma unroll
     for (int c = 0; c < CW; ++c) {
-      float dot = 0.f;
+      dot[c] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         S[c][e] *= al[e];
-        dot = fmaf(S[c][e], kh[e], dot);
+        dot[c] = fmaf(S[c][e], kh[e], dot[c]);
       }
-      const float u = pv_[r * C + warp * CW + c] - warp_sum(dot);
+    }
+    warp_sum_n(dot);  // the columns' reductions interleaved
+#pragma unroll
+    for (int c = 0; c < CW; ++c) {
+      const float u = pv_[r * C + warp * CW + c] - dot[c];
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[c][e] = fmaf(beta * kh[e], u, S[c][e]);
     }
@@ -1411,8 +1432,11 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
   if (a > 0) {
 #pragma unroll
     for (int c = 0; c < CW; ++c)
-      if (jw + c < dv)
-        for (int e = 0; e < E; ++e) __stcg(Sp + c * dk + e, S[c][e]);
+      if (jw + c < dv) {
+        if (E == 4) __stcg(reinterpret_cast<float4*>(Sp + c * dk), make_float4(S[c][0], S[c][1], S[c][2], S[c][3]));
+        else
+          for (int e = 0; e < E; ++e) __stcg(Sp + c * dk + e, S[c][e]);
+      }
   }
 
   const float qs = rsqrtf((float)dk);
@@ -1437,26 +1461,35 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
       kv[e] *= ik;
     }
     float* pw = pend_at(cur, r);
+    float dot[CW], od[CW];
 #pragma unroll
     for (int c = 0; c < CW; ++c) {
-      float dot = 0.f;
+      dot[c] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         S[c][e] *= al[e];
-        dot = fmaf(S[c][e], kv[e], dot);
+        dot[c] = fmaf(S[c][e], kv[e], dot[c]);
       }
-      const float vj = sv_[r * C + warp * CW + c];
-      const float u = vj - warp_sum(dot);
-      float od = 0.f;
+    }
+    warp_sum_n(dot);
+#pragma unroll
+    for (int c = 0; c < CW; ++c) {
+      const float u = sv_[r * C + warp * CW + c] - dot[c];
+      od[c] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         S[c][e] = fmaf(beta * kv[e], u, S[c][e]);
-        od = fmaf(S[c][e], qv[e], od);
+        od[c] = fmaf(S[c][e], qv[e], od[c]);
       }
-      const float o = warp_sum(od);
-      if (lane == 0 && jw + c < dv) {
-        __stcg(op.out + (size_t)n * op.out_stride + h * dv + jw + c, o);
-        __stcg(pw + dk + jw + c, vj);  // stored for replay by the next call
+    }
+    warp_sum_n(od);
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) {
+        if (jw + c < dv) {
+          __stcg(op.out + (size_t)n * op.out_stride + h * dv + jw + c, od[c]);
+          __stcg(pw + dk + jw + c, sv_[r * C + warp * CW + c]);  // stored for replay by the next call
+        }
       }
     }
     if (jg == 0 && warp == 0) {
