@@ -427,7 +427,9 @@ __device__ __forceinline__ void inv_rms_rows(const KParams& p, int slot, int wid
 // hi/lo bf16 columns of the staged activations: slot n (n < N) = hi of row n, slot N + n = lo of row n,
 // each Kp + 8 elements long (Kp = K rounded up to whole atoms, zeros past K; the 8 pad elements put
 // successive slots in different banks). With RMSNorm the 1/rms of each row is computed while the first round
-// of input loads is in flight, so the staging costs one L2 round trip per 16 loads a thread issues.
+// of input loads is in flight. Loads go out in rounds of kBatch = 4 per thread: deeper rounds (8 to 20 loads in
+// flight) measured slower at batch 1 although they need fewer round trips; the unrolled code of a deep round,
+// run once per instruction, cost more than the round trips it saved.
 template <int kBatch, bool norm>  // kBatch: loads in flight per thread before any of them is converted
 __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, CSmem& cs, uint16_t* cols, int ctid) {
   const int K = op.K, N = p.N, Kp = tc_atoms(op) * 64, cp = Kp + 8;
@@ -444,7 +446,7 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
       g[u] = make_uint2(0u, 0u);
       if (i < total4) {
         const int e = i * 4;
-        const int n = e / Kp, k = e % Kp;
+        const int n = (e >= Kp) + (e >= 2 * Kp) + (e >= 3 * Kp), k = e - n * Kp;  // N <= 4: no division
         if (k < K) {
           const float* src =
               norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
@@ -462,7 +464,7 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
       const int i = i0 + u * kConsumerThreads;
       if (i >= total4) break;
       const int e = i * 4;
-      const int n = e / Kp, k = e % Kp;
+      const int n = (e >= Kp) + (e >= 2 * Kp) + (e >= 3 * Kp), k = e - n * Kp;
       float4 x = v[u];
       if (norm) {
         const float s = cs.inv_rms[n];
@@ -527,9 +529,8 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
     xr[u] = i < nx ? __ldcg(p.x + (size_t)(i / nrows) * p.d + in.a + i % nrows) : 0.f;
   }
   if (in.b > in.a) {
-    // (the full build's handlers get fewer registers: it keeps the shallower batch there)
-    if (norm) stage_hilo<kFull ? 8 : 12, true>(p, op, cs, cols, ctid);
-    else stage_hilo<kFull ? 8 : 20, false>(p, op, cs, cols, ctid);
+    if (norm) stage_hilo<4, true>(p, op, cs, cols, ctid);
+    else stage_hilo<4, false>(p, op, cs, cols, ctid);
   }
 #pragma unroll
   for (int u = 0; u < 2; ++u)
@@ -742,7 +743,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 // met, so the staging warps never wait on one another without a limit.
 __device__ __forceinline__ void tc_stage(const KParams& p, const OpDesc& op, CSmem& cs, uint8_t* buf, int a0,
                                          int a1, int stid, int nthr, bool rms, bool ok) {
-  constexpr int kBatch = 8;  // items whose loads are all in flight before any of them is converted
+  constexpr int kBatch = 3;  // items whose loads are all in flight before any of them is converted (2 to 8 measured)
   const bool norm = op.in_kind == IN_NORM;
   const int N = p.N, K = op.K, nc = op.ncols;
   const int pairs = nc >> 1;                 // activation rows incl. the zero padding
@@ -830,78 +831,83 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
   const uint32_t idesc = umma_idesc(nc);
   const uint32_t ring_s = smem_u32(rg.base);
   uint32_t ck = chunk;  // ring position of the MMA thread
+  const int nkp = (nat + KP - 1) / KP;  // K parts per row group
   for (int g0 = in.a; g0 < in.b;) {
     const int g1 = tc_group_end(op, g0, in.b);
-    for (int a0 = 0; a0 < nat; a0 += KP) {
-      const int a1 = min(nat, a0 + KP);
-      const uint32_t buf = ts.kp & 1u, use = ts.kp >> 1;
-      uint8_t* bb = act + buf * kTcBBytes;
-      if (warp >= 1) {
+    const uint32_t kp0 = ts.kp;
+    if (warp >= 1) {
+      for (int i = 0; i < nkp; ++i) {
+        const int a0 = i * KP, a1 = min(nat, a0 + KP);
+        const uint32_t buf = (kp0 + i) & 1u, use = (kp0 + i) >> 1;
+        uint8_t* bb = act + buf * kTcBBytes;
         bool ok = true;
         if (use > 0) ok = wait_bar(&bfree[buf], (use - 1) & 1u, p);
         tc_stage(p, op, cs, bb, a0, a1, ctid - 32, kConsumerThreads - 32, norm && g0 == in.a && a0 == 0, ok);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&bready[buf]);
         if (tr && ctid == 32) tr[8] = global_timer();
-      } else {
-        // Warp 0 walks the chunks together and lane 0 issues the MMAs: the other lanes must not run ahead into a
-        // barrier poll, which would stall the warp and with it the issuing lane. The issuing lane's own work bounds
-        // this loop (an M = 128, K = 16 MMA takes ~30-45 cycles when its operands are ready; computing each
-        // descriptor from scratch tripled that): descriptors are built once per chunk and stepped by constants
-        // (the start address sits in the low bits, in 16-byte units).
-        const bool bok = wait_bar(&bready[buf], use & 1u, p);
-        if (tr && lane == 0 && g0 == in.a && a0 == 0) tr[5] = global_timer();
-        const uint64_t bd0 = umma_desc(smem_u32(bb));
-        const uint64_t b_atom = (uint64_t)((nc * 128) >> 4);
-        int col = 0;
+      }
+    } else {
+      // Lane 0 alone walks every K part and chunk of the row group and issues the MMAs; lanes 1..31 wait at the
+      // warp barrier below. Entering and leaving a one-lane branch per chunk cost ~300 cycles each time (the
+      // MMA stream stalls while the warp reconverges), and lanes left free to run ahead would spin on the
+      // accumulator barrier and take the issuing lane's cycles. Descriptors are built once per chunk and
+      // stepped by constants (the start address sits in the low bits, in 16-byte units).
+      if (lane == 0) {
         const int tiles = swiglu ? 2 : 1;
-        for (int r = g0; r < g1;) {
-          PkBlock blk;
-          r = pk_block(op, r, g1, blk);
-          const uint64_t a_atom = (uint64_t)((blk.P * 128) >> 4);
-          const uint64_t a_up = (uint64_t)((blk.rows8 * 128) >> 4);  // SwiGLU: the up rows follow the gate rows
-          const uint32_t dg = ts.tmem + (uint32_t)col, du = dg + (uint32_t)nc;
-          for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
-            const int na = min(blk.atoms, a1 - c0);
-            const bool ok = ring_wait_full(rg, ck, p) && bok;
-            if (tr && lane == 0 && ck == chunk) tr[6] = global_timer();
-            tc_fence_after();
-            if (ok && lane == 0) {
-              uint64_t ad = umma_desc(ring_s + (ck % kSlots) * kSlotBytes);
-              uint64_t bd = bd0 + (uint64_t)(c0 - a0) * b_atom;
-              uint32_t acc = c0 > 0 ? 1u : 0u;  // the group's first MMA starts its accumulators
-              for (int a = 0; a < na; ++a, ad += a_atom, bd += b_atom) {
-                umma_bf16(dg, ad, bd, idesc, acc);
-                umma_bf16(dg, ad + 2, bd + 2, idesc, 1u);
-                umma_bf16(dg, ad + 4, bd + 4, idesc, 1u);
-                umma_bf16(dg, ad + 6, bd + 6, idesc, 1u);
-                if (tiles == 2) {
-                  const uint64_t au = ad + a_up;
-                  umma_bf16(du, au, bd, idesc, acc);
-                  umma_bf16(du, au + 2, bd + 2, idesc, 1u);
-                  umma_bf16(du, au + 4, bd + 4, idesc, 1u);
-                  umma_bf16(du, au + 6, bd + 6, idesc, 1u);
+        for (int i = 0; i < nkp; ++i) {
+          const int a0 = i * KP, a1 = min(nat, a0 + KP);
+          const uint32_t buf = (kp0 + i) & 1u, use = (kp0 + i) >> 1;
+          const bool bok = wait_bar(&bready[buf], use & 1u, p);
+          if (tr && g0 == in.a && a0 == 0) tr[5] = global_timer();
+          const uint64_t bd0 = umma_desc(smem_u32(act + buf * kTcBBytes));
+          const uint64_t b_atom = (uint64_t)((nc * 128) >> 4);
+          int col = 0;
+          for (int r = g0; r < g1;) {
+            PkBlock blk;
+            r = pk_block(op, r, g1, blk);
+            const uint64_t a_atom = (uint64_t)((blk.P * 128) >> 4);
+            const uint64_t a_up = (uint64_t)((blk.rows8 * 128) >> 4);  // SwiGLU: the up rows follow the gate rows
+            const uint32_t dg = ts.tmem + (uint32_t)col, du = dg + (uint32_t)nc;
+            for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
+              const int na = min(blk.atoms, a1 - c0);
+              const bool ok = ring_wait_full(rg, ck, p) && bok;
+              if (tr && ck == chunk) tr[6] = global_timer();
+              tc_fence_after();
+              if (ok) {
+                uint64_t ad = umma_desc(ring_s + (ck % kSlots) * kSlotBytes);
+                uint64_t bd = bd0 + (uint64_t)(c0 - a0) * b_atom;
+                uint32_t acc = c0 > 0 ? 1u : 0u;  // the group's first MMA starts its accumulators
+                for (int a = 0; a < na; ++a, ad += a_atom, bd += b_atom) {
+                  umma_bf16(dg, ad, bd, idesc, acc);
+                  umma_bf16(dg, ad + 2, bd + 2, idesc, 1u);
+                  umma_bf16(dg, ad + 4, bd + 4, idesc, 1u);
+                  umma_bf16(dg, ad + 6, bd + 6, idesc, 1u);
+                  if (tiles == 2) {
+                    const uint64_t au = ad + a_up;
+                    umma_bf16(du, au, bd, idesc, acc);
+                    umma_bf16(du, au + 2, bd + 2, idesc, 1u);
+                    umma_bf16(du, au + 4, bd + 4, idesc, 1u);
+                    umma_bf16(du, au + 6, bd + 6, idesc, 1u);
+                  }
+                  acc = 1u;
                 }
-                acc = 1u;
               }
-            }
-            // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
-            __syncwarp();
-            if (lane == 0) {
+              // the slot is free once these MMAs have read it: 7 arrivals now, the 8th from the commit
               mbar_arrive_n(&rg.empty[ck % kSlots], kConsumerWarps - 1);
               umma_commit(&rg.empty[ck % kSlots]);
+              ++ck;
             }
-            ++ck;
+            col += tiles * nc;
           }
-          col += tiles * nc;
+          umma_commit(&bfree[buf]);
+          if (tr) tr[7] = global_timer();
         }
-        if (lane == 0) umma_commit(&bfree[buf]);
-        if (tr && lane == 0) tr[7] = global_timer();
-        __syncwarp();
+        umma_commit(accb);
       }
-      ++ts.kp;
+      __syncwarp();
     }
-    if (ctid == 0) umma_commit(accb);
+    ts.kp = kp0 + (uint32_t)nkp;
     wait_bar(accb, ts.rg & 1u, p);
     ++ts.rg;
     tc_fence_after();
@@ -1367,37 +1373,59 @@ __device__ MK_OUTLINE void delta_consume(const KParams& p, const OpDesc& op, con
       for (int e = 0; e < 4; ++e) S[c][e] = (e < E && j < dv) ? __ldcg(Sp + c * dk + e) : 0.f;
     }
   }
-  for (int i = ctid; i < R * dk; i += kConsumerThreads) {
-    const int r = i / dk, e = i % dk;
-    const float* row = op.in + (size_t)(b * R + r) * op.in_stride;
-    sq_[i] = __ldcg(row + h * dk + e);
-    sk_[i] = __ldcg(row + offk + h * dk + e);
-    if (kda) sa_[i] = sigmoidf_(__ldcg(row + offa + h * dk + e));
-  }
-  for (int i = ctid; i < R * C; i += kConsumerThreads) {
-    const int r = i / C, c = i % C;
-    const float* row = op.in + (size_t)(b * R + r) * op.in_stride;
-    sv_[i] = (j0 + c < dv) ? __ldcg(row + offv + h * dv + j0 + c) : 0.f;
-  }
-  if (ctid < R) {
-    const float* row = op.in + (size_t)(b * R + ctid) * op.in_stride;
-    if (!kda) sa_[ctid] = sigmoidf_(__ldcg(row + offa + h));
-    sb_[ctid] = sigmoidf_(__ldcg(row + offb + h));
-  }
-  for (int i = ctid; i < a * dk; i += kConsumerThreads) {
-    const int r = i / dk, e = i % dk;
-    const float* pr = pend_at(prev, r);
-    pk_[i] = __ldcg(pr + e);
-    if (kda) pa_[i] = __ldcg(pr + dk + dv + e);
-  }
-  for (int i = ctid; i < a * C; i += kConsumerThreads) {
-    const int r = i / C, c = i % C;
-    pv_[i] = (j0 + c < dv) ? __ldcg(pend_at(prev, r) + dk + j0 + c) : 0.f;
-  }
-  if (ctid < a) {
-    const float* pr = pend_at(prev, ctid);
-    if (!kda) pa_[ctid] = __ldcg(pr + dk + dv);
-    pb_[ctid] = __ldcg(pr + 2 * dk + dv);
+  // All staged values in one flat index space laid out like the staging area (stage[i] is item i), loaded in
+  // rounds of 4 per thread: one round trip for the usual 1 to 2 items a thread stages. dk and C are powers of 2.
+  const int ldk = __ffs(dk) - 1, lc = __ffs(C) - 1;
+  const int e0 = R * dk, e1 = 2 * R * dk, e2 = e1 + R * na, e3 = e2 + R, e4 = e3 + R * C;
+  const int e5 = e4 + a * dk, e6 = e5 + a * na, e7 = e6 + a, e8 = e7 + a * C;
+  // source of item i (nullptr: zero); the gate sigmoid applies to items [e1, e3)
+  auto item_src = [&](int i) -> const float* {
+    if (i < e3) {  // new rows: q, k, alpha, beta from the projection output
+      int r, off;
+      if (i < e1) {
+        const int j = i < e0 ? i : i - e0;
+        r = j >> ldk;
+        off = (i < e0 ? 0 : offk) + h * dk + (j & (dk - 1));
+      } else {
+        const int j = i < e2 ? i - e1 : i - e2;
+        if (i < e2 && kda) {
+          r = j >> ldk;
+          off = offa + h * dk + (j & (dk - 1));
+        } else {
+          r = j;
+          off = (i < e2 ? offa : offb) + h;
+        }
+      }
+      return op.in + (size_t)(b * R + r) * op.in_stride + off;
+    }
+    if (i < e4) {  // new rows: v of this instruction's columns
+      const int j = i - e3, c = j & (C - 1);
+      return j0 + c < dv ? op.in + (size_t)(b * R + (j >> lc)) * op.in_stride + offv + h * dv + j0 + c : nullptr;
+    }
+    if (i < e7) {  // accepted rows: k_hat, alpha, beta from the pending store
+      if (i < e5) return pend_at(prev, (i - e4) >> ldk) + ((i - e4) & (dk - 1));
+      if (i < e6) {
+        const int j = i - e5;
+        return kda ? pend_at(prev, j >> ldk) + dk + dv + (j & (dk - 1)) : pend_at(prev, j) + dk + dv;
+      }
+      return pend_at(prev, i - e6) + 2 * dk + dv;
+    }
+    const int j = i - e7, c = j & (C - 1);  // accepted rows: v
+    return j0 + c < dv ? pend_at(prev, j >> lc) + dk + j0 + c : nullptr;
+  };
+  for (int i0 = ctid; i0 < e8; i0 += 4 * kConsumerThreads) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      const float* src = i < e8 ? item_src(i) : nullptr;
+      v[u] = src ? __ldcg(src) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kConsumerThreads;
+      if (i < e8) stage[i] = (i >= e1 && i < e3) ? sigmoidf_(v[u]) : v[u];
+    }
   }
   consumer_sync();
 
@@ -2563,8 +2591,10 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
         if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         else if (op.col_group == 32) delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-        else if (op.col_group == 64) delta_consume<8>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-        else delta_consume<16>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        else if constexpr (!kFull) {  // (the full build's column groups stop at 32)
+          if (op.col_group == 64) delta_consume<8>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+          else delta_consume<16>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
+        }
         break;
       case OP_FINAL: final_consume(p, cs, step, ctid); break;
       default: break;
