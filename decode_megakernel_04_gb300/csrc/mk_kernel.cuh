@@ -2601,7 +2601,8 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
     }
     consumer_sync();
     if (ctid == 0 && (op.type != OP_FINAL || step + 1 < p.n_steps)) {
-      __threadfence();
+      // the release add orders every consumer thread's writes before it: they precede the barrier above, and a
+      // release is cumulative over what its thread has synchronised with (a separate fence measured slower)
       red_release_add(&p.counters[in.op], 1u);
     }
     if (ctid == 0 && trace && step == 0) p.trace[(size_t)qi * kTraceWords + 2] = global_timer();
