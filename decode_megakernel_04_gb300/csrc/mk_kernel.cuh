@@ -435,18 +435,16 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
   const int K = op.K, N = p.N, Kp = tc_atoms(op) * 64, cp = Kp + 8;
   const int total4 = N * Kp / 4;
   const int rounds = (total4 + kConsumerThreads * kBatch - 1) / (kConsumerThreads * kBatch);
-  for (int rd = 0; rd < rounds; ++rd) {
-    const int i0 = rd * kConsumerThreads * kBatch + ctid;
-    float4 v[kBatch];
-    uint2 g[kBatch];
+  // item i = 4 consecutive inputs of activation row n at column k (N <= 4: no division)
+  auto load = [&](int rd, float4 (&v)[kBatch], uint2 (&g)[kBatch]) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kConsumerThreads;
+      const int i = rd * kConsumerThreads * kBatch + ctid + u * kConsumerThreads;
       v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       g[u] = make_uint2(0u, 0u);
       if (i < total4) {
         const int e = i * 4;
-        const int n = (e >= Kp) + (e >= 2 * Kp) + (e >= 3 * Kp), k = e - n * Kp;  // N <= 4: no division
+        const int n = (e >= Kp) + (e >= 2 * Kp) + (e >= 3 * Kp), k = e - n * Kp;
         if (k < K) {
           const float* src =
               norm ? p.x + (size_t)n * p.d + op.k_begin + k : op.in + (size_t)n * op.in_stride + op.k_begin + k;
@@ -455,13 +453,23 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
         }
       }
     }
-    if (norm && rd == 0) {
-      inv_rms_rows(p, op.ssq_in, op.ldw, cs, ctid >> 5, ctid & 31);
-      consumer_sync();
-    }
+  };
+  float4 v[kBatch];
+  uint2 g[kBatch];
+  load(0, v, g);
+  if (norm) {
+    inv_rms_rows(p, op.ssq_in, op.ldw, cs, ctid >> 5, ctid & 31);
+    consumer_sync();
+  }
+  // the loads of round rd + 1 are in flight while round rd is converted
+#pragma unroll 1
+  for (int rd = 0; rd < rounds; ++rd) {
+    float4 w[kBatch];
+    uint2 h[kBatch];
+    load(rd + 1, w, h);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kConsumerThreads;
+      const int i = rd * kConsumerThreads * kBatch + ctid + u * kConsumerThreads;
       if (i >= total4) break;
       const int e = i * 4;
       const int n = (e >= Kp) + (e >= 2 * Kp) + (e >= 3 * Kp), k = e - n * Kp;
@@ -484,6 +492,11 @@ __device__ __forceinline__ void stage_hilo(const KParams& p, const OpDesc& op, C
           make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
       *reinterpret_cast<uint2*>(cols + (size_t)(N + n) * cp + k) =
           make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      v[u] = w[u];
+      g[u] = h[u];
     }
   }
 }
@@ -656,7 +669,7 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
         if (ov > best_v || (ov == best_v && oi < best_i)) { best_v = ov; best_i = oi; }
       }
     }
-    consumer_sync();
+    // (cs.red is not used earlier in this instruction, so each warp writes its row without a barrier)
     if (lane < 4) {
       cs.red[warp][lane] = op.out_kind == OUT_RESID ? ssq_acc : best_v;
       cs.red[warp][4 + lane] = __int_as_float(best_i);
@@ -678,6 +691,9 @@ __device__ __noinline__ void gemv_mma_consume(const KParams& p, const OpDesc& op
         p.amax_part[(size_t)sm * kMaxN + ctid] = make_float2(bv, __int_as_float(bi));
       }
     }
+    // the instruction's last writes are warp 0's (N <= 4): ordered before its lane 0's completion signal, which
+    // therefore needs no block barrier after this handler
+    if (warp == 0) __syncwarp();
   }
 }
 
@@ -2599,7 +2615,10 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
       case OP_FINAL: final_consume(p, cs, step, ctid); break;
       default: break;
     }
-    consumer_sync();
+    // every thread's writes must precede the completion signal; an mma.sync GEMV with a residual or logits
+    // output ends with a barrier and warp-0-only writes of its own, so it skips this one
+    if (!(op.type == OP_GEMV && op.mma != 2 && (op.out_kind == OUT_RESID || op.out_kind == OUT_LOGITS)))
+      consumer_sync();
     if (ctid == 0 && (op.type != OP_FINAL || step + 1 < p.n_steps)) {
       // the release add orders every consumer thread's writes before it: they precede the barrier above, and a
       // release is cumulative over what its thread has synchronised with (a separate fence measured slower)
