@@ -782,10 +782,12 @@ mk_status construct_program(mk_handle* h, int B, int R, bool head, HostProgram& 
       dl.dk = dk;
       dl.dv = dv;
       dl.per_channel_decay = kda ? 1 : 0;
-      // value columns per instruction: 8 to 128 (1 to 16 per warp), the fewest that keep the instruction
-      // count within one per SM (one instruction costs a few dependent memory round trips, whatever its width)
-      // (the full build of the kernel, with the MLA / MoE handlers, gives this handler fewer registers: up to 32)
-      const int cw_max = h->full_ops ? 4 : 16;
+      // value columns per instruction: 8 to 64 (1 to 8 per warp), the fewest that keep the instruction
+      // count within one per SM (one instruction costs a few dependent memory round trips, whatever its width);
+      // 16 columns per warp measured slower than 8 at batch 8 (their serial per-row work outweighs the
+      // fewer instructions). The full build of the kernel, with the MLA / MoE handlers, gives this handler
+      // fewer registers: up to 32 columns there.
+      const int cw_max = h->full_ops ? 4 : 8;
       int cw = 1;
       while (cw < cw_max && (int64_t)B * H * ((dv + kConsumerWarps * cw - 1) / (kConsumerWarps * cw)) > h->n_sm) cw *= 2;
       dl.col_group = kConsumerWarps * cw;

@@ -2607,10 +2607,8 @@ __device__ void run_consumer(const KParams& p, const Ring& rg, CSmem& cs, uint16
         if (op.col_group == 8) delta_consume<1>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         else if (op.col_group == 16) delta_consume<2>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         else if (op.col_group == 32) delta_consume<4>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-        else if constexpr (!kFull) {  // (the full build's column groups stop at 32)
-          if (op.col_group == 64) delta_consume<8>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-          else delta_consume<16>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
-        }
+        else if constexpr (!kFull)  // (the full build's column groups stop at 32)
+          delta_consume<8>(p, op, in, cs, reinterpret_cast<float*>(act), step, ctid);
         break;
       case OP_FINAL: final_consume(p, cs, step, ctid); break;
       default: break;
