@@ -313,11 +313,30 @@ __device__ __forceinline__ const uint8_t* pk_block_src(const OpDesc& op, int sta
   return op.wp + (size_t)start * per_row + (size_t)op.pa0 * blk.P * 128;
 }
 
-// end of the tcgen05 row group that starts at `start` (as many blocks as fit the TMEM columns)
+// K stacking of a tcgen05 block: with P <= 64 physical rows, one M = 128 MMA reads s = 128 / P consecutive
+// atoms of the block (atom a + q lands in TMEM lanes q*P ..), and an N = 16 s operand reads the activations of
+// the same s atoms (columns 16 q ..): the diagonal blocks (lanes q*P + r, columns 16 q ..) are row r's partial
+// sums over atom a + q, the rest is discarded. This takes s atoms per MMA instead of one. Used for
+// non-SwiGLU ops with 16 activation columns (up to 8 rows), at most 4 segments.
+__device__ __forceinline__ int tc_stack(const OpDesc& op, const PkBlock& blk) {
+  if (op.out_kind == OUT_SWIGLU || op.ncols != 16) return 1;
+  return max(1, min(min(4, 128 / blk.P), (op.K + 63) >> 6));
+}
+
+// end of the tcgen05 row group that starts at `start`: as many blocks as fit the TMEM columns (a block takes
+// ncols per tile, times its K-stacking factor)
 __device__ __forceinline__ int tc_group_end(const OpDesc& op, int start, int end) {
   const int tiles = op.out_kind == OUT_SWIGLU ? 2 : 1;
-  const int blocks = max(1, kTcCols / (tiles * op.ncols));
-  return min(end, start + blocks * pk_block_lrows(tiles - 1));
+  int cols = 0, r = start;
+  while (r < end) {
+    PkBlock blk;
+    const int e = pk_block(op, r, end, blk);
+    const int c = tiles * op.ncols * tc_stack(op, blk);
+    if (r > start && cols + c > kTcCols) break;
+    cols += c;
+    r = e;
+  }
+  return r;
 }
 
 __device__ __forceinline__ int tc_atoms(const OpDesc& op) { return (op.K + 63) >> 6; }
@@ -885,6 +904,8 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             const uint64_t a_atom = (uint64_t)((blk.P * 128) >> 4);
             const uint64_t a_up = (uint64_t)((blk.rows8 * 128) >> 4);  // SwiGLU: the up rows follow the gate rows
             const uint32_t dg = ts.tmem + (uint32_t)col, du = dg + (uint32_t)nc;
+            const int st = tc_stack(op, blk);
+            const uint32_t idesc_st = umma_idesc(nc * st);
             for (int c0 = a0; c0 < a1; c0 += blk.atoms) {
               const int na = min(blk.atoms, a1 - c0);
               const bool ok = ring_wait_full(rg, ck, p) && bok;
@@ -893,8 +914,20 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
               if (ok) {
                 uint64_t ad = umma_desc(ring_s + (ck % kSlots) * kSlotBytes);
                 uint64_t bd = bd0 + (uint64_t)(c0 - a0) * b_atom;
-                uint32_t acc = c0 > 0 ? 1u : 0u;  // the group's first MMA starts its accumulators
-                for (int a = 0; a < na; ++a, ad += a_atom, bd += b_atom) {
+                // the block's first MMA starts its accumulators: stacked, so that it covers all 16 st columns
+                // (the first chunk of a block always holds st atoms or more)
+                uint32_t acc = c0 > 0 ? 1u : 0u;
+                int a = 0;
+                if (st > 1) {
+                  for (; a + st <= na; a += st, ad += st * a_atom, bd += st * b_atom) {
+                    umma_bf16(dg, ad, bd, idesc_st, acc);
+                    umma_bf16(dg, ad + 2, bd + 2, idesc_st, 1u);
+                    umma_bf16(dg, ad + 4, bd + 4, idesc_st, 1u);
+                    umma_bf16(dg, ad + 6, bd + 6, idesc_st, 1u);
+                    acc = 1u;
+                  }
+                }
+                for (; a < na; ++a, ad += a_atom, bd += b_atom) {
                   umma_bf16(dg, ad, bd, idesc, acc);
                   umma_bf16(dg, ad + 2, bd + 2, idesc, 1u);
                   umma_bf16(dg, ad + 4, bd + 4, idesc, 1u);
@@ -914,7 +947,7 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
               umma_commit(&rg.empty[ck % kSlots]);
               ++ck;
             }
-            col += tiles * nc;
+            col += tiles * nc * st;
           }
           umma_commit(&bfree[buf]);
           if (tr) tr[7] = global_timer();
@@ -931,19 +964,75 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
     // epilogue: warp w reads TMEM lanes 32 (w & 3) .. + 31 (rows of a tile), columns half (w >> 2) of each tile
     const int q = warp & 3, half = warp >> 2;
     const int hc = nc >> 1;  // columns per half (hi / lo pairs: hc / 2 activation rows)
+    // value `val` of output row `row` for activation row n (store, residual + RMS partial, or logits + argmax);
+    // every lane of the warp calls it with the same n
+    auto emit = [&](int row, int n, float val, bool live) {
+      if (op.out_kind == OUT_STORE) {
+        if (live) op.out[(size_t)n * op.out_stride + row] = val;
+      } else if (op.out_kind == OUT_RESID) {
+        float xn = 0.f;
+        if (live) {
+          xn = __ldcg(p.x + (size_t)n * p.d + row) + val;
+          __stcg(p.x + (size_t)n * p.d + row, xn);
+        }
+        const float s2 = warp_sum(xn * xn);
+        if (lane == 0 && n < N) pred[warp * 64 + n] += s2;
+      } else {  // OUT_LOGITS
+        if (live && p.logits) p.logits[(size_t)n * p.V + row] = val;
+        float bv = live ? val : -CUDART_INF_F;
+        int bi = live ? row : 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0 && n < N) {
+          const float cv = pred[warp * 64 + n];
+          const int ci = pidx[warp * 64 + n];
+          if (bv > cv || (bv == cv && bi < ci)) { pred[warp * 64 + n] = bv; pidx[warp * 64 + n] = bi; }
+        }
+      }
+    };
     int col = 0;
     for (int r = g0; r < g1;) {
       PkBlock blk;
       const int r0 = r;
       r = pk_block(op, r, g1, blk);
-      {
+      const int st = tc_stack(op, blk);
+      if (st > 1) {
+        // K-stacked block (16 columns a segment, N <= 8): lane m = qs*P + rr holds segment qs's partial of row rr
+        // in columns 16 qs ..; each lane keeps its own segment's 4 values of this warp's half in shared memory,
+        // then the segments are summed per (row, activation row)
+        const int P = blk.P;
+        float* part = cs.mred + kConsumerWarps * 64;  // [st * P][8], after the argmax index partials
+        const int m = q * 32 + lane, qs = m / P;
+        for (int qq = 0; qq < st; ++qq) {
+          float v[8];
+          tmem_ld8(ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + qq * nc + half * 8), v);
+          if (qs == qq) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) part[m * 8 + half * 4 + t] = v[2 * t] + v[2 * t + 1];
+          }
+        }
+        consumer_sync();
+        const int n = warp;  // one activation row a warp
+        for (int rb = 0; rb < blk.rows; rb += 32) {
+          const int rr = rb + lane;
+          const bool live = rr < blk.rows && n < N;
+          float val = 0.f;
+          if (live)
+            for (int qq = 0; qq < st; ++qq) val += part[(qq * P + rr) * 8 + n];
+          emit(r0 + rr, n, val, live);
+        }
+        consumer_sync();  // the partials are rewritten by the next stacked block
+      } else {
         // lane i of the tile is the block's row i
-        const int s = 0;
         const int i = q * 32 + lane;
         const bool valid = i < blk.rows;
         const int row = r0 + i;
         for (int pc = 0; pc < hc; pc += 8) {
-          const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + s * nc + half * hc + pc);
+          const uint32_t ta = ts.tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(col + half * hc + pc);
           float v[8], u[8];
           tmem_ld8(ta, v);
           if (swiglu) tmem_ld8(ta + (uint32_t)nc, u);
@@ -955,36 +1044,13 @@ __device__ __noinline__ void gemv_tc_consume(const KParams& p, const OpDesc& op,
             if (swiglu) {
               const float up = u[2 * t] + u[2 * t + 1];
               if (live) op.out[(size_t)n * op.out_stride + row] = val / (1.0f + expf(-val)) * up;
-            } else if (op.out_kind == OUT_STORE) {
-              if (live) op.out[(size_t)n * op.out_stride + row] = val;
-            } else if (op.out_kind == OUT_RESID) {
-              float xn = 0.f;
-              if (live) {
-                xn = __ldcg(p.x + (size_t)n * p.d + row) + val;
-                __stcg(p.x + (size_t)n * p.d + row, xn);
-              }
-              const float s2 = warp_sum(xn * xn);
-              if (lane == 0 && n < N) pred[warp * 64 + n] += s2;
-            } else {  // OUT_LOGITS
-              if (live && p.logits) p.logits[(size_t)n * p.V + row] = val;
-              float bv = live ? val : -CUDART_INF_F;
-              int bi = live ? row : 0x7fffffff;
-#pragma unroll
-              for (int o = 16; o >= 1; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-              }
-              if (lane == 0 && n < N) {
-                const float cv = pred[warp * 64 + n];
-                const int ci = pidx[warp * 64 + n];
-                if (bv > cv || (bv == cv && bi < ci)) { pred[warp * 64 + n] = bv; pidx[warp * 64 + n] = bi; }
-              }
+            } else {
+              emit(row, n, val, live);
             }
           }
         }
       }
-      col += (swiglu ? 2 : 1) * nc;
+      col += (swiglu ? 2 : 1) * nc * st;
     }
     tc_fence_before();
     consumer_sync();  // TMEM reads done before the next row group's MMAs overwrite the tiles

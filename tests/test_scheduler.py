@@ -68,13 +68,27 @@ def walk_chunks(o, instrs, packed_groups):
     KP = 256 // o["ncols"] if tc else nat
     per_group = packed_groups.setdefault(o["pk_offset"], {"bytes": (-(-o["rows"] // 8) * 8) * A * 128 * (1 + sw),
                                                           "ranges": []})
+    def group_end(g0, b):
+        # as many blocks as fit 512 TMEM columns: ncols per tile, times the block's K-stacking factor (up to 4
+        # atoms per MMA for non-SwiGLU blocks of at most 64 rows with 16 activation columns)
+        cols, r = 0, g0
+        while r < b:
+            e = min(b, r + br)
+            P = (-(-(e - r) // 8) * 8) << sw
+            st = 1 if (sw or o["ncols"] != 16) else max(1, min(4, 128 // P, nat))
+            c = (1 + sw) * o["ncols"] * st
+            if r > g0 and cols + c > 512:
+                break
+            cols, r = cols + c, e
+        return r
+
     for x in instrs:
         a, b = x["a"], x["b"]
         if b <= a:
             continue
         g0 = a
         while g0 < b:
-            g1 = min(b, g0 + (max(1, 512 // ((1 + sw) * o["ncols"])) if tc else 1) * br)
+            g1 = group_end(g0, b) if tc else min(b, g0 + br)
             for a0 in range(0, nat, KP):
                 r = g0
                 while r < g1:
