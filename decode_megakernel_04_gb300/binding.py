@@ -186,6 +186,8 @@ def model_desc(cfg, max_batch: int, max_rows: int, max_ctx: int) -> ModelDesc:
               "kv_lora", "qk_nope", "qk_rope", "v_head", "ffn_dim", "n_experts", "top_k", "n_shared", "expert_dim"):
         setattr(d, f, int(getattr(cfg, f)))
     d.ffn_kind = 0 if cfg.ffn == "dense" else 1
+    if cfg.expert_fmt not in ("bf16", "nvfp4"):
+        raise ValueError(f"expert format {cfg.expert_fmt!r} has no kernel path (bf16 and nvfp4 do)")
     d.expert_format = 0 if cfg.expert_fmt == "bf16" else 1
     d.route_scale = cfg.route_scale
     d.max_batch, d.max_rows, d.max_ctx = max_batch, max_rows, max_ctx

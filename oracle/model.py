@@ -113,8 +113,13 @@ class Oracle:
             return self.w[name][e]
         key = (name, e)
         if key not in self._dequant_cache:
-            self._dequant_cache[key] = ops.nvfp4_decode(
-                self.w[name + ".q"][e], self.w[name + ".s"][e], float(self.w[name + ".g"][e]))
+            if self.cfg.expert_fmt == "nvfp4":
+                self._dequant_cache[key] = ops.nvfp4_decode(
+                    self.w[name + ".q"][e], self.w[name + ".s"][e], float(self.w[name + ".g"][e]))
+            elif mat == "down":  # "f4": MXFP4 down projection
+                self._dequant_cache[key] = ops.mxfp4_decode(self.w[name + ".q"][e], self.w[name + ".x"][e])
+            else:  # "f4": FP8-E4M3 gate / up with one bf16 scale per 256 rows
+                self._dequant_cache[key] = ops.fp8_rows_decode(self.w[name + ".f8"][e], self.w[name + ".f8s"][e])
         return self._dequant_cache[key]
 
     # ------------------------------------------------------------------------------------------

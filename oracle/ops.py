@@ -2,7 +2,7 @@
 
 Citations name the page and section of the source material. The pages name the operations
 (RMSNorm, residual, grouped-query attention, MLA with a 576-wide latent, the KDA / gated-delta-net
-recurrence, sigmoid top-k routing, SwiGLU experts, NVFP4 experts) but print almost no formulas, so
+recurrence, sigmoid top-k routing, SwiGLU experts, NVFP4 and MXFP4 / FP8-E4M3 experts) but print almost no formulas, so
 most definitions below are the plainest standard reading of those names; each says which.
 """
 from __future__ import annotations
@@ -224,6 +224,43 @@ def e4m3_value(bits: np.ndarray) -> np.ndarray:
     mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, np.exp2(e - 7.0) * (1.0 + m / 8.0))
     mag = np.where((e == 15) & (m == 7), np.nan, mag)
     return sign * mag
+
+
+def e8m0_value(bits: np.ndarray) -> np.ndarray:
+    """Value of an E8M0 scale byte (the microscaling formats' shared scale): 2^(bits - 127); 0xFF is NaN.
+    Pinned by its closed forms (1, 2, 2^-127, 2^127, NaN)."""
+    b = np.asarray(bits).astype(np.int64)
+    return np.where(b == 255, np.nan, np.exp2(b - 127.0))
+
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    """Value of a bfloat16 bit pattern (the high half of a float32). Pinned against torch's bfloat16."""
+    b = (np.asarray(bits).astype(np.int64) & 0xFFFF).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(F64)
+
+
+def mxfp4_decode(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Decode MXFP4 weights [..., K] from packed e2m1 codes q [..., K/2] (element 2i in the low nibble) and
+    E8M0 block scales s [..., K/32]: w = e2m1(code) * 2^(s - 127). The down projection of the pages' own
+    expert format is MXFP4 (Kimi K3's TPU megakernel, "How it maps onto a TPU v7"); blocks of 32 along the
+    input axis with an E8M0 scale are the microscaling format's definition.
+    Pinned: a hand-built block, the encoder's grid round trip, and the FP8 re-encoding's exactness."""
+    q = np.asarray(q, dtype=np.uint8)
+    codes = np.stack([q & 0x0F, q >> 4], axis=-1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    return e2m1_value(codes) * np.repeat(e8m0_value(s), 32, axis=-1)
+
+
+def fp8_rows_decode(codes: np.ndarray, scale_bits: np.ndarray, rows_per_scale: int = 256) -> np.ndarray:
+    """Decode FP8-E4M3 gate / up weights [rows, K] from their e4m3 codes and one bf16 scale per
+    ``rows_per_scale`` consecutive rows: w[r, k] = e4m3(codes[r, k]) * bf16(scale_bits[r // 256]) (the
+    loader's re-encoding of the MXFP4 gate / up projections: Kimi K3's TPU megakernel, "How it maps onto a
+    TPU v7"; "rows" read as the matrix's output rows).
+    Pinned: rows 255 and 256 take different scales in a hand-built case; decodes the re-encoder's output
+    to the MXFP4 values bit for bit."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    rows = codes.shape[0]
+    scale = bf16_value(scale_bits)[np.arange(rows) // rows_per_scale]
+    return e4m3_value(codes) * scale[:, None]
 
 
 def nvfp4_decode(q: np.ndarray, s: np.ndarray, g: float) -> np.ndarray:

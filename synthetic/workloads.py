@@ -4,7 +4,9 @@ Every tensor is drawn from its own ``torch.Generator`` whose seed is a hash of (
 so any tensor can be regenerated alone and the draw does not depend on generation order.
 Draws are N(0, init_std) in fp32, rounded to bf16 round-to-nearest-even by ``Tensor.to``.
 Norm gains are 1. Expert weights of NVFP4 models are drawn the same way and then encoded by
-``synthetic.nvfp4.quantize_nvfp4``.
+``synthetic.nvfp4.quantize_nvfp4``; those of the "f4" format (the pages' own: FP8-E4M3 gate / up with a
+bf16 scale per 256 rows, MXFP4 down) are encoded to MXFP4 by ``synthetic.mxfp4.quantize_mxfp4`` and the
+gate / up re-encoded by ``synthetic.mxfp4.reencode_fp8_rows``.
 
 Draws on "cuda" and on "cpu" differ for the same seed (different generators); a test that compares
 the two paths generates once, on one device, and hands copies of the same tensors to both.
@@ -18,6 +20,7 @@ from dataclasses import dataclass, field
 import torch
 
 from .nvfp4 import quantize_nvfp4_experts
+from .mxfp4 import quantize_mxfp4, reencode_fp8_rows
 
 
 @dataclass(frozen=True)
@@ -55,7 +58,7 @@ class ModelConfig:
     expert_dim: int = 0
     route_scale: float = 1.0
     router_bias_std: float = 0.0
-    expert_fmt: str = "bf16"  # "bf16" | "nvfp4"
+    expert_fmt: str = "bf16"  # "bf16" | "nvfp4" | "f4" (FP8-E4M3 gate / up + MXFP4 down; oracle only)
 
     def with_layers(self, n_layers: int) -> "ModelConfig":
         """Same widths, fewer (or more) layers; the mixer pattern is re-derived."""
@@ -192,7 +195,10 @@ _EXPERT = ("e_gate", "e_up", "e_down", "s_gate", "s_up", "s_down")
 def make_weights(cfg: ModelConfig, seed: int = 0, device="cpu") -> dict[str, torch.Tensor]:
     """Draw every weight of ``cfg``. bf16 tensors keep their logical shape; NVFP4 expert
     tensors become ``<name>.q`` (uint8, two e2m1 codes per byte, element 2i in the low nibble),
-    ``<name>.s`` (uint8 e4m3 bits, one per 16 inputs) and ``<name>.g`` (fp32, one per expert)."""
+    ``<name>.s`` (uint8 e4m3 bits, one per 16 inputs) and ``<name>.g`` (fp32, one per expert). In the
+    "f4" format a down projection becomes ``<name>.q`` (packed e2m1 codes) and ``<name>.x`` (uint8 E8M0,
+    one per 32 inputs); a gate / up projection ``<name>.f8`` (uint8 e4m3 codes, one per weight) and
+    ``<name>.f8s`` (int32 holding bf16 bits, one per 256 rows)."""
     out: dict[str, torch.Tensor] = {}
     for name, shape in weight_names(cfg).items():
         leaf = name.rsplit(".", 1)[-1]
@@ -217,6 +223,17 @@ def make_weights(cfg: ModelConfig, seed: int = 0, device="cpu") -> dict[str, tor
             out[name + ".q"] = torch.cat(qs)
             out[name + ".s"] = torch.cat(ss)
             out[name + ".g"] = torch.cat(gs).to(torch.float32)
+        elif leaf in _EXPERT and cfg.expert_fmt == "f4":
+            # MXFP4 as shipped; gate / up re-encoded to e4m3 codes with one bf16 scale per 256 rows
+            enc = [quantize_mxfp4(_bf16(shape[1:], seed, f"{name}.{e}", cfg.init_std, device).float())
+                   for e in range(shape[0])]
+            if leaf.endswith("_down"):
+                out[name + ".q"] = torch.stack([q for q, _ in enc])
+                out[name + ".x"] = torch.stack([x for _, x in enc])
+            else:
+                f8 = [reencode_fp8_rows(q, x) for q, x in enc]
+                out[name + ".f8"] = torch.stack([c for c, _ in f8])
+                out[name + ".f8s"] = torch.stack([sb for _, sb in f8])
         elif leaf in _EXPERT:
             out[name] = torch.stack(
                 [_bf16(shape[1:], seed, f"{name}.{e}", cfg.init_std, device) for e in range(shape[0])])
