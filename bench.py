@@ -146,14 +146,19 @@ class Clocks:
 
 
 def dist_setup(args):
+    """One process per GPU under torchrun (NCCL); the same host logic runs over gloo on a machine without a
+    GPU, which is how the multi-rank path is tested."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return ws, rank, local
 
 
@@ -168,9 +173,15 @@ def max_over_ranks(v: float, ws: int) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(ws: int, units_per_rank: float, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank (every rank runs the same replica work)."""
+    return ws * units_per_rank / seconds
 
 
 # ------------------------------------------------------------------------------------------------
@@ -411,7 +422,7 @@ class ModelBench:
             mk.step_host(tk, np.full(B, self.T + s, dtype=np.int32), am, stream=self.sh)
             tk = am.reshape(B, 1).copy()
         dt = max_over_ranks((time.perf_counter() - t0) / K, ws)
-        return {"value": ws * B / dt, "unit": "tokens/s", "h2d_bytes_per_step": int(4 * (B + B)),
+        return {"value": whole_job_rate(ws, B, dt), "unit": "tokens/s", "h2d_bytes_per_step": int(4 * (B + B)),
                 "d2h_bytes_per_step": int(4 * B), "ms_per_step": dt * 1e3,
                 "how": "mk_decode_step_host: token and position copied in, greedy token copied out, every step"}
 
@@ -447,8 +458,8 @@ class ModelBench:
         for s in range(W, W + K):
             mk.steps_host(tk, np.array([self.T + s * S], dtype=np.int32), S, o, stream=sh)
         dt = max_over_ranks((time.perf_counter() - t0) / K, ws)
-        return {"steps_per_launch": S, "ms_per_launch": ms, "tokens_per_s": ws * S / (ms * 1e-3),
-                "e2e_tokens_per_s": ws * S / dt, "e2e_ms_per_call": dt * 1e3, "h2d_bytes_per_call": 8,
+        return {"steps_per_launch": S, "ms_per_launch": ms, "tokens_per_s": whole_job_rate(ws, S, ms * 1e-3),
+                "e2e_tokens_per_s": whole_job_rate(ws, S, dt), "e2e_ms_per_call": dt * 1e3, "h2d_bytes_per_call": 8,
                 "d2h_bytes_per_call": 4 * S}
 
     def close(self):
@@ -462,7 +473,7 @@ def result_entry(model, B, R, acc, m, hbm, ws):
     ms = m["ms"]
     gbs = m["bytes"]["total"] / (ms * 1e-3) / 1e9
     e = {"workload": model, "batch": B, "rows": R, "mode": "verify" if R > 1 else "decode",
-         "ms_per_step": ms, "tokens_per_s": ws * B * (acc if R > 1 else 1) / (ms * 1e-3),
+         "ms_per_step": ms, "tokens_per_s": whole_job_rate(ws, B * (acc if R > 1 else 1), ms * 1e-3),
          "hbm_gbs": gbs, "frac": gbs / hbm, "frac_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
          "bytes_per_step": m["bytes"]["total"], "context": m["context"], "clocks": m["clocks"]}
     if R > 1:
@@ -544,7 +555,7 @@ def run_mk(args, wl, cfg):
         traffic = KNOWN_TRAFFIC[key][0]
     hwl = WORKLOADS_BY_MODEL(head_model, R)
     line = {
-        "metric": METRIC, "value": ws * B * (acc if R > 1 else 1) / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "metric": METRIC, "value": whole_job_rate(ws, B * (acc if R > 1 else 1), ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if hcfg.expert_fmt == "bf16" else "bf16+nvfp4", "data": "synthetic",
         "config": workload_config(hwl, hcfg, B, argparse.Namespace(accept=acc, context=T_head)),
