@@ -276,7 +276,8 @@ typedef struct mk_plan_op {
                           chunk, weight rows per group, activation passes                              */
   int32_t out_kind;    /* GEMV epilogue: store 0, residual 1, SwiGLU 2, logits 3                        */
   int32_t nchunk, groups, head_dim, n_heads, n_kv_heads, col_group;  /* attention / delta / MLA       */
-  int32_t ncols;       /* GEMV, tcgen05: TMEM columns per accumulator tile                             */
+  int32_t ncols;       /* GEMV, tcgen05: activation columns per tile (hi / lo pairs, 2 N rounded up to 16);
+                          a K-stacked block (P <= 64 rows, ncols 16) takes min(4, 128 / P) x ncols TMEM columns */
   int32_t pa0, patoms; /* GEMV: first packed atom (64 inputs) this op reads, atoms per packed row       */
   int64_t pk_offset;   /* GEMV: byte offset of the op's weight group in the packed copy                */
 } mk_plan_op;
